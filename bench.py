@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of the self-speculative decoding hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of the synthetic
+workload (Llama-3.1-8B attention shape, batch 128, context 32768, gamma 4 by
+default): SnapKV selection of the draft cache (window scores, max-pool, top-K,
+gather), gamma draft steps (draft attention over the compacted cache + draft
+token draw), verify attention over the full cache (gamma+1 rows), and
+rejection sampling.  The headline metric is verified tokens per second per
+layer (B * (gamma+1) per step); per-kernel KV-read GB/s and the HBM roofline
+fraction of the verify kernel are reported beside it.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--config 2|3|4]
+
+With --gpus N > 1 launch under torch.distributed.run: every rank runs the same
+batch on its own GPU (weak scaling, no collective on the data path); the
+timed region is bracketed by barriers and the max over ranks is reported.
+--impl reference times the float64 CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "verified tokens/s/layer and KV-read GB/s (% of GB300 HBM peak) at batch x ctx"
+UNIT = "tokens/s/layer"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", type=int, default=3, choices=[2, 3, 4])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=1, help="sequences in the oracle sample")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ peaks and clocks
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "mgd_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ the GPU workload
+class Workload:
+    def __init__(self, cid, device, seed=0):
+        from long_context_speculative_split_gb300 import mgd, ops
+        from long_context_speculative_split_gb300 import workloads as wl
+        self.ops, self.mgd, self.wl = ops, mgd, wl
+        c = self.cfg = wl.CONFIGS[cid]
+        self.dev = device
+        self.B, self.Hq, self.Hkv, self.D = c["B"], c["Hq"], c["Hkv"], c["D"]
+        self.gamma, self.K, self.W, self.P, self.V = c["gamma"], c["K"], c["W"], c["pool"], c["V"]
+        self.T = self.gamma + 1
+        self.kv_len = wl.lengths(c, seed)
+        self.cap = wl.capacity(c, seed)
+        self.kv_len_d = self.kv_len.to(device)
+        self.k, self.v = wl.kv_cache(c, device, seed, kv_len=self.kv_len, cap=self.cap)
+        self.q = wl.queries(c, device, seed)
+        self.qw = wl.window_queries(c, device, seed)
+        self.qd = torch.stack([wl.draft_queries(c, device, seed, step=s)[:, 0] for s in range(self.gamma)])
+        self.t, self.d = wl.logits(c, device, seed)
+        self.u = wl.uniforms(c, device, seed)
+        B, Hq, Hkv, D, K = self.B, self.Hq, self.Hkv, self.D, self.K
+        f32, i32 = torch.float32, torch.int32
+        self.sel = dict(sel_idx=torch.empty((B, Hkv, K), dtype=i32, device=device),
+                        k_draft=torch.zeros((B, Hkv, K, D), dtype=self.k.dtype, device=device),
+                        v_draft=torch.zeros((B, Hkv, K, D), dtype=self.k.dtype, device=device),
+                        draft_len=torch.empty((B,), dtype=i32, device=device), scores=None)
+        self.dout = torch.empty((B, Hq, D), dtype=f32, device=device)
+        self.dlse = torch.empty((B, Hq), dtype=f32, device=device)
+        self.vout = torch.empty((B, self.T, Hq, D), dtype=f32, device=device)
+        self.vlse = torch.empty((B, self.T, Hq), dtype=f32, device=device)
+        self.tok = torch.empty((B, self.gamma), dtype=i32, device=device)
+        self.out_tok = torch.empty((B, self.T), dtype=i32, device=device)
+        self.nacc = torch.empty((B,), dtype=i32, device=device)
+        ws = ops.workspace
+        self.ws_snap = ws(mgd.mgd_snapkv_workspace_size(B, Hq, Hkv, D, self.cap, self.W), device)
+        self.ws_draft = ws(mgd.mgd_draft_workspace_size(B, Hq, Hkv, D, K), device)
+        self.ws_verify = ws(mgd.mgd_verify_workspace_size(B, self.T, Hq, Hkv, D, self.cap), device)
+        self.ws_spec = ws(mgd.mgd_spec_workspace_size(B, self.gamma, self.V), device)
+        L = self.kv_len.double()
+        esz = self.k.element_size()
+        self.bytes_verify = float((2 * Hkv * L * D * esz).sum())
+        Keff = torch.clamp(L, max=K)
+        self.bytes_draft = float((2 * Hkv * Keff * D * esz).sum())
+        self.bytes_snap = float((2 * Hkv * L * D * esz).sum() + 4 * Hkv * Keff.sum() * D * esz)
+        self.bytes_spec = float(B * (2 * self.gamma + 1) * self.V * 4)
+        self.launches_per_step = 3 + self.gamma * 1 + self.gamma * 2 + 1 + 2
+
+    def step(self, ev=None):
+        ops = self.ops
+        if ev:
+            ev[0].record()
+        ops.snapkv_select(self.qw, self.k, self.v, self.kv_len_d, self.W, self.P, self.K, ws=self.ws_snap,
+                          out=self.sel)
+        if ev:
+            ev[1].record()
+        for s in range(self.gamma):
+            ops.draft_attn(self.qd[s], self.sel["k_draft"], self.sel["v_draft"], self.sel["draft_len"],
+                           ws=self.ws_draft, out=self.dout, lse=self.dlse)
+            ops.draft_draw(self.d, self.u, draft_tokens=self.tok, row=s, ws=self.ws_spec)
+        if ev:
+            ev[2].record()
+        ops.verify_attn(self.q, self.k, self.v, self.kv_len_d, ws=self.ws_verify, out=self.vout, lse=self.vlse)
+        if ev:
+            ev[3].record()
+        ops.rejection_sample(self.t, self.d, self.tok, self.u, ws=self.ws_spec, out_tokens=self.out_tok,
+                             num_accepted=self.nacc)
+        if ev:
+            ev[4].record()
+
+    def time_draft_only(self, reps=20):
+        """Draft attention alone (one launch per rep), for its own roofline figure."""
+        ops = self.ops
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            ops.draft_attn(self.qd[0], self.sel["k_draft"], self.sel["v_draft"], self.sel["draft_len"],
+                           ws=self.ws_draft, out=self.dout, lse=self.dlse)
+        flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=self.dev)
+        times = []
+        for _ in range(reps):
+            flush.fill_(1.0)  # evict the draft cache from L2
+            s.record()
+            ops.draft_attn(self.qd[0], self.sel["k_draft"], self.sel["v_draft"], self.sel["draft_len"],
+                           ws=self.ws_draft, out=self.dout, lse=self.dlse)
+            e.record()
+            e.synchronize()
+            times.append(s.elapsed_time(e))
+        del flush
+        return statistics.median(times)
+
+
+def run_e2e(w, steps, warmup):
+    """Same metric through the public API with pinned host inputs copied in every step."""
+    host = {}
+    for name in ("k", "v", "q", "qw", "qd", "t", "d", "u"):
+        src = getattr(w, name)
+        h = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
+        h.copy_(src)
+        host[name] = h
+    host["kv_len"] = w.kv_len.clone().pin_memory()
+    out_tok_h = torch.empty(w.out_tok.shape, dtype=torch.int32, pin_memory=True)
+    nacc_h = torch.empty(w.nacc.shape, dtype=torch.int32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_tok_h.numel() * 4 + nacc_h.numel() * 4
+
+    def one():
+        for name in ("k", "v", "q", "qw", "qd", "t", "d", "u"):
+            getattr(w, name).copy_(host[name], non_blocking=True)
+        w.kv_len_d.copy_(host["kv_len"], non_blocking=True)
+        w.step()
+        out_tok_h.copy_(w.out_tok, non_blocking=True)
+        nacc_h.copy_(w.nacc, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    del host
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------------ the oracle on host cores
+def oracle_sample_step(cfg, n_seq, seed=0):
+    """One pass of the float64 oracle over the first n_seq sequences of the workload; returns seconds."""
+    import math
+
+    from long_context_speculative_split_gb300 import workloads as wl
+    from oracle.attention import attention, draft_attention
+    from oracle.sampling import draft_draw, rejection_sample
+    from oracle.snapkv import snapkv_select
+
+    c = dict(cfg)
+    lens = wl.lengths(cfg, seed)[:n_seq]
+    c["B"] = n_seq
+    c["lens"] = [int(x) for x in lens]
+    cap = int(lens.max())
+    k, v = wl.kv_cache(c, "cpu", seed, kv_len=lens, cap=cap)
+    q, qw = wl.queries(c, "cpu", seed), wl.window_queries(c, "cpu", seed)
+    t, d = wl.logits(c, "cpu", seed)
+    u = wl.uniforms(c, "cpu", seed)
+    scale = 1.0 / math.sqrt(c["D"])
+    t0 = time.perf_counter()
+    sel = snapkv_select(qw, k, v, lens, c["W"], c["pool"], c["K"], scale)
+    toks = []
+    for s in range(c["gamma"]):
+        qd = wl.draft_queries(c, "cpu", seed, step=s)
+        draft_attention(qd, sel["k_draft"], sel["v_draft"], sel["draft_len"], scale)
+        x, _ = draft_draw(d[:, s:s + 1], u[:, s:s + 1])
+        toks.append(x[:, 0])
+    attention(q, k, v, lens, scale)
+    rejection_sample(t, d, torch.stack([torch.as_tensor(x) for x in toks], dim=1).numpy(), u)
+    return time.perf_counter() - t0
+
+
+def cpu_cores_used():
+    return 1  # the oracle runs single-threaded (BLAS pinned to one thread above)
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from long_context_speculative_split_gb300 import workloads as wl
+    cfg = wl.CONFIGS[args.config]
+    T = cfg["gamma"] + 1
+    for _ in range(args.warmup):
+        oracle_sample_step(cfg, 1)
+    times = [oracle_sample_step(cfg, 1) for _ in range(args.steps)]
+    sec = sum(times) / len(times)
+    value = T / sec
+    sample = "1 of %d sequences per step (all %d KV heads, full context), whole path" % (cfg["B"], cfg["Hkv"])
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(cfg),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(cfg):
+    lens = cfg["lens"]
+    ctx = lens if not isinstance(lens, tuple) else "U[%d, %d]" % lens
+    return {"workload": "%s: batch %d, context %s, %dq/%dkv heads, head_dim %d, gamma %d, draft budget K=%d, "
+                        "SnapKV window %d, pool %d, vocab %d (Llama-3.1-8B attention shape, synthetic)" % (
+                            cfg["name"], cfg["B"], ctx, cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["gamma"], cfg["K"],
+                            cfg["W"], cfg["pool"], cfg["V"]),
+            "batch": cfg["B"], "ctx": ctx, "gamma": cfg["gamma"], "K": cfg["K"],
+            "l2": "inputs larger than L2 (KV 17 GB, draft cache 0.5 GB, logits 0.6 GB at batch 128)",
+            "parallelism": "weak: one full batch per GPU"}
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU (the oracle arm is --impl reference)"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    w = Workload(args.config, dev, seed=rank)
+    for _ in range(args.warmup):
+        w.step()
+    torch.cuda.synchronize()
+    nev = 5
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(args.steps):
+        w.step(evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_step = total_ms / args.steps
+    phase = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)] for j in range(nev - 1)]
+    snap_ms, draft_ms, verify_ms, spec_ms = (statistics.mean(x) for x in phase)
+    errs = w.mgd.mgd_workspace_errors(w.ws_verify) | w.mgd.mgd_workspace_errors(w.ws_snap)
+    tokens = w.B * w.T
+    value = world * tokens / (ms_step / 1e3)
+    peak, peak_kind = hbm_peak()
+    verify_gbs = w.bytes_verify / (verify_ms / 1e3) / 1e9
+    draft_alone_ms = w.time_draft_only()
+    draft_gbs = w.bytes_draft / (draft_alone_ms / 1e3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = run_e2e(w, max(1, min(args.steps, 5)), 1)
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": world * tokens / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
+    traffic = load_traffic(args.config)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_block(w.cfg),
+        "roofline": {"kernel": "verify attention (split-KV, tensor-core mma, TMA)", "bound": "hbm",
+                     "achieved": verify_gbs, "peak": peak, "unit": "GB/s", "frac": verify_gbs / peak,
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": w.bytes_verify, "ms_per_launch": verify_ms},
+        "kernels": {
+            "verify_attention": {"ms": verify_ms, "kv_gbs": verify_gbs, "frac_of_peak": verify_gbs / peak,
+                                 "verified_tokens_per_s_per_layer": tokens / (verify_ms / 1e3)},
+            "draft_attention": {"ms_alone_l2_flushed": draft_alone_ms, "kv_gbs": draft_gbs,
+                                "frac_of_peak": draft_gbs / peak, "ms_per_step_all_gamma_incl_draw": draft_ms},
+            "snapkv_select": {"ms": snap_ms, "kv_gbs": w.bytes_snap / (snap_ms / 1e3) / 1e9},
+            "rejection_sample": {"ms": spec_ms, "gbs": w.bytes_spec / (spec_ms / 1e3) / 1e9},
+        },
+        "gpu_launches": w.launches_per_step * args.steps,
+        "device_error_flags": errs,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_sample
+        sec = oracle_sample_step(w.cfg, n)
+        line["cpu_baseline"] = {"value": n * w.T / sec, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
+                                "sample": "%d of %d sequences (all %d KV heads, full context), whole path, %.1f s"
+                                          % (n, w.B, w.Hkv, sec)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def load_traffic(cid):
+    """DRAM bytes per verify launch from the committed ncu summary, if it matches this kernel build."""
+    path = os.path.join(ROOT, "profiles", "verify_attention_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("config%d" % cid)
+    except Exception:
+        return None
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,198 @@
+/*
+ * mgd.h -- C ABI of libmgd.so: the GPU hot path of self-speculative decoding
+ * with a compressed draft KV cache (MagicDec-style), for NVIDIA GB300 (sm_103a).
+ *
+ * Sources restated here (the pages give the method, never an interface):
+ *   [MagicDec] "MAGICDEC: BREAKING THE LATENCY-THROUGHPUT TRADEOFF FOR LONG
+ *              CONTEXT GENERATION WITH SPECULATIVE DECODING" (paper notes,
+ *              arXiv:2408.11049): quick-read summary, sections 3.1-3.3,
+ *              4.1 (Eq. 3), 4.4, appendix A.1.
+ *   [SD-Serving] "Wann beschleunigt spekulatives Decoding das LLM-Serving?",
+ *              section "Eine Verifizierungsrunde verstehen".
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is CALLER-OWNED DEVICE memory on the current
+ *     device.  The library never allocates device memory; scratch space is
+ *     the caller's `ws` buffer of at least the size the matching
+ *     mgd_*_workspace_size() returns for the same shape.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream; nothing synchronises.
+ *   - Shape / argument errors are detected on the host before anything is
+ *     launched and return MGD_ERR_INVALID_ARG / MGD_ERR_UNSUPPORTED /
+ *     MGD_ERR_WORKSPACE; a failed launch returns MGD_ERR_CUDA.  A text for the
+ *     last error of the calling thread is available from mgd_last_error().
+ *   - Values that live on the device (kv_len, draft_len, token ids) cannot be
+ *     checked on the host.  Kernels that meet an out-of-range device value skip
+ *     that sequence (its outputs are unspecified) and set a bit in the error
+ *     word kept at the start of `ws`; mgd_workspace_errors() reads it back.
+ *   - Element strides are in elements, layouts are row-major, the innermost
+ *     dimension (D or V) is contiguous.  Every device pointer must be 16-byte
+ *     aligned and bf16 KV strides must be multiples of 8 elements (the K/V
+ *     tiles are fetched by the Tensor Memory Accelerator).
+ *   - Calls are thread-safe as long as concurrent calls use distinct `ws`.
+ *   - B == 0 is a valid no-op.
+ */
+#ifndef MGD_H_
+#define MGD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MGD_OK = 0,
+  MGD_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, bad stride, misaligned pointer */
+  MGD_ERR_UNSUPPORTED = 2,   /* valid request the kernels do not implement (e.g. D not in {64,128}) */
+  MGD_ERR_WORKSPACE = 3,     /* ws NULL or smaller than mgd_*_workspace_size() */
+  MGD_ERR_CUDA = 4           /* a CUDA runtime / driver call failed; see mgd_last_error() */
+} mgd_status;
+
+typedef enum { MGD_BF16 = 0, MGD_F32 = 1 } mgd_dtype;
+
+typedef enum {
+  MGD_VERIFY = 0,      /* accept / reject a whole speculation round */
+  MGD_DRAW_DRAFT = 1   /* draw draft tokens from the draft distributions */
+} mgd_sample_mode;
+
+/* Bits of the device error word (see mgd_workspace_errors). */
+#define MGD_DEVERR_KV_LEN   0x1u   /* kv_len[b] < T, or > kv_cap; or draft_len[b] < 1 or > k_cap */
+#define MGD_DEVERR_SNAP_LEN 0x2u   /* kv_len[b] < W or > kv_cap in mgd_snapkv_select */
+#define MGD_DEVERR_TOKEN    0x4u   /* a draft token id outside [0, V) */
+#define MGD_DEVERR_TIMEOUT  0x8u   /* a bounded wait inside a kernel gave up (never expected) */
+
+const char *mgd_status_string(mgd_status s);
+/* Detail text of the last non-OK status returned on the calling thread ("" if none). */
+const char *mgd_last_error(void);
+/* Library version, major * 10000 + minor * 100 + patch. */
+int mgd_version(void);
+
+/*
+ * Reads the device error word of a workspace after the work queued on
+ * `stream` finished (this call synchronises `stream`).  *flags receives the
+ * OR of MGD_DEVERR_* bits raised by the last call that used `ws`.
+ */
+mgd_status mgd_workspace_errors(const void *ws, void *stream, uint32_t *flags);
+
+/* ------------------------------------------------------------------------ *
+ * Verify attention.  [MagicDec] section 3.2: verifying gamma draft tokens
+ * and decoding read the same KV cache, so the target's verify pass is decode
+ * attention over T = gamma + 1 query rows per sequence against the full
+ * cache (the extra row gives the bonus-token distribution of [SD-Serving]).
+ *
+ *   q        [B, T, Hq, D]            in_dtype, contiguous
+ *   k, v     [B, Hkv, kv_cap, D]      in_dtype; element (b, h, j, d) at
+ *                                     b*kv_batch_stride + h*kv_head_stride + j*D + d
+ *   kv_len   [B] int32 (device)       rows of sequence b, INCLUDING the T rows
+ *                                     being verified; T <= kv_len[b] <= kv_cap
+ *   out      [B, T, Hq, D]            out_dtype (MGD_F32 or MGD_BF16)
+ *   lse      [B, T, Hq] float32 or NULL: natural-log sum of exp(scores)
+ *
+ * Query head h reads KV head h / (Hq/Hkv).  Row t sits at position
+ * kv_len[b]-T+t and attends to keys 0 .. kv_len[b]-T+t (causal among the
+ * appended rows); scores are sm_scale * <q, k>; softmax and accumulation in
+ * float32.  Supported: D in {64, 128}; 1 <= T <= 8; Hq % Hkv == 0.
+ * in_dtype MGD_BF16 runs the tensor-core split-KV kernel; MGD_F32 runs a
+ * float32 CUDA-core kernel (for float32 inputs; not the timed path).
+ * ------------------------------------------------------------------------ */
+size_t mgd_verify_workspace_size(int B, int T, int Hq, int Hkv, int D, int kv_cap);
+mgd_status mgd_verify_attn(const void *q, const void *k, const void *v, const int32_t *kv_len,
+                           int B, int T, int Hq, int Hkv, int D, int kv_cap,
+                           int64_t kv_batch_stride, int64_t kv_head_stride, float sm_scale,
+                           mgd_dtype in_dtype, void *out, mgd_dtype out_dtype, float *lse,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Draft attention.  [MagicDec] quick-read summary and section 4.1 (Eq. 3):
+ * the draft is the target model itself reading a compressed KV of budget K,
+ * costing T_D(K) per draft step.  One query row per sequence attends to all
+ * draft_len[b] rows of the compacted cache (no mask).
+ *
+ *   q                 [B, Hq, D]              in_dtype (the single draft row)
+ *   k_draft, v_draft  [B, Hkv, k_cap, D]      in_dtype, strides as for verify
+ *   draft_len         [B] int32 (device)      1 <= draft_len[b] <= k_cap
+ *   out [B, Hq, D] out_dtype;  lse [B, Hq] float32 or NULL.
+ * Identical arithmetic to mgd_verify_attn with T = 1.
+ * ------------------------------------------------------------------------ */
+size_t mgd_draft_workspace_size(int B, int Hq, int Hkv, int D, int k_cap);
+mgd_status mgd_draft_attn(const void *q, const void *k_draft, const void *v_draft,
+                          const int32_t *draft_len, int B, int Hq, int Hkv, int D, int k_cap,
+                          int64_t kv_batch_stride, int64_t kv_head_stride, float sm_scale,
+                          mgd_dtype in_dtype, void *out, mgd_dtype out_dtype, float *lse,
+                          void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * SnapKV draft-cache selection.  [MagicDec] section 4.4 (static selection,
+ * SnapKV named) and appendix A.1 (the compressed KV is built at prefill and
+ * reused by every draft step).  The pages do not define SnapKV; this call
+ * computes the plain reading:
+ *   1. window queries q_win[b, w, h] (position kv_len[b]-W+w) attend causally
+ *      to keys 0 .. kv_len[b]-W+w; their softmax probabilities are summed over
+ *      the W window rows and the G = Hq/Hkv heads of a KV head, for every
+ *      prefix key j < kv_len[b]-W;
+ *   2. max-pool along the sequence with odd kernel `pool` (stride 1, positions
+ *      outside the prefix ignored);
+ *   3. keep K_eff = min(K, kv_len[b]) rows: the top K_eff-W prefix positions
+ *      (ties -> lower position) plus the W window positions, ascending;
+ *   4. gather those K and V rows into the draft cache.
+ *
+ *   q_win    [B, W, Hq, D] in_dtype;  k, v, kv_len as for mgd_verify_attn
+ *            (W <= kv_len[b] <= kv_cap)
+ *   sel_idx  [B, Hkv, draft_cap] int32: kept positions, -1 after K_eff
+ *   k_draft, v_draft [B, Hkv, draft_cap, D] in_dtype, contiguous; rows after
+ *            K_eff are left untouched (draft_cap >= K leaves room for rows
+ *            appended while drafting)
+ *   draft_len [B] int32: K_eff
+ *   scores   [B, Hkv, kv_cap] float32 or NULL: pooled scores of the prefix
+ *            positions (entries >= kv_len[b]-W unspecified)
+ * Supported: D in {64, 128}; 1 <= W <= 64; 1 <= pool <= 63 and odd; W <= K <= draft_cap.
+ * ------------------------------------------------------------------------ */
+size_t mgd_snapkv_workspace_size(int B, int Hq, int Hkv, int D, int kv_cap, int W);
+mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, const int32_t *kv_len,
+                             int B, int Hq, int Hkv, int D, int kv_cap,
+                             int64_t kv_batch_stride, int64_t kv_head_stride,
+                             int W, int pool, int K, float sm_scale, mgd_dtype in_dtype,
+                             int32_t *sel_idx, void *k_draft, void *v_draft, int draft_cap,
+                             int32_t *draft_len, float *scores,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Speculative sampling.  [SD-Serving] "Eine Verifizierungsrunde verstehen":
+ * candidates are accepted left to right using both distributions; at the
+ * first rejection a correction is drawn from the residual target
+ * distribution max(0, p - q) (renormalised) and later candidates are
+ * dropped; when all are accepted one more token is drawn from the target.
+ * The paragraph after it states that this preserves the target distribution.
+ *
+ *   target_logits [B, gamma+1, V] float32 (MGD_VERIFY only; may be NULL otherwise)
+ *   draft_logits  [B, gamma, V]   float32
+ *   draft_tokens  [B, gamma] int32: written by MGD_DRAW_DRAFT, read by MGD_VERIFY
+ *   u             [B, gamma+1, 3] float32 in [0,1): slot 0 draws the draft
+ *                 token of position i, slot 1 is the acceptance test, slot 2
+ *                 the correction draw; position gamma uses slot 2 only (bonus)
+ *   row           MGD_DRAW_DRAFT: draw only position `row` (0 <= row < gamma),
+ *                 or every position when row < 0.  Ignored by MGD_VERIFY.
+ *   out_tokens    [B, gamma+1] int32 (MGD_VERIFY): accepted drafts, then the
+ *                 correction or bonus token, then -1
+ *   num_accepted  [B] int32 (MGD_VERIFY)
+ *
+ * p = softmax(target logits), q = softmax(draft logits), temperature 1.
+ * Accept position i iff u[b,i,1] * q_i(x_i) < p_i(x_i).  A draw from weights r
+ * with uniform u returns the smallest index whose running sum (index order)
+ * exceeds u * sum(r), else the last index with r > 0; a residual that sums to
+ * zero (rounding only) falls back to p.  Arithmetic in float32.
+ * Supported: 1 <= gamma <= 16; 1 <= V < 2^31.
+ * ------------------------------------------------------------------------ */
+size_t mgd_spec_workspace_size(int B, int gamma, int V);
+mgd_status mgd_spec_sample(const float *target_logits, const float *draft_logits,
+                           int32_t *draft_tokens, const float *u, int B, int gamma, int V,
+                           int mode, int row, int32_t *out_tokens, int32_t *num_accepted,
+                           void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MGD_H_ */

@@ -1,0 +1,558 @@
+// Split-KV ("flash-decoding") GQA attention for the verify and draft passes,
+// bf16 K/V/Q, float32 softmax and accumulation, sm_103a.
+//
+// MagicDec notes, section 3.2: verifying gamma draft tokens loads the same KV
+// cache as decoding one token, so at long context the verify pass costs about
+// one decode step -- the whole point is to read every KV byte once.  This
+// kernel therefore processes, for each (sequence, KV head), all G query heads
+// of the group and all T = gamma+1 verify rows against each K/V tile while the
+// tile sits in shared memory.  The draft pass (quick-read summary and section
+// 4.1, Eq. 3: the target itself drafting over a compressed cache of budget K)
+// is the same kernel with T = 1 over the compacted cache.
+//
+// Structure (one CTA = 4 consumer warps + 1 producer warp, 2 CTAs per SM):
+//   * work unit = (sequence, KV head, row group, chunk of C keys); a
+//     persistent grid pulls units from an atomic counter, so ragged lengths
+//     balance themselves and the producer keeps prefetching across units;
+//   * the producer streams 64-key K and V tiles with the Tensor Memory
+//     Accelerator (128-byte swizzled boxes) into a 3-stage mbarrier ring;
+//   * each consumer warp owns 16 keys of every tile and computes
+//     S^T = K Q^T with mma.m16n8k16 (keys on the M side, so G*T rows pad only
+//     to a multiple of 8), an online softmax in the exp2 domain, and
+//     O^T += V^T P^T where P is split into bf16 hi + lo parts (two mmas) so
+//     the probabilities keep ~16 significant bits;
+//   * at the end of a unit the 4 warps merge in shared memory; a unit that
+//     covers the whole sequence writes the final output, otherwise it writes
+//     a partial (O, lse) and the CTA that completes the last chunk of that
+//     sequence merges all partials (atomic ticket, no waiting).
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace mgd {
+namespace {
+
+constexpr int kTileKeys = 64;
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kBoxBytes = 64 * 128;  // 64 rows x 64 bf16
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct TileMeta {
+  int unit;
+  int tile;
+  int ntiles;
+  int L;
+};
+
+struct KParams {
+  int T, Hq, Hkv, G, rows, RG, C, nchunk, kv_cap;
+  unsigned total_units;
+  float sl2;  // sm_scale * log2(e)
+  size_t off_tickets, off_part_o, off_part_l;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;  // K boxes then V boxes
+  static constexpr int kOStride = 68;                          // epilogue row stride (64 cols + 4)
+  static constexpr int off_epi = kStages * kStageBytes;
+  static constexpr int off_m = off_epi + 32 * kOStride * 4;  // float [4][32]
+  static constexpr int off_l = off_m + 4 * 32 * 4;           // float [4][32]
+  static constexpr int off_rowM = off_l + 4 * 32 * 4;        // float [32]
+  static constexpr int off_rowL = off_rowM + 32 * 4;         // float [32]
+  static constexpr int off_meta = off_rowL + 32 * 4;         // TileMeta [kStages]
+  static constexpr int off_bar = off_meta + kStages * 16;    // uint64 full[kStages], empty[kStages]
+  static constexpr int off_flag = off_bar + 2 * kStages * 8;
+  static constexpr int bytes = off_flag + 16;
+  static constexpr int alloc = bytes + 1024;  // slack to align the base to 1024
+};
+
+template <int D, int NT, int MINB>
+__global__ void __maxnreg__(MINB == 2 ? 200 : 255)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                   const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ kv_len,
+                   float *__restrict__ out_f32, __nv_bfloat16 *__restrict__ out_bf16, float *__restrict__ lse_out,
+                   unsigned char *__restrict__ ws, KParams p) {
+  using Lay = Layout<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float *sm_O = reinterpret_cast<float *>(smem + Lay::off_epi);
+  float *sm_m = reinterpret_cast<float *>(smem + Lay::off_m);
+  float *sm_l = reinterpret_cast<float *>(smem + Lay::off_l);
+  float *sm_rowM = reinterpret_cast<float *>(smem + Lay::off_rowM);
+  float *sm_rowL = reinterpret_cast<float *>(smem + Lay::off_rowL);
+  TileMeta *meta = reinterpret_cast<TileMeta *>(smem + Lay::off_meta);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::off_bar);
+  uint64_t *empty = full + kStages;
+  int *sm_flag = reinterpret_cast<int *>(smem + Lay::off_flag);
+
+  WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+  unsigned *tickets = reinterpret_cast<unsigned *>(ws + p.off_tickets);
+  float *part_o = reinterpret_cast<float *>(ws + p.off_part_o);
+  float *part_l = reinterpret_cast<float *>(ws + p.off_part_l);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  __syncthreads();
+
+  // ====================================================================== producer
+  if (warp == kConsumerWarps) {
+    if (lane != 0) return;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    while (ok) {
+      const unsigned u = atomicAdd(&hdr->next_unit, 1u);
+      if (u >= p.total_units) break;
+      const int pair = static_cast<int>(u) / p.nchunk;
+      const int chunk = static_cast<int>(u) % p.nchunk;
+      const int bh = pair / p.RG;
+      const int hkv = bh % p.Hkv;
+      const int b = bh / p.Hkv;
+      const int L = kv_len[b];
+      if (L < p.T || L > p.kv_cap) {
+        if (chunk == 0) raise_error(hdr, 0x1u);
+        continue;
+      }
+      const int start = chunk * p.C;
+      if (start >= L) continue;
+      const int end = min(start + p.C, L);
+      const int ntiles = (end - start + kTileKeys - 1) / kTileKeys;
+      for (int t = 0; t < ntiles; ++t) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+          raise_error(hdr, 0x8u);
+          ok = false;
+          break;
+        }
+        meta[stage] = TileMeta{static_cast<int>(u), t, ntiles, L};
+        mbar_arrive_expect_tx(&full[stage], Lay::kStageBytes);
+        unsigned char *st = smem + stage * Lay::kStageBytes;
+        const int row = start + t * kTileKeys;
+#pragma unroll
+        for (int h = 0; h < Lay::kBoxes; ++h) tma_load_4d(st + h * kBoxBytes, &kmap, &full[stage], h * 64, row, hkv, b);
+#pragma unroll
+        for (int h = 0; h < Lay::kBoxes; ++h)
+          tma_load_4d(st + (Lay::kBoxes + h) * kBoxBytes, &vmap, &full[stage], h * 64, row, hkv, b);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (ok && mbar_wait(&empty[stage], phase ^ 1u)) {
+      meta[stage].unit = -1;
+      mbar_arrive(&full[stage]);
+    } else {
+      raise_error(hdr, 0x8u);
+      // drain: wait (bounded) for every load still in flight before leaving
+      for (int s = 0; s < kStages; ++s) mbar_wait(&full[s], phase);
+    }
+    return;
+  }
+
+  // ====================================================================== consumers
+  const int gid = lane >> 2;
+  const int tig = lane & 3;
+  constexpr int MT = D / 16;  // m16 tiles over D (PV) == k16 steps over D (QK)
+
+  float acc[MT][NT][4];
+  uint32_t qf[MT][NT][2];
+  float m_run[NT][2], l_run[NT][2];
+  int lim[NT][2];
+
+  int stage = 0;
+  uint32_t phase = 0;
+  while (true) {
+    if (!mbar_wait(&full[stage], phase)) {
+      raise_error(hdr, 0x8u);
+      break;
+    }
+    const TileMeta md = meta[stage];
+    if (md.unit < 0) break;
+    const int pair = md.unit / p.nchunk;
+    const int chunk = md.unit % p.nchunk;
+    const int rg = pair % p.RG;
+    const int bh = pair / p.RG;
+    const int hkv = bh % p.Hkv;
+    const int b = bh / p.Hkv;
+    const int L = md.L;
+    const int start = chunk * p.C;
+
+    if (md.tile == 0) {
+      // ---- new unit: query fragments (B operand of S^T = K Q^T), state reset
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int qg = rg * 32 + 8 * j + 2 * tig + e;
+          lim[j][e] = (qg < p.rows) ? (L - p.T + qg / p.G) : (L - 1);
+          m_run[j][e] = -INFINITY;
+          l_run[j][e] = 0.f;
+        }
+        const int qg = rg * 32 + 8 * j + gid;
+        const __nv_bfloat16 *qrow = nullptr;
+        if (qg < p.rows) {
+          const int t = qg / p.G, g = qg % p.G;
+          qrow = q + ((static_cast<size_t>(b) * p.T + t) * p.Hq + hkv * p.G + g) * D;
+        }
+#pragma unroll
+        for (int kk = 0; kk < MT; ++kk) {
+          if (qrow) {
+            qf[kk][j][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tig);
+            qf[kk][j][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 8 + 2 * tig);
+          } else {
+            qf[kk][j][0] = 0u;
+            qf[kk][j][1] = 0u;
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[kk][j][c] = 0.f;
+        }
+      }
+    }
+
+    unsigned char *st = smem + stage * Lay::kStageBytes;
+    const int key0 = start + md.tile * kTileKeys + warp * 16;
+    if (key0 < L) {
+      // ---- S^T[16 keys][8*NT rows] = K Q^T
+      float s[NT][4];
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s[j][c] = 0.f;
+      const uint32_t kbase = smem_addr(st);
+      const int kr = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+      for (int kk = 0; kk < MT; ++kk) {
+        const int d = 16 * kk + 8 * (lane >> 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kbase + (d >> 6) * kBoxBytes + swz128(kr, (d & 63) >> 3), a0, a1, a2, a3);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_bf16_16816(s[j], a0, a1, a2, a3, qf[kk][j][0], qf[kk][j][1]);
+      }
+      // ---- scale, mask, online softmax (exp2 domain)
+      const bool need_mask = key0 + 15 > L - p.T;
+      const int k_lo = key0 + gid, k_hi = key0 + gid + 8;
+      uint32_t phi[NT][2], plo[NT][2];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        float alpha[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float v0 = s[j][e] * p.sl2;
+          float v1 = s[j][2 + e] * p.sl2;
+          if (need_mask) {
+            if (k_lo > lim[j][e]) v0 = -INFINITY;
+            if (k_hi > lim[j][e]) v1 = -INFINITY;
+          }
+          const float mx = warp_max_xor(fmaxf(v0, v1), 4, 16);
+          const float mnew = fmaxf(m_run[j][e], mx);
+          const float muse = (mnew == -INFINITY) ? 0.f : mnew;
+          alpha[e] = exp2f(m_run[j][e] - muse);
+          const float p0 = exp2f(v0 - muse);
+          const float p1 = exp2f(v1 - muse);
+          l_run[j][e] = l_run[j][e] * alpha[e] + p0 + p1;
+          m_run[j][e] = mnew;
+          s[j][e] = p0;
+          s[j][2 + e] = p1;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          acc[mt][j][0] *= alpha[0];
+          acc[mt][j][1] *= alpha[1];
+          acc[mt][j][2] *= alpha[0];
+          acc[mt][j][3] *= alpha[1];
+        }
+        uint32_t h0, l0, h1, l1;
+        split_bf16(s[j][0], s[j][1], h0, l0);  // keys gid,   rows 2tig, 2tig+1
+        split_bf16(s[j][2], s[j][3], h1, l1);  // keys gid+8, rows 2tig, 2tig+1
+        phi[j][0] = movmatrix_t(h0);
+        phi[j][1] = movmatrix_t(h1);
+        plo[j][0] = movmatrix_t(l0);
+        plo[j][1] = movmatrix_t(l1);
+      }
+      // ---- rows past the sequence end hold stale bytes: zero this warp's V rows there
+      if (key0 + 16 > L) {
+        const int r0 = L - key0;  // first invalid local row (1..15)
+        const int nchunks = (16 - r0) * 8 * Lay::kBoxes;
+        for (int i = lane; i < nchunks; i += 32) {
+          const int h = i / ((16 - r0) * 8);
+          const int rem = i % ((16 - r0) * 8);
+          const int r = warp * 16 + r0 + rem / 8;
+          const int c = rem % 8;
+          *reinterpret_cast<uint4 *>(st + (Lay::kBoxes + h) * kBoxBytes + swz128(r, c)) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // ---- O^T[D][rows] += V^T P^T
+      const uint32_t vbase = smem_addr(st + Lay::kBoxes * kBoxBytes);
+      const int vr = warp * 16 + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int d = 16 * mt + 8 * ((lane >> 3) & 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vbase + (d >> 6) * kBoxBytes + swz128(vr, (d & 63) >> 3), a0, a1, a2, a3);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          mma_bf16_16816(acc[mt][j], a0, a1, a2, a3, phi[j][0], phi[j][1]);
+          mma_bf16_16816(acc[mt][j], a0, a1, a2, a3, plo[j][0], plo[j][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (md.tile != md.ntiles - 1) continue;
+
+    // ================================================================ unit epilogue
+    const int rows_valid = min(32, p.rows - rg * 32);
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) l_run[j][e] = warp_sum_xor(l_run[j][e], 4, 16);
+    if (gid == 0) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          sm_m[warp * 32 + 8 * j + 2 * tig + e] = m_run[j][e];
+          sm_l[warp * 32 + 8 * j + 2 * tig + e] = l_run[j][e];
+        }
+    }
+    named_bar(1, kConsumerWarps * 32);
+    if (threadIdx.x < 32) {
+      const int r = threadIdx.x;
+      float M = -INFINITY;
+      for (int w = 0; w < kConsumerWarps; ++w)
+        if (r < 8 * NT) M = fmaxf(M, sm_m[w * 32 + r]);
+      const float Mu = (M == -INFINITY) ? 0.f : M;
+      float Lt = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w)
+        if (r < 8 * NT) Lt += sm_l[w * 32 + r] * exp2f(sm_m[w * 32 + r] - Mu);
+      sm_rowM[r] = Mu;
+      sm_rowL[r] = Lt;
+    }
+    named_bar(1, kConsumerWarps * 32);
+    float f[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) f[j][e] = exp2f(m_run[j][e] - sm_rowM[8 * j + 2 * tig + e]);
+
+    const int nch_b = (L + p.C - 1) / p.C;
+    const bool single = (nch_b == 1);
+    const size_t part_base = (static_cast<size_t>(pair) * p.nchunk + chunk) * 32;
+    for (int dh = 0; dh < D / 64; ++dh) {
+      for (int i = threadIdx.x; i < 32 * Lay::kOStride; i += kConsumerWarps * 32) sm_O[i] = 0.f;
+      named_bar(1, kConsumerWarps * 32);
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm) {
+        const int mt = dh * 4 + mm;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int r = 8 * j + 2 * tig + e;
+            atomicAdd(&sm_O[r * Lay::kOStride + 16 * mm + gid], acc[mt][j][e] * f[j][e]);
+            atomicAdd(&sm_O[r * Lay::kOStride + 16 * mm + gid + 8], acc[mt][j][2 + e] * f[j][e]);
+          }
+      }
+      named_bar(1, kConsumerWarps * 32);
+      for (int i = threadIdx.x; i < rows_valid * 16; i += kConsumerWarps * 32) {
+        const int r = i >> 4, dq = i & 15;
+        const float Lt = sm_rowL[r];
+        const float inv = (Lt > 0.f) ? 1.f / Lt : 0.f;
+        float4 o = *reinterpret_cast<const float4 *>(&sm_O[r * Lay::kOStride + 4 * dq]);
+        o.x *= inv;
+        o.y *= inv;
+        o.z *= inv;
+        o.w *= inv;
+        const int d = dh * 64 + 4 * dq;
+        const int qg = rg * 32 + r;
+        if (single) {
+          const int t = qg / p.G, g = qg % p.G;
+          const size_t orow = (static_cast<size_t>(b) * p.T + t) * p.Hq + hkv * p.G + g;
+          if (out_bf16) {
+            uint2 pk;
+            pk.x = pack_bf16(o.x, o.y);
+            pk.y = pack_bf16(o.z, o.w);
+            *reinterpret_cast<uint2 *>(out_bf16 + orow * D + d) = pk;
+          } else {
+            *reinterpret_cast<float4 *>(out_f32 + orow * D + d) = o;
+          }
+          if (lse_out && dh == 0 && dq == 0)
+            lse_out[orow] = (Lt > 0.f) ? (sm_rowM[r] + log2f(Lt)) * kLn2 : -INFINITY;
+        } else {
+          *reinterpret_cast<float4 *>(part_o + (part_base + r) * D + d) = o;
+          if (dh == 0 && dq == 0) part_l[part_base + r] = (Lt > 0.f) ? (sm_rowM[r] + log2f(Lt)) * kLn2 : -INFINITY;
+        }
+      }
+      named_bar(1, kConsumerWarps * 32);
+    }
+    if (single) continue;
+
+    // ---- the CTA that finishes the last chunk of this pair merges all partials
+    __threadfence();
+    named_bar(1, kConsumerWarps * 32);
+    if (threadIdx.x == 0) {
+      const unsigned old = atomicAdd(&tickets[pair], 1u);
+      *sm_flag = (old == static_cast<unsigned>(nch_b - 1)) ? 1 : 0;
+    }
+    named_bar(1, kConsumerWarps * 32);
+    if (*sm_flag) {
+      __threadfence();
+      const size_t pb0 = static_cast<size_t>(pair) * p.nchunk * 32;
+      if (threadIdx.x < rows_valid) {
+        const int r = threadIdx.x;
+        float M = -INFINITY;
+        for (int c = 0; c < nch_b; ++c) M = fmaxf(M, __ldcg(part_l + pb0 + c * 32 + r));
+        float W = 0.f;
+        for (int c = 0; c < nch_b; ++c) W += expf(__ldcg(part_l + pb0 + c * 32 + r) - M);
+        sm_rowM[r] = M;
+        sm_rowL[r] = W;
+      }
+      named_bar(1, kConsumerWarps * 32);
+      for (int i = threadIdx.x; i < rows_valid * (D / 4); i += kConsumerWarps * 32) {
+        const int r = i / (D / 4), dq = i % (D / 4);
+        const float M = sm_rowM[r];
+        const float inv = 1.f / sm_rowL[r];
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < nch_b; ++c) {
+          const float w = expf(__ldcg(part_l + pb0 + c * 32 + r) - M) * inv;
+          const float4 x = __ldcg(reinterpret_cast<const float4 *>(part_o + (pb0 + c * 32 + r) * D + 4 * dq));
+          o.x += w * x.x;
+          o.y += w * x.y;
+          o.z += w * x.z;
+          o.w += w * x.w;
+        }
+        const int qg = rg * 32 + r;
+        const int t = qg / p.G, g = qg % p.G;
+        const size_t orow = (static_cast<size_t>(b) * p.T + t) * p.Hq + hkv * p.G + g;
+        if (out_bf16) {
+          uint2 pk;
+          pk.x = pack_bf16(o.x, o.y);
+          pk.y = pack_bf16(o.z, o.w);
+          *reinterpret_cast<uint2 *>(out_bf16 + orow * D + 4 * dq) = pk;
+        } else {
+          *reinterpret_cast<float4 *>(out_f32 + orow * D + 4 * dq) = o;
+        }
+        if (lse_out && dq == 0) lse_out[orow] = M + logf(sm_rowL[r]);
+      }
+      named_bar(1, kConsumerWarps * 32);
+    }
+  }
+}
+
+template <int D, int NT>
+cudaError_t launch_one(const AttnPlan &pl, const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap) {
+  constexpr int MINB = (NT <= 3) ? 2 : 1;
+  auto kern = attn_tc_kernel<D, NT, MINB>;
+  const int smem = Layout<D>::alloc;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  KParams kp;
+  kp.T = pl.T;
+  kp.Hq = pl.Hq;
+  kp.Hkv = pl.Hkv;
+  kp.G = pl.G;
+  kp.rows = pl.rows;
+  kp.RG = pl.RG;
+  kp.C = pl.C;
+  kp.nchunk = pl.nchunk;
+  kp.kv_cap = pl.kv_cap;
+  kp.total_units = static_cast<unsigned>(pl.pairs) * static_cast<unsigned>(pl.nchunk);
+  kp.sl2 = a.sm_scale * kLog2e;
+  kp.off_tickets = pl.off_tickets;
+  kp.off_part_o = pl.off_part_o;
+  kp.off_part_l = pl.off_part_l;
+  int grid = pl.grid;
+  if (static_cast<unsigned>(grid) > kp.total_units) grid = static_cast<int>(kp.total_units);
+  kern<<<grid, kThreads, smem, a.stream>>>(kmap, vmap, static_cast<const __nv_bfloat16 *>(a.q), a.kv_len,
+                                           a.out_bf16 ? nullptr : static_cast<float *>(a.out),
+                                           a.out_bf16 ? static_cast<__nv_bfloat16 *>(a.out) : nullptr, a.lse,
+                                           static_cast<unsigned char *>(a.ws), kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_tc_min_blocks(int NT) { return NT <= 3 ? 2 : 1; }
+
+cudaError_t launch_attention_tc(const AttnPlan &pl, const AttnArgs &a, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap) {
+  const size_t clear = pl.off_part_o;  // header + tickets
+  cudaError_t e = cudaMemsetAsync(a.ws, 0, clear, a.stream);
+  if (e != cudaSuccess) return e;
+  if (pl.D == 128) {
+    switch (pl.NT) {
+      case 1: return launch_one<128, 1>(pl, a, kmap, vmap);
+      case 2: return launch_one<128, 2>(pl, a, kmap, vmap);
+      case 3: return launch_one<128, 3>(pl, a, kmap, vmap);
+      default: return launch_one<128, 4>(pl, a, kmap, vmap);
+    }
+  } else {
+    switch (pl.NT) {
+      case 1: return launch_one<64, 1>(pl, a, kmap, vmap);
+      case 2: return launch_one<64, 2>(pl, a, kmap, vmap);
+      case 3: return launch_one<64, 3>(pl, a, kmap, vmap);
+      default: return launch_one<64, 4>(pl, a, kmap, vmap);
+    }
+  }
+}
+
+AttnPlan plan_attention(int B, int T, int Hq, int Hkv, int D, int kv_cap, int sm_count) {
+  AttnPlan p{};
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.kv_cap = kv_cap;
+  p.G = Hq / Hkv;
+  p.rows = p.G * T;
+  p.RG = (p.rows + 31) / 32;
+  p.rows_pg = p.RG == 1 ? p.rows : 32;
+  p.NT = (p.rows_pg + 7) / 8;
+  p.pairs = B * Hkv * p.RG;
+  const int slots = attn_tc_min_blocks(p.NT) * sm_count;
+  // Largest chunk that still leaves >= 6 units per persistent CTA; at most 64
+  // chunks per pair (the merge keeps one weight per chunk).
+  int C = 4096;
+  const int cmin = std::max(256, ((kv_cap + 63) / 64 + 63) / 64 * 64);
+  while (C > cmin && static_cast<long long>(p.pairs) * ((kv_cap + C - 1) / C) < 6LL * slots) C /= 2;
+  if (C < cmin) C = cmin;
+  p.C = C;
+  p.nchunk = (kv_cap + C - 1) / C;
+  p.grid = slots;
+  size_t off = kAlign;  // header
+  p.off_tickets = off;
+  off = align_up(off + sizeof(unsigned) * static_cast<size_t>(p.pairs));
+  p.off_part_o = off;
+  const size_t nparts = (p.nchunk > 1) ? static_cast<size_t>(p.pairs) * p.nchunk * 32 : 0;
+  off = align_up(off + nparts * D * sizeof(float));
+  p.off_part_l = off;
+  off = align_up(off + nparts * sizeof(float));
+  p.ws_bytes = off;
+  return p;
+}
+
+}  // namespace mgd

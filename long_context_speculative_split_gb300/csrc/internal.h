@@ -1,0 +1,124 @@
+// Internal (not exported) declarations shared by the libmgd translation units:
+// workspace layouts, launch plans and the kernel launchers that api.cu calls
+// after validating the arguments.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mgd {
+
+// Every workspace starts with this 256-byte header.  It is cleared at the
+// start of every call (cudaMemsetAsync on the call's stream).
+struct WsHeader {
+  unsigned err;        // OR of MGD_DEVERR_* raised by the call
+  unsigned next_unit;  // dynamic work counter of persistent kernels
+  unsigned next_unit2;
+  unsigned pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+// Number of SMs of the current device (152 on GB300 when no device is visible,
+// so that size queries made without a GPU stay deterministic).
+int current_sm_count();
+
+// ------------------------------------------------------------------ attention
+// Split-KV plan for the tensor-core attention kernel.  A "pair" is one
+// (sequence, KV head, row group); a "unit" is one chunk of C keys of a pair.
+struct AttnPlan {
+  int B, T, Hq, Hkv, D, kv_cap;
+  int G;          // query heads per KV head
+  int rows;       // G * T query rows per KV head
+  int RG;         // row groups (rows > 32 are split into groups of <= 32)
+  int rows_pg;    // rows per group (<= 32)
+  int NT;         // n8 tiles per row group = ceil(rows_pg / 8)
+  int C;          // keys per unit (multiple of 64)
+  int nchunk;     // chunk slots per pair = ceil(kv_cap / C)
+  int pairs;      // B * Hkv * RG
+  int grid;       // persistent CTAs
+  size_t off_tickets, off_part_o, off_part_l, ws_bytes;
+};
+AttnPlan plan_attention(int B, int T, int Hq, int Hkv, int D, int kv_cap, int sm_count);
+
+struct AttnArgs {
+  const void *q;
+  const void *k;
+  const void *v;
+  const int32_t *kv_len;
+  int64_t kv_batch_stride, kv_head_stride;
+  float sm_scale;
+  void *out;
+  int out_bf16;
+  float *lse;
+  void *ws;
+  cudaStream_t stream;
+};
+// bf16 inputs, tensor cores, TMA tiles, persistent split-KV with in-kernel merge.
+cudaError_t launch_attention_tc(const AttnPlan &p, const AttnArgs &a, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap);
+// Any-dtype CUDA-core attention, one CTA per (sequence, KV head).
+size_t simt_attention_ws_bytes();
+cudaError_t launch_attention_simt(const AttnPlan &p, const AttnArgs &a, int in_f32);
+
+// Encode a 4-D bf16 tensor map over a KV tensor [B, Hkv, kv_cap, D] with
+// 64x64 boxes and 128-byte swizzling.  Returns a CUDA driver status.
+int encode_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Hkv, int kv_cap, int D,
+                         int64_t batch_stride, int64_t head_stride);
+
+// ------------------------------------------------------------------ SnapKV
+struct SnapPlan {
+  int B, Hq, Hkv, D, kv_cap, W, G, rows, RG;
+  int C;       // keys per scoring unit (multiple of 64)
+  int nchunk;  // ceil(kv_cap / C)
+  int pairs;   // B * Hkv
+  size_t off_part, off_scores, off_pooled, ws_bytes;
+};
+SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W);
+
+struct SnapArgs {
+  const void *q_win;
+  const void *k;
+  const void *v;
+  const int32_t *kv_len;
+  int64_t kv_batch_stride, kv_head_stride;
+  int pool, K, draft_cap;
+  float sm_scale;
+  int32_t *sel_idx;
+  void *k_draft;
+  void *v_draft;
+  int32_t *draft_len;
+  float *scores_out;
+  void *ws;
+  cudaStream_t stream;
+};
+cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, const CUtensorMap *kmap);
+
+// ------------------------------------------------------------------ sampling
+struct SpecPlan {
+  int B, gamma, V;
+  int split;     // elements per statistics block
+  int nsplit;    // ceil(V / split)
+  int nrows;     // 2*gamma + 1 rows per sequence (gamma+1 target, gamma draft)
+  size_t off_stats, ws_bytes;
+};
+SpecPlan plan_spec(int B, int gamma, int V);
+
+struct SpecArgs {
+  const float *target;
+  const float *draft;
+  int32_t *draft_tokens;
+  const float *u;
+  int mode, row;
+  int32_t *out_tokens;
+  int32_t *num_accepted;
+  void *ws;
+  cudaStream_t stream;
+};
+cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a);
+
+}  // namespace mgd

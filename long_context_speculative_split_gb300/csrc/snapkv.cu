@@ -1,0 +1,635 @@
+// SnapKV-style static selection of the draft KV cache.
+//
+// MagicDec notes, section 4.4: static selectors (SnapKV named) gather the
+// sparse draft KV once, so drafting pays no per-token search; appendix A.1:
+// this compressed KV is built at prefill and reused by every draft step; the
+// quick-read summary gives its size as the draft budget K.  The pages do not
+// define SnapKV itself; the steps computed here are the plain reading:
+//   1. the last W positions are the observation window; each window query
+//      attends causally and its softmax probabilities are summed over the W
+//      window rows and the G query heads of a KV head, per prefix key;
+//   2. max-pool of the scores along the sequence (odd kernel, stride 1);
+//   3. the top K_eff - W prefix positions (ties -> lower position) plus the W
+//      window positions, K_eff = min(K, L), kept in ascending order;
+//   4. the kept K and V rows are gathered into the compacted draft cache.
+//
+// Kernels:
+//   snap_score_tc<PASS>  bf16 tensor-core scoring, one CTA per (sequence, KV
+//                        head, row group, key chunk); K tiles arrive through
+//                        TMA; pass 1 computes each window row's log-sum-exp,
+//                        pass 2 sums the probabilities per prefix key;
+//   snap_score_simt      the same two passes on CUDA cores (float32 inputs);
+//   snap_select          max-pool, 3-pass radix select of the K_eff-W-th
+//                        largest pooled score, ordered compaction, gather.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace mgd {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kScoreStages = 4;
+constexpr int kScoreThreads = 160;  // 4 consumer warps + 1 producer warp
+constexpr int kRowsPerCta = 128;    // window rows (w, g) scored per CTA
+constexpr int kBoxBytes = 64 * 128;
+
+struct SnapK {
+  int W, G, Hq, Hkv, rows, RG, C, nchunk, kv_cap;
+  float sl2;
+  size_t off_part, off_scores;
+};
+
+template <int D>
+struct ScoreLayout {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStageBytes = kBoxes * kBoxBytes;
+  static constexpr int off_lse = kScoreStages * kStageBytes;  // float [128]
+  static constexpr int off_cs = off_lse + kRowsPerCta * 4;     // float [4][64]
+  static constexpr int off_bar = off_cs + 4 * 64 * 4;          // uint64 full[], empty[]
+  static constexpr int bytes = off_bar + 2 * kScoreStages * 8;
+  static constexpr int alloc = bytes + 1024;
+};
+
+template <int D, int PASS>
+__global__ void __launch_bounds__(kScoreThreads, 2)
+    snap_score_tc(const __grid_constant__ CUtensorMap kmap, const __nv_bfloat16 *__restrict__ qw,
+                  const int32_t *__restrict__ kv_len, unsigned char *__restrict__ ws, SnapK p) {
+  using Lay = ScoreLayout<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float *sm_lse = reinterpret_cast<float *>(smem + Lay::off_lse);
+  float *sm_cs = reinterpret_cast<float *>(smem + Lay::off_cs);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::off_bar);
+  uint64_t *empty = full + kScoreStages;
+  WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+  float2 *part = reinterpret_cast<float2 *>(ws + p.off_part);
+  float *scores = reinterpret_cast<float *>(ws + p.off_scores);
+
+  const int unit = blockIdx.x;
+  const int chunk = unit % p.nchunk;
+  const int prg = unit / p.nchunk;
+  const int rg = prg % p.RG;
+  const int pair = prg / p.RG;
+  const int hkv = pair % p.Hkv;
+  const int b = pair / p.Hkv;
+  const int L = kv_len[b];
+  if (L < p.W || L > p.kv_cap) {
+    if (threadIdx.x == 0 && chunk == 0 && rg == 0 && hkv == 0) raise_error(hdr, 0x2u);
+    return;
+  }
+  const int kend = (PASS == 1) ? L : L - p.W;
+  const int start = chunk * p.C;
+  if (start >= kend) return;
+  const int end = min(start + p.C, kend);
+  const int ntiles = (end - start + 63) / 64;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScoreStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 4) {  // producer
+    if (lane != 0) return;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = 0; t < ntiles; ++t) {
+      if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+        raise_error(hdr, 0x8u);
+        for (int s = 0; s < kScoreStages; ++s) mbar_wait(&full[s], phase);
+        return;
+      }
+      mbar_arrive_expect_tx(&full[stage], Lay::kStageBytes);
+#pragma unroll
+      for (int h = 0; h < Lay::kBoxes; ++h)
+        tma_load_4d(smem + stage * Lay::kStageBytes + h * kBoxBytes, &kmap, &full[stage], h * 64, start + 64 * t,
+                    hkv, b);
+      if (++stage == kScoreStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    return;
+  }
+
+  const int gid = lane >> 2, tig = lane & 3;
+  constexpr int KK = D / 16;
+  // ---- query fragments: A operand rows (mt, half) -> local row warp*32 + mt*16 + half*8 + gid
+  uint32_t qa[2][KK][4];
+  int pos[2][2];
+  float lr[2][2];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int r = rg * kRowsPerCta + warp * 32 + mt * 16 + hf * 8 + gid;
+      pos[mt][hf] = -1;
+      const __nv_bfloat16 *qr = nullptr;
+      if (r < p.rows) {
+        const int w = r / p.G, g = r % p.G;
+        pos[mt][hf] = L - p.W + w;
+        qr = qw + ((static_cast<size_t>(b) * p.W + w) * p.Hq + hkv * p.G + g) * D;
+      }
+#pragma unroll
+      for (int kk = 0; kk < KK; ++kk) {
+        const uint32_t x0 = qr ? *reinterpret_cast<const uint32_t *>(qr + 16 * kk + 2 * tig) : 0u;
+        const uint32_t x1 = qr ? *reinterpret_cast<const uint32_t *>(qr + 16 * kk + 8 + 2 * tig) : 0u;
+        qa[mt][kk][hf] = x0;      // a0 (row gid) / a1 (row gid+8)
+        qa[mt][kk][2 + hf] = x1;  // a2 / a3: columns +8
+      }
+    }
+  }
+  float m_run[2][2], l_run[2][2];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      m_run[mt][hf] = -INFINITY;
+      l_run[mt][hf] = 0.f;
+    }
+
+  if (PASS == 2) {
+    // log2-sum-exp of every window row from the pass-1 partials of all chunks
+    const int nch1 = (L + p.C - 1) / p.C;
+    if (threadIdx.x < kRowsPerCta) {
+      const int rl = threadIdx.x;
+      const int r = rg * kRowsPerCta + rl;
+      float v = INFINITY;  // padding rows: probability 0
+      if (r < p.rows) {
+        const float2 *pp = part + (static_cast<size_t>(pair * p.RG + rg) * p.nchunk) * kRowsPerCta + rl;
+        float M = -INFINITY;
+        for (int c = 0; c < nch1; ++c) M = fmaxf(M, pp[c * kRowsPerCta].x);
+        float S = 0.f;
+        for (int c = 0; c < nch1; ++c) {
+          const float2 x = pp[c * kRowsPerCta];
+          if (x.y > 0.f) S += x.y * exp2f(x.x - M);
+        }
+        v = M + log2f(S);
+      }
+      sm_lse[rl] = v;
+    }
+    named_bar(1, 128);
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) lr[mt][hf] = sm_lse[warp * 32 + mt * 16 + hf * 8 + gid];
+  }
+
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int t = 0; t < ntiles; ++t) {
+    if (!mbar_wait(&full[stage], phase)) {
+      raise_error(hdr, 0x8u);
+      return;
+    }
+    const int kt0 = start + 64 * t;
+    const uint32_t kbase = smem_addr(smem + stage * Lay::kStageBytes);
+    float s[2][8][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s[mt][nt][c] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KK; ++kk) {
+      const int d = 16 * kk + 8 * ((lane >> 3) & 1);
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        const int key = 16 * np + (lane & 7) + 8 * (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + (d >> 6) * kBoxBytes + swz128(key, (d & 63) >> 3), b0, b1, b2, b3);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          mma_bf16_16816(s[mt][2 * np], qa[mt][kk][0], qa[mt][kk][1], qa[mt][kk][2], qa[mt][kk][3], b0, b1);
+          mma_bf16_16816(s[mt][2 * np + 1], qa[mt][kk][0], qa[mt][kk][1], qa[mt][kk][2], qa[mt][kk][3], b2, b3);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == kScoreStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+
+    if (PASS == 1) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int key = kt0 + 8 * nt + 2 * tig + e;
+              float v = s[mt][nt][2 * hf + e] * p.sl2;
+              if (key > pos[mt][hf]) v = -INFINITY;
+              s[mt][nt][2 * hf + e] = v;
+              mx = fmaxf(mx, v);
+            }
+          mx = warp_max_xor(mx, 1, 2);
+          const float mn = fmaxf(m_run[mt][hf], mx);
+          const float mu = (mn == -INFINITY) ? 0.f : mn;
+          float acc = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) acc += exp2f(s[mt][nt][2 * hf + e] - mu);
+          l_run[mt][hf] = l_run[mt][hf] * exp2f(m_run[mt][hf] - mu) + acc;
+          m_run[mt][hf] = mn;
+        }
+    } else {
+      // column sums of exp2(s - lse) over this thread's 4 rows, then over the 8 row groups of the warp
+      float cs[8][2];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float acc = 0.f;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) acc += exp2f(s[mt][nt][2 * hf + e] * p.sl2 - lr[mt][hf]);
+          cs[nt][e] = warp_sum_xor(acc, 4, 16);
+        }
+      if (gid == 0) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) sm_cs[warp * 64 + 8 * nt + 2 * tig + e] = cs[nt][e];
+      }
+      named_bar(1, 128);
+      if (threadIdx.x < 64) {
+        const int key = kt0 + threadIdx.x;
+        if (key < end) {
+          const float v = sm_cs[threadIdx.x] + sm_cs[64 + threadIdx.x] + sm_cs[128 + threadIdx.x] +
+                          sm_cs[192 + threadIdx.x];
+          float *dst = scores + (static_cast<size_t>(b) * p.Hkv + hkv) * p.kv_cap + key;
+          if (p.RG == 1)
+            *dst = v;
+          else
+            atomicAdd(dst, v);
+        }
+      }
+      named_bar(1, 128);
+    }
+  }
+
+  if (PASS == 1) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const float l = warp_sum_xor(l_run[mt][hf], 1, 2);
+        if (tig == 0) {
+          const int rl = warp * 32 + mt * 16 + hf * 8 + gid;
+          part[(static_cast<size_t>(pair * p.RG + rg) * p.nchunk + chunk) * kRowsPerCta + rl] =
+              make_float2(m_run[mt][hf], l);
+        }
+      }
+  }
+}
+
+// ---------------------------------------------------------------- CUDA-core scoring
+template <typename Tin, int D>
+__global__ void __launch_bounds__(256)
+    snap_score_simt(const Tin *__restrict__ qw, const Tin *__restrict__ k, const int32_t *__restrict__ kv_len,
+                    int64_t bstride, int64_t hstride, unsigned char *__restrict__ ws, SnapK p) {
+  extern __shared__ float sm_lse2[];  // [rows]
+  __shared__ float red[2][8];
+  WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+  float *scores = reinterpret_cast<float *>(ws + p.off_scores);
+  const int b = blockIdx.x / p.Hkv, hkv = blockIdx.x % p.Hkv;
+  const int L = kv_len[b];
+  if (L < p.W || L > p.kv_cap) {
+    if (threadIdx.x == 0 && hkv == 0) raise_error(hdr, 0x2u);
+    return;
+  }
+  const Tin *kb = k + b * bstride + hkv * hstride;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = 0; r < p.rows; ++r) {
+    const int w = r / p.G, g = r % p.G;
+    const int posn = L - p.W + w;
+    const Tin *qr = qw + ((static_cast<size_t>(b) * p.W + w) * p.Hq + hkv * p.G + g) * D;
+    float m = -INFINITY, l = 0.f;
+    for (int j = threadIdx.x; j <= posn; j += 256) {
+      float dot = 0.f;
+      for (int d = 0; d < D; ++d) dot = fmaf(to_f32(qr[d]), to_f32(kb[static_cast<size_t>(j) * D + d]), dot);
+      const float v = dot * p.sl2;
+      if (v > m) {
+        l = l * exp2f(m - v) + 1.f;
+        m = v;
+      } else {
+        l += exp2f(v - m);
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      const float mn = fmaxf(m, m2);
+      const float mu = (mn == -INFINITY) ? 0.f : mn;
+      l = l * exp2f(m - mu) + l2 * exp2f(m2 - mu);
+      m = mn;
+    }
+    if (lane == 0) {
+      red[0][warp] = m;
+      red[1][warp] = l;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float M = -INFINITY;
+      for (int i = 0; i < 8; ++i) M = fmaxf(M, red[0][i]);
+      float S = 0.f;
+      for (int i = 0; i < 8; ++i) S += red[1][i] * exp2f(red[0][i] - M);
+      sm_lse2[r] = M + log2f(S);
+    }
+    __syncthreads();
+  }
+  const int n = L - p.W;
+  for (int j = threadIdx.x; j < n; j += 256) {
+    float acc = 0.f;
+    for (int r = 0; r < p.rows; ++r) {
+      const int w = r / p.G, g = r % p.G;
+      const Tin *qr = qw + ((static_cast<size_t>(b) * p.W + w) * p.Hq + hkv * p.G + g) * D;
+      float dot = 0.f;
+      for (int d = 0; d < D; ++d) dot = fmaf(to_f32(qr[d]), to_f32(kb[static_cast<size_t>(j) * D + d]), dot);
+      acc += exp2f(dot * p.sl2 - sm_lse2[r]);
+    }
+    scores[(static_cast<size_t>(b) * p.Hkv + hkv) * p.kv_cap + j] = acc;
+  }
+}
+
+// ---------------------------------------------------------------- select + gather
+constexpr int kSelThreads = 1024;
+
+struct SelParams {
+  int Hkv, W, pool, K, kv_cap, draft_cap, row_bytes;
+  int64_t bstride_bytes, hstride_bytes;
+};
+
+// Exclusive block scan of one unsigned per thread (kSelThreads threads); returns
+// the prefix and writes the block total to *total.
+__device__ unsigned block_excl_scan(unsigned v, unsigned *sm_warp, unsigned *total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned x = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned w = sm_warp[lane];
+    unsigned s = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    sm_warp[lane] = s - w;  // exclusive per-warp offsets
+    if (lane == 31) sm_warp[32] = s;
+  }
+  __syncthreads();
+  const unsigned r = sm_warp[warp] + x - v;
+  *total = sm_warp[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+    snap_select(const unsigned char *__restrict__ k, const unsigned char *__restrict__ v,
+                const int32_t *__restrict__ kv_len, SelParams sp, int32_t *__restrict__ sel_idx,
+                unsigned char *__restrict__ k_draft, unsigned char *__restrict__ v_draft,
+                int32_t *__restrict__ draft_len, float *__restrict__ scores_out, unsigned char *__restrict__ ws,
+                size_t off_scores, size_t off_pooled) {
+  __shared__ unsigned hist[2048];
+  __shared__ unsigned sm_warp[33];
+  __shared__ unsigned s_bin, s_above;
+  WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+  const int b = blockIdx.x / sp.Hkv, hkv = blockIdx.x % sp.Hkv;
+  const int L = kv_len[b];
+  const size_t pr = static_cast<size_t>(b) * sp.Hkv + hkv;
+  int32_t *sel = sel_idx + pr * sp.draft_cap;
+  if (L < sp.W || L > sp.kv_cap) {
+    for (int i = threadIdx.x; i < sp.draft_cap; i += kSelThreads) sel[i] = -1;
+    if (threadIdx.x == 0 && hkv == 0) {
+      draft_len[b] = 0;
+      raise_error(hdr, 0x2u);
+    }
+    return;
+  }
+  const float *s = reinterpret_cast<const float *>(ws + off_scores) + pr * sp.kv_cap;
+  float *pooled = reinterpret_cast<float *>(ws + off_pooled) + pr * sp.kv_cap;
+  const int n = L - sp.W;
+  const int Keff = min(sp.K, L);
+  const int ktop = Keff - sp.W;
+  const int r = sp.pool / 2;
+
+  // ---- 1. max-pool (and the optional copy out)
+  for (int j = threadIdx.x; j < n; j += kSelThreads) {
+    float m = s[j];
+    const int lo = max(0, j - r), hi = min(n - 1, j + r);
+    for (int t = lo; t <= hi; ++t) m = fmaxf(m, s[t]);
+    pooled[j] = m;
+    if (scores_out) scores_out[pr * sp.kv_cap + j] = m;
+  }
+  __syncthreads();
+
+  // ---- 2. radix select of the ktop-th largest pooled value (scores are >= 0,
+  //         so their IEEE bit patterns order like the values)
+  unsigned prefix = 0u, mask = 0u, krem = static_cast<unsigned>(ktop);
+  const bool partial = (ktop > 0 && ktop < n);
+  if (partial) {
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = (pass == 0) ? 21 : (pass == 1) ? 10 : 0;
+      const int nb = (pass == 2) ? 1024 : 2048;
+      for (int i = threadIdx.x; i < nb; i += kSelThreads) hist[i] = 0u;
+      __syncthreads();
+      for (int j = threadIdx.x; j < n; j += kSelThreads) {
+        const unsigned key = __float_as_uint(pooled[j]);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      // bins in descending order, two per thread
+      const int b_hi = nb - 1 - 2 * threadIdx.x;
+      const int b_lo = b_hi - 1;
+      const unsigned c_hi = (b_hi >= 0) ? hist[b_hi] : 0u;
+      const unsigned c_lo = (b_lo >= 0) ? hist[b_lo] : 0u;
+      unsigned tot;
+      const unsigned above = block_excl_scan(c_hi + c_lo, sm_warp, &tot);
+      if (b_hi >= 0 && above < krem && krem <= above + c_hi) {
+        s_bin = b_hi;
+        s_above = above;
+      } else if (b_lo >= 0 && above + c_hi < krem && krem <= above + c_hi + c_lo) {
+        s_bin = b_lo;
+        s_above = above + c_hi;
+      }
+      __syncthreads();
+      prefix |= s_bin << shift;
+      mask |= static_cast<unsigned>(nb - 1) << shift;
+      krem -= s_above;
+      __syncthreads();
+    }
+  }
+  // ---- 3. ordered compaction: position of j = #(greater before j) + min(#(equal before j), krem)
+  const unsigned tau = prefix;
+  unsigned run_gt = 0u, run_eq = 0u;
+  for (int base = 0; base < n; base += kSelThreads) {
+    const int j = base + threadIdx.x;
+    unsigned gt = 0u, eq = 0u;
+    if (j < n) {
+      if (!partial) {
+        gt = (ktop >= n) ? 1u : 0u;  // keep all or nothing
+      } else {
+        const unsigned key = __float_as_uint(pooled[j]);
+        gt = key > tau;
+        eq = key == tau;
+      }
+    }
+    unsigned tot;
+    const unsigned pre = block_excl_scan((gt << 16) | eq, sm_warp, &tot);
+    const unsigned g_before = run_gt + (pre >> 16), e_before = run_eq + (pre & 0xffffu);
+    if (gt || (eq && e_before < krem)) sel[g_before + min(e_before, krem)] = j;
+    run_gt += tot >> 16;
+    run_eq += tot & 0xffffu;
+  }
+  for (int w = threadIdx.x; w < sp.W; w += kSelThreads) sel[ktop + w] = n + w;
+  for (int i = Keff + threadIdx.x; i < sp.draft_cap; i += kSelThreads) sel[i] = -1;
+  if (threadIdx.x == 0 && hkv == 0) draft_len[b] = Keff;
+  __syncthreads();
+
+  // ---- 4. gather the kept rows (16-byte vectors)
+  const int vecs = sp.row_bytes / 16;
+  const unsigned char *ks = k + b * sp.bstride_bytes + hkv * sp.hstride_bytes;
+  const unsigned char *vs = v + b * sp.bstride_bytes + hkv * sp.hstride_bytes;
+  unsigned char *kd = k_draft + pr * sp.draft_cap * sp.row_bytes;
+  unsigned char *vd = v_draft + pr * sp.draft_cap * sp.row_bytes;
+  for (int i = threadIdx.x; i < Keff * vecs; i += kSelThreads) {
+    const int row = i / vecs, c = i % vecs;
+    const size_t src = static_cast<size_t>(sel[row]) * sp.row_bytes + c * 16;
+    const size_t dst = static_cast<size_t>(row) * sp.row_bytes + c * 16;
+    *reinterpret_cast<uint4 *>(kd + dst) = __ldg(reinterpret_cast<const uint4 *>(ks + src));
+    *reinterpret_cast<uint4 *>(vd + dst) = __ldg(reinterpret_cast<const uint4 *>(vs + src));
+  }
+}
+
+}  // namespace
+
+SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W) {
+  SnapPlan p{};
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.kv_cap = kv_cap;
+  p.W = W;
+  p.G = Hq / Hkv;
+  p.rows = p.G * W;
+  p.RG = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
+  p.pairs = B * Hkv;
+  const int slots = 2 * current_sm_count();
+  int C = 4096;
+  const int cmin = std::max(256, ((kv_cap + 63) / 64 + 63) / 64 * 64);
+  while (C > cmin && static_cast<long long>(p.pairs) * p.RG * ((kv_cap + C - 1) / C) < 8LL * slots) C /= 2;
+  if (C < cmin) C = cmin;
+  p.C = C;
+  p.nchunk = (kv_cap + C - 1) / C;
+  size_t off = kAlign;
+  p.off_part = off;
+  off = align_up(off + sizeof(float2) * static_cast<size_t>(p.pairs) * p.RG * p.nchunk * kRowsPerCta);
+  p.off_scores = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(p.pairs) * kv_cap);
+  p.off_pooled = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(p.pairs) * kv_cap);
+  p.ws_bytes = off;
+  return p;
+}
+
+cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, const CUtensorMap *kmap) {
+  cudaError_t e = cudaMemsetAsync(a.ws, 0, kAlign, a.stream);
+  if (e != cudaSuccess) return e;
+  unsigned char *ws = static_cast<unsigned char *>(a.ws);
+  SnapK kp;
+  kp.W = p.W;
+  kp.G = p.G;
+  kp.Hq = p.Hq;
+  kp.Hkv = p.Hkv;
+  kp.rows = p.rows;
+  kp.RG = p.RG;
+  kp.C = p.C;
+  kp.nchunk = p.nchunk;
+  kp.kv_cap = p.kv_cap;
+  kp.sl2 = a.sm_scale * kLog2e;
+  kp.off_part = p.off_part;
+  kp.off_scores = p.off_scores;
+  if (in_f32 || kmap == nullptr) {
+    const size_t smem = sizeof(float) * p.rows;
+    if (in_f32) {
+      if (p.D == 128)
+        snap_score_simt<float, 128><<<p.pairs, 256, smem, a.stream>>>(
+            static_cast<const float *>(a.q_win), static_cast<const float *>(a.k), a.kv_len, a.kv_batch_stride,
+            a.kv_head_stride, ws, kp);
+      else
+        snap_score_simt<float, 64><<<p.pairs, 256, smem, a.stream>>>(
+            static_cast<const float *>(a.q_win), static_cast<const float *>(a.k), a.kv_len, a.kv_batch_stride,
+            a.kv_head_stride, ws, kp);
+    } else {
+      if (p.D == 128)
+        snap_score_simt<__nv_bfloat16, 128><<<p.pairs, 256, smem, a.stream>>>(
+            static_cast<const __nv_bfloat16 *>(a.q_win), static_cast<const __nv_bfloat16 *>(a.k), a.kv_len,
+            a.kv_batch_stride, a.kv_head_stride, ws, kp);
+      else
+        snap_score_simt<__nv_bfloat16, 64><<<p.pairs, 256, smem, a.stream>>>(
+            static_cast<const __nv_bfloat16 *>(a.q_win), static_cast<const __nv_bfloat16 *>(a.k), a.kv_len,
+            a.kv_batch_stride, a.kv_head_stride, ws, kp);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else {
+    if (p.RG > 1) {
+      e = cudaMemsetAsync(ws + p.off_scores, 0, p.off_pooled - p.off_scores, a.stream);
+      if (e != cudaSuccess) return e;
+    }
+    const int units = p.pairs * p.RG * p.nchunk;
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q_win);
+#define MGD_SCORE(DD, PP)                                                                                   \
+  do {                                                                                                      \
+    auto kern = snap_score_tc<DD, PP>;                                                                      \
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ScoreLayout<DD>::alloc);    \
+    if (e != cudaSuccess) return e;                                                                         \
+    kern<<<units, kScoreThreads, ScoreLayout<DD>::alloc, a.stream>>>(*kmap, q, a.kv_len, ws, kp);           \
+    e = cudaGetLastError();                                                                                 \
+    if (e != cudaSuccess) return e;                                                                         \
+  } while (0)
+    if (p.D == 128) {
+      MGD_SCORE(128, 1);
+      MGD_SCORE(128, 2);
+    } else {
+      MGD_SCORE(64, 1);
+      MGD_SCORE(64, 2);
+    }
+#undef MGD_SCORE
+  }
+  SelParams sp;
+  sp.Hkv = p.Hkv;
+  sp.W = p.W;
+  sp.pool = a.pool;
+  sp.K = a.K;
+  sp.kv_cap = p.kv_cap;
+  sp.draft_cap = a.draft_cap;
+  sp.row_bytes = p.D * (in_f32 ? 4 : 2);
+  sp.bstride_bytes = a.kv_batch_stride * (in_f32 ? 4 : 2);
+  sp.hstride_bytes = a.kv_head_stride * (in_f32 ? 4 : 2);
+  snap_select<<<p.pairs, kSelThreads, 0, a.stream>>>(
+      static_cast<const unsigned char *>(a.k), static_cast<const unsigned char *>(a.v), a.kv_len, sp, a.sel_idx,
+      static_cast<unsigned char *>(a.k_draft), static_cast<unsigned char *>(a.v_draft), a.draft_len, a.scores_out,
+      ws, p.off_scores, p.off_pooled);
+  return cudaGetLastError();
+}
+
+}  // namespace mgd

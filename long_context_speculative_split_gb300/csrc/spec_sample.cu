@@ -1,0 +1,371 @@
+// Draft-token draw and modified rejection sampling over vocab-sized float32
+// distributions.
+//
+// "Wann beschleunigt spekulatives Decoding das LLM-Serving?", section "Eine
+// Verifizierungsrunde verstehen": candidates are accepted left to right using
+// both distributions; at the first rejection a correction is drawn from the
+// residual target distribution and later candidates are dropped; if all are
+// accepted one more target token is drawn.  The paragraph after it: this
+// preserves the target distribution.
+//
+// Two kernels per call:
+//   1. spec_stats: (max, sum of exp) of every logit row the mode needs, each
+//      row split over several CTAs (HBM stream, float4 loads);
+//   2. spec_finish: one CTA per sequence merges the row statistics, walks the
+//      acceptance chain (u1 * q(x) < p(x)), then draws the correction / bonus
+//      (or, in draft mode, the draft token) by inverse CDF: 32 warps each sum
+//      a contiguous slice of the weights, a double-precision prefix over the
+//      32 slice totals finds the slice holding u * Z, and that warp rescans
+//      its slice with warp scans to find the first index whose running sum
+//      exceeds u * Z.
+#include "common.cuh"
+
+namespace mgd {
+namespace {
+
+constexpr int kStatThreads = 256;
+constexpr int kFinThreads = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct StatParams {
+  int B, gamma, V, split, nsplit, nrows;
+  int r_begin, nr;  // rows [r_begin, r_begin + nr) of every sequence (unified row index)
+};
+
+// unified row r of sequence b: r <= gamma -> target row r, else draft row r - gamma - 1
+__device__ __forceinline__ const float *row_ptr(const float *target, const float *draft, int b, int r, int gamma,
+                                                int V) {
+  if (r <= gamma) return target + (static_cast<size_t>(b) * (gamma + 1) + r) * V;
+  return draft + (static_cast<size_t>(b) * gamma + (r - gamma - 1)) * V;
+}
+
+template <bool VEC4>
+__global__ void __launch_bounds__(kStatThreads) spec_stats_kernel(const float *__restrict__ target,
+                                                                   const float *__restrict__ draft, StatParams sp,
+                                                                   float2 *__restrict__ stats) {
+  const int b = blockIdx.x / sp.nr;
+  const int r = sp.r_begin + blockIdx.x % sp.nr;
+  const int s = blockIdx.y;
+  const float *x = row_ptr(target, draft, b, r, sp.gamma, sp.V);
+  const int lo = s * sp.split;
+  const int hi = min(lo + sp.split, sp.V);
+  float m = -INFINITY, l = 0.f;
+  auto add = [&](float v) {
+    if (v > m) {
+      l = l * exp2f((m - v) * kLog2e) + 1.f;
+      m = v;
+    } else if (v != -INFINITY) {
+      l += exp2f((v - m) * kLog2e);
+    }
+  };
+  if (VEC4) {
+    for (int i = lo + 4 * threadIdx.x; i < hi; i += 4 * kStatThreads) {
+      const float4 v = __ldcs(reinterpret_cast<const float4 *>(x + i));
+      add(v.x);
+      add(v.y);
+      add(v.z);
+      add(v.w);
+    }
+  } else {
+    for (int i = lo + threadIdx.x; i < hi; i += kStatThreads) add(__ldcs(x + i));
+  }
+  // block reduce of (m, l)
+  __shared__ float sm[2][kStatThreads / 32];
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+    const float mn = fmaxf(m, m2);
+    const float mu = (mn == -INFINITY) ? 0.f : mn;
+    l = l * exp2f((m - mu) * kLog2e) + l2 * exp2f((m2 - mu) * kLog2e);
+    m = mn;
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    sm[0][w] = m;
+    sm[1][w] = l;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int i = 0; i < kStatThreads / 32; ++i) M = fmaxf(M, sm[0][i]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float Lt = 0.f;
+    for (int i = 0; i < kStatThreads / 32; ++i) Lt += sm[1][i] * exp2f((sm[0][i] - Mu) * kLog2e);
+    stats[(static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit + s] = make_float2(M, Lt);
+  }
+}
+
+// Weights of a draw: MODE 0 -> exp(a - Ma) (an unnormalised softmax);
+// MODE 1 -> max(0, exp(a - Ma) * ia - exp(c - Mc) * ic) (residual p - q).
+struct DrawSrc {
+  const float *a;
+  const float *c;
+  float Ma, ia, Mc, ic;
+  int mode;
+};
+
+__device__ __forceinline__ float draw_weight(const DrawSrc &s, int i) {
+  const float pa = exp2f((__ldg(s.a + i) - s.Ma) * kLog2e);
+  if (s.mode == 0) return pa;
+  const float pc = exp2f((__ldg(s.c + i) - s.Mc) * kLog2e);
+  return fmaxf(0.f, pa * s.ia - pc * s.ic);
+}
+
+struct DrawShared {
+  float tot[32];
+  int last[32];
+  double base;
+  double target;
+  int wstar;
+  int idx;
+  int status;  // 0 ok, 1 total weight is zero
+};
+
+// Block-wide inverse-CDF draw (kFinThreads threads).  Returns the index, or -1
+// when the weights sum to zero.
+template <bool VEC4>
+__device__ int block_draw(const DrawSrc &src, int V, float u, DrawShared &sh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = ((V + 32 * 128 - 1) / (32 * 128)) * 128;  // slice per warp, multiple of 128
+  const int lo = warp * per, hi = min(lo + per, V);
+  float sum = 0.f;
+  int last = -1;
+  for (int i = lo + 4 * lane; i < hi; i += 128) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (i + e < hi) {
+        const float w = draw_weight(src, i + e);
+        sum += w;
+        if (w > 0.f) last = i + e;
+      }
+    }
+  }
+  sum = warp_sum_xor(sum, 1, 16);
+  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  if (lane == 0) {
+    sh.tot[warp] = sum;
+    sh.last[warp] = last;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double Z = 0.0;
+    for (int w = 0; w < 32; ++w) Z += static_cast<double>(sh.tot[w]);
+    sh.status = (Z > 0.0) ? 0 : 1;
+    const double target = static_cast<double>(u) * Z;
+    double run = 0.0;
+    int ws = -1;
+    double base = 0.0;
+    for (int w = 0; w < 32; ++w) {
+      if (sh.tot[w] > 0.f && run + static_cast<double>(sh.tot[w]) > target) {
+        ws = w;
+        base = run;
+        break;
+      }
+      run += static_cast<double>(sh.tot[w]);
+    }
+    if (ws < 0) {  // rounding pushed u*Z past the total: last slice with mass
+      for (int w = 31; w >= 0; --w)
+        if (sh.tot[w] > 0.f) {
+          ws = w;
+          break;
+        }
+      base = run;  // forces the fallback below
+      if (ws >= 0) base = target + 1.0;
+    }
+    sh.wstar = ws;
+    sh.base = base;
+    sh.target = target;
+    sh.idx = -1;
+  }
+  __syncthreads();
+  if (sh.status != 0) return -1;
+  if (warp == sh.wstar) {
+    double run = sh.base;
+    const double target = sh.target;
+    int found = -1;
+    if (run <= target) {
+      for (int i0 = lo; i0 < hi && found < 0; i0 += 128) {
+        float w4[4];
+        float ls = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = i0 + 4 * lane + e;
+          w4[e] = (i < hi) ? draw_weight(src, i) : 0.f;
+          ls += w4[e];
+        }
+        float incl = ls;
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const bool cross = (run + static_cast<double>(incl)) > target;
+        const unsigned bal = __ballot_sync(0xffffffffu, cross);
+        if (bal) {
+          const int fl = __ffs(bal) - 1;
+          if (lane == fl) {
+            double c = run + static_cast<double>(incl - ls);
+            int pick = -1;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              c += static_cast<double>(w4[e]);
+              if (pick < 0 && w4[e] > 0.f && c > target) pick = i0 + 4 * lane + e;
+            }
+            if (pick < 0) {  // crossing straddled by rounding: last positive weight of this lane
+              for (int e = 3; e >= 0; --e)
+                if (w4[e] > 0.f) {
+                  pick = i0 + 4 * lane + e;
+                  break;
+                }
+            }
+            sh.idx = pick;
+          }
+          found = 1;
+        } else {
+          run += static_cast<double>(__shfl_sync(0xffffffffu, incl, 31));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && sh.idx < 0) sh.idx = sh.last[warp];
+  }
+  __syncthreads();
+  return sh.idx;
+}
+
+__device__ __forceinline__ void merge_stats(const float2 *st, int nsplit, float &M, float &Z) {
+  M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, st[s].x);
+  Z = 0.f;
+  for (int s = 0; s < nsplit; ++s) Z += st[s].y * exp2f((st[s].x - M) * kLog2e);
+}
+
+template <bool VEC4>
+__global__ void __launch_bounds__(kFinThreads) spec_finish_kernel(const float *__restrict__ target,
+                                                                   const float *__restrict__ draft,
+                                                                   int32_t *__restrict__ draft_tokens,
+                                                                   const float *__restrict__ u, StatParams sp,
+                                                                   int mode, int32_t *__restrict__ out_tokens,
+                                                                   int32_t *__restrict__ num_accepted,
+                                                                   const float2 *__restrict__ stats, WsHeader *hdr) {
+  __shared__ float sM[33], sZ[33];
+  __shared__ int s_j;
+  __shared__ DrawShared sh;
+  const int b = blockIdx.x;
+  const int g = sp.gamma, V = sp.V;
+  for (int r = sp.r_begin + threadIdx.x; r < sp.r_begin + sp.nr; r += kFinThreads)
+    merge_stats(stats + (static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit, sp.nsplit, sM[r], sZ[r]);
+  __syncthreads();
+
+  if (mode == 1) {  // draft draw: row s uses draft row s, uniform slot 0
+    for (int r = sp.r_begin; r < sp.r_begin + sp.nr; ++r) {
+      const int s = r - g - 1;
+      DrawSrc src{row_ptr(target, draft, b, r, g, V), nullptr, sM[r], 1.f, 0.f, 0.f, 0};
+      const float uu = u[(static_cast<size_t>(b) * (g + 1) + s) * 3 + 0];
+      const int tok = block_draw<VEC4>(src, V, uu, sh);
+      if (threadIdx.x == 0) draft_tokens[static_cast<size_t>(b) * g + s] = tok;
+      __syncthreads();
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    int j = g;
+    for (int i = 0; i < g; ++i) {
+      const int x = draft_tokens[static_cast<size_t>(b) * g + i];
+      if (x < 0 || x >= V) {
+        raise_error(hdr, 0x4u);
+        j = i;
+        break;
+      }
+      const float *t = row_ptr(target, draft, b, i, g, V);
+      const float *d = row_ptr(target, draft, b, g + 1 + i, g, V);
+      const float px = exp2f((t[x] - sM[i]) * kLog2e) / sZ[i];
+      const float qx = exp2f((d[x] - sM[g + 1 + i]) * kLog2e) / sZ[g + 1 + i];
+      const float u1 = u[(static_cast<size_t>(b) * (g + 1) + i) * 3 + 1];
+      if (!(u1 * qx < px)) {
+        j = i;
+        break;
+      }
+      out_tokens[static_cast<size_t>(b) * (g + 1) + i] = x;
+    }
+    s_j = j;
+    num_accepted[b] = j;
+  }
+  __syncthreads();
+  const int j = s_j;
+  const float uu = u[(static_cast<size_t>(b) * (g + 1) + j) * 3 + 2];
+  int tok;
+  if (j < g) {
+    DrawSrc src{row_ptr(target, draft, b, j, g, V), row_ptr(target, draft, b, g + 1 + j, g, V), sM[j],
+                1.f / sZ[j], sM[g + 1 + j], 1.f / sZ[g + 1 + j], 1};
+    tok = block_draw<VEC4>(src, V, uu, sh);
+    if (tok < 0) {  // the residual vanished through rounding: draw from p_j
+      DrawSrc sp2{row_ptr(target, draft, b, j, g, V), nullptr, sM[j], 1.f, 0.f, 0.f, 0};
+      tok = block_draw<VEC4>(sp2, V, uu, sh);
+    }
+  } else {
+    DrawSrc src{row_ptr(target, draft, b, g, g, V), nullptr, sM[g], 1.f, 0.f, 0.f, 0};
+    tok = block_draw<VEC4>(src, V, uu, sh);
+  }
+  if (threadIdx.x == 0) {
+    out_tokens[static_cast<size_t>(b) * (g + 1) + j] = tok;
+    for (int i = j + 1; i <= g; ++i) out_tokens[static_cast<size_t>(b) * (g + 1) + i] = -1;
+  }
+}
+
+}  // namespace
+
+SpecPlan plan_spec(int B, int gamma, int V) {
+  SpecPlan p{};
+  p.B = B;
+  p.gamma = gamma;
+  p.V = V;
+  p.split = 16384;
+  p.nsplit = (V + p.split - 1) / p.split;
+  p.nrows = 2 * gamma + 1;
+  p.off_stats = kAlign;
+  p.ws_bytes = align_up(p.off_stats + sizeof(float2) * static_cast<size_t>(B) * p.nrows * p.nsplit);
+  return p;
+}
+
+cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
+  cudaError_t e = cudaMemsetAsync(a.ws, 0, kAlign, a.stream);
+  if (e != cudaSuccess) return e;
+  StatParams sp;
+  sp.B = p.B;
+  sp.gamma = p.gamma;
+  sp.V = p.V;
+  sp.split = p.split;
+  sp.nsplit = p.nsplit;
+  sp.nrows = p.nrows;
+  if (a.mode == 0) {
+    sp.r_begin = 0;
+    sp.nr = p.nrows;
+  } else if (a.row < 0) {
+    sp.r_begin = p.gamma + 1;
+    sp.nr = p.gamma;
+  } else {
+    sp.r_begin = p.gamma + 1 + a.row;
+    sp.nr = 1;
+  }
+  float2 *stats = reinterpret_cast<float2 *>(static_cast<unsigned char *>(a.ws) + p.off_stats);
+  WsHeader *hdr = static_cast<WsHeader *>(a.ws);
+  const bool vec4 = (p.V % 4) == 0 && (reinterpret_cast<uintptr_t>(a.draft) % 16) == 0 &&
+                    (a.target == nullptr || (reinterpret_cast<uintptr_t>(a.target) % 16) == 0);
+  dim3 g1(p.B * sp.nr, p.nsplit);
+  if (vec4)
+    spec_stats_kernel<true><<<g1, kStatThreads, 0, a.stream>>>(a.target, a.draft, sp, stats);
+  else
+    spec_stats_kernel<false><<<g1, kStatThreads, 0, a.stream>>>(a.target, a.draft, sp, stats);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (vec4)
+    spec_finish_kernel<true><<<p.B, kFinThreads, 0, a.stream>>>(a.target, a.draft, a.draft_tokens, a.u, sp, a.mode,
+                                                               a.out_tokens, a.num_accepted, stats, hdr);
+  else
+    spec_finish_kernel<false><<<p.B, kFinThreads, 0, a.stream>>>(a.target, a.draft, a.draft_tokens, a.u, sp, a.mode,
+                                                                a.out_tokens, a.num_accepted, stats, hdr);
+  return cudaGetLastError();
+}
+
+}  // namespace mgd

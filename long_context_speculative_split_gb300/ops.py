@@ -1,0 +1,124 @@
+"""Tensor-level wrappers over the C ABI: infer shapes and strides from torch
+tensors, allocate outputs and workspaces with torch (device memory only) and
+call ``mgd``.  No arithmetic of the method happens here.
+"""
+import math
+
+import torch
+
+from . import mgd
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return mgd.MGD_BF16
+    if t.dtype == torch.float32:
+        return mgd.MGD_F32
+    raise TypeError("unsupported dtype %s (bfloat16 or float32)" % t.dtype)
+
+
+def _kv_strides(k, v, D):
+    if k.stride(3) != 1 or k.stride(2) != D or k.stride() != v.stride():
+        raise ValueError("K and V must share strides with contiguous rows of D elements")
+    return k.stride(0), k.stride(1)
+
+
+def workspace(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def verify_attn(q, k, v, kv_len, sm_scale=None, out_dtype=torch.float32, ws=None, out=None, lse=None,
+                stream=None):
+    """q [B,T,Hq,D], k/v [B,Hkv,kv_cap,D] (same dtype), kv_len [B] int32 -> (out [B,T,Hq,D], lse [B,T,Hq])."""
+    B, T, Hq, D = q.shape
+    Hkv, cap = k.shape[1], k.shape[2]
+    sb, sh = _kv_strides(k, v, D)
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
+    if out is None:
+        out = torch.empty((B, T, Hq, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+    need = mgd.mgd_verify_workspace_size(B, T, Hq, Hkv, D, cap)
+    if ws is None:
+        ws = workspace(need, q.device)
+    mgd.mgd_verify_attn(q, k, v, kv_len, B, T, Hq, Hkv, D, cap, sb, sh, scale, _dtype_code(q), out,
+                        _dtype_code(out), lse, ws, ws.numel(), stream)
+    return out, lse
+
+
+def draft_attn(q, k_draft, v_draft, draft_len, sm_scale=None, out_dtype=torch.float32, ws=None, out=None,
+               lse=None, stream=None):
+    """q [B,Hq,D] or [B,1,Hq,D], compacted k/v [B,Hkv,k_cap,D], draft_len [B] -> (out [B,Hq,D], lse [B,Hq])."""
+    if q.dim() == 4:
+        q = q[:, 0]
+    B, Hq, D = q.shape
+    Hkv, cap = k_draft.shape[1], k_draft.shape[2]
+    sb, sh = _kv_strides(k_draft, v_draft, D)
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = mgd.mgd_draft_workspace_size(B, Hq, Hkv, D, cap)
+    if ws is None:
+        ws = workspace(need, q.device)
+    mgd.mgd_draft_attn(q, k_draft, v_draft, draft_len, B, Hq, Hkv, D, cap, sb, sh, scale, _dtype_code(q), out,
+                       _dtype_code(out), lse, ws, ws.numel(), stream)
+    return out, lse
+
+
+def snapkv_select(q_win, k, v, kv_len, W, pool, K, draft_cap=None, sm_scale=None, ws=None, want_scores=False,
+                  out=None, stream=None):
+    """Returns dict(sel_idx [B,Hkv,draft_cap] int32, k_draft, v_draft [B,Hkv,draft_cap,D], draft_len [B],
+    scores [B,Hkv,kv_cap] float32 or None)."""
+    B, Wq, Hq, D = q_win.shape
+    assert Wq == W
+    Hkv, cap = k.shape[1], k.shape[2]
+    sb, sh = _kv_strides(k, v, D)
+    cap_d = K if draft_cap is None else draft_cap
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
+    dev = q_win.device
+    if out is None:
+        out = dict(sel_idx=torch.empty((B, Hkv, cap_d), dtype=torch.int32, device=dev),
+                   k_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
+                   v_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
+                   draft_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                   scores=torch.zeros((B, Hkv, cap), dtype=torch.float32, device=dev) if want_scores else None)
+    need = mgd.mgd_snapkv_workspace_size(B, Hq, Hkv, D, cap, W)
+    if ws is None:
+        ws = workspace(need, dev)
+    mgd.mgd_snapkv_select(q_win, k, v, kv_len, B, Hq, Hkv, D, cap, sb, sh, W, pool, K, scale, _dtype_code(k),
+                          out["sel_idx"], out["k_draft"], out["v_draft"], cap_d, out["draft_len"], out["scores"],
+                          ws, ws.numel(), stream)
+    return out
+
+
+def draft_draw(draft_logits, u, draft_tokens=None, row=-1, ws=None, stream=None):
+    """Fill draft_tokens [B, gamma] from softmax(draft_logits[b, s]) with u[b, s, 0] (row < 0: every s)."""
+    B, gamma, V = draft_logits.shape
+    if draft_tokens is None:
+        draft_tokens = torch.full((B, gamma), -1, dtype=torch.int32, device=draft_logits.device)
+    need = mgd.mgd_spec_workspace_size(B, gamma, V)
+    if ws is None:
+        ws = workspace(need, draft_logits.device)
+    mgd.mgd_spec_sample(None, draft_logits, draft_tokens, u, B, gamma, V, mgd.MGD_DRAW_DRAFT, row, None, None, ws,
+                        ws.numel(), stream)
+    return draft_tokens
+
+
+def rejection_sample(target_logits, draft_logits, draft_tokens, u, ws=None, out_tokens=None, num_accepted=None,
+                     stream=None):
+    """-> (out_tokens [B, gamma+1] int32 (-1 padded), num_accepted [B] int32)."""
+    B, gp1, V = target_logits.shape
+    gamma = gp1 - 1
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, gp1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    need = mgd.mgd_spec_workspace_size(B, gamma, V)
+    if ws is None:
+        ws = workspace(need, dev)
+    mgd.mgd_spec_sample(target_logits, draft_logits, draft_tokens, u, B, gamma, V, mgd.MGD_VERIFY, -1, out_tokens,
+                        num_accepted, ws, ws.numel(), stream)
+    return out_tokens, num_accepted

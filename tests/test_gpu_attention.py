@@ -1,0 +1,174 @@
+"""GPU parity of verify and draft attention (C ABI via the binding) against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from _parity import assert_attention_close, assert_lse_close, gpu_or_skip, to64
+from long_context_speculative_split_gb300 import mgd, ops
+from long_context_speculative_split_gb300 import workloads as wl
+from oracle.attention import attention as ref_attention
+from oracle.attention import draft_attention as ref_draft
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(B, T, Hq, Hkv, D, lens, cap, seed, dtype=torch.bfloat16, hh=True):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, T, Hq, D), generator=g).to(dtype)
+    k = torch.randn((B, Hkv, cap, D), generator=g)
+    v = torch.randn((B, Hkv, cap, D), generator=g)
+    if hh:  # a few heavy-hitter keys per head
+        for b in range(B):
+            idx = torch.randperm(lens[b], generator=g)[: max(1, lens[b] // 100)]
+            k[b, :, idx] *= 8
+    return q, k.to(dtype), v.to(dtype), torch.tensor(lens, dtype=torch.int32)
+
+
+CASES = [
+    # B, T, Hq, Hkv, D, lens, cap
+    (2, 4, 32, 8, 128, [1000, 77], 1000),          # G*T = 16 rows, several chunks + merge
+    (3, 5, 32, 8, 128, [4101, 64, 129], 4101),     # 20 rows, ragged tails, one-tile and tile+1
+    (2, 1, 8, 2, 128, [513, 1], 513),              # draft form, a single key
+    (2, 3, 32, 8, 64, [300, 3], 300),              # head_dim 64, kv_len == T
+    (1, 8, 16, 4, 128, [2000], 2048),              # 32 rows (four n8 tiles)
+    (2, 5, 64, 8, 128, [700, 650], 700),           # 40 rows -> two row groups
+    (2, 2, 4, 4, 128, [5000, 4999], 5000),         # MHA (G=1), many chunks
+    (1, 4, 32, 8, 128, [64], 64),                  # exactly one tile
+    (1, 4, 32, 8, 128, [65], 128),                 # one key into the second tile
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%d_T%d_G%d_D%d_L%s" % (c[0], c[1], c[2] // c[3], c[4],
+                                                                                  "-".join(map(str, c[5]))))
+def test_verify_bf16_matches_oracle(case):
+    dev = gpu_or_skip()
+    B, T, Hq, Hkv, D, lens, cap = case
+    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=sum(lens) + T)
+    out, lse = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev))
+    torch.cuda.synchronize()
+    ref, ref_lse = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(D))
+    assert_attention_close(out, ref)
+    assert_lse_close(lse, ref_lse)
+
+
+def test_verify_bf16_output_dtype():
+    dev = gpu_or_skip()
+    q, k, v, kv_len = _case(2, 4, 32, 8, 128, [900, 333], 900, seed=5)
+    out, _ = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev), out_dtype=torch.bfloat16)
+    ref, _ = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(128))
+    g = to64(out)
+    # bf16 output adds its own rounding (2^-9 relative): checked against that bound
+    assert np.abs(g - ref).max() <= 2e-2
+    assert np.linalg.norm(g - ref) / np.linalg.norm(ref) <= 5e-3
+
+
+def test_verify_float32_tiny_config_full():
+    dev = gpu_or_skip()
+    c = wl.CONFIGS[1]
+    kv_len = wl.lengths(c)
+    k, v = wl.kv_cache(c, dev, kv_len=kv_len)
+    q = wl.queries(c, dev)
+    out, lse = ops.verify_attn(q, k, v, kv_len.to(dev))
+    ref, ref_lse = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(c["D"]))
+    assert_attention_close(out, ref)
+    assert_lse_close(lse, ref_lse)
+
+
+def test_draft_float32_tiny_config_full():
+    dev = gpu_or_skip()
+    c = wl.CONFIGS[1]
+    kv_len = wl.lengths(c)
+    k, v = wl.kv_cache(c, dev, kv_len=kv_len)
+    qd = wl.draft_queries(c, dev)
+    dlen = torch.tensor([64, 37], dtype=torch.int32)
+    kd, vd = k[:, :, :64].contiguous(), v[:, :, :64].contiguous()
+    out, lse = ops.draft_attn(qd, kd, vd, dlen.to(dev))
+    ref, ref_lse = ref_draft(qd, kd, vd, dlen, 1.0 / math.sqrt(c["D"]))
+    assert_attention_close(out, ref[:, 0])
+    assert_lse_close(lse, ref_lse[:, 0])
+
+
+@pytest.mark.parametrize("lens,cap", [([1024, 700, 1], 1024), ([516, 512, 64, 65], 516)])
+def test_draft_bf16_matches_oracle(lens, cap):
+    dev = gpu_or_skip()
+    B = len(lens)
+    q, k, v, dlen = _case(B, 1, 32, 8, 128, lens, cap, seed=cap)
+    out, lse = ops.draft_attn(q.to(dev), k.to(dev), v.to(dev), dlen.to(dev))
+    ref, ref_lse = ref_draft(q, k, v, dlen, 1.0 / math.sqrt(128))
+    assert_attention_close(out, ref[:, 0])
+    assert_lse_close(lse, ref_lse[:, 0])
+
+
+def test_empty_batch_is_a_noop():
+    dev = gpu_or_skip()
+    q = torch.empty((0, 4, 32, 128), dtype=torch.bfloat16, device=dev)
+    k = torch.empty((0, 8, 64, 128), dtype=torch.bfloat16, device=dev)
+    out, _ = ops.verify_attn(q, k, k, torch.empty(0, dtype=torch.int32, device=dev))
+    assert out.shape == (0, 4, 32, 128)
+
+
+def test_out_of_range_length_raises_device_flag_and_spares_others():
+    dev = gpu_or_skip()
+    q, k, v, kv_len = _case(2, 4, 32, 8, 128, [500, 500], 500, seed=9)
+    bad = torch.tensor([500, 9999], dtype=torch.int32)
+    ws = ops.workspace(mgd.mgd_verify_workspace_size(2, 4, 32, 8, 128, 500), dev)
+    out, _ = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), bad.to(dev), ws=ws)
+    flags = mgd.mgd_workspace_errors(ws)
+    assert flags & mgd.MGD_DEVERR_KV_LEN
+    ref, _ = ref_attention(q[:1], k[:1], v[:1], kv_len[:1], 1.0 / math.sqrt(128))
+    assert_attention_close(out[:1], ref)
+    # a clean call clears the word
+    ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev), ws=ws)
+    assert mgd.mgd_workspace_errors(ws) == 0
+
+
+def _sampled_pairs(kv_len, Hkv, n=3, seed=0):
+    L = kv_len.numpy()
+    rng = np.random.default_rng(seed)
+    bs = {int(np.argmax(L)), int(np.argmin(L))}
+    while len(bs) < n:
+        bs.add(int(rng.integers(len(L))))
+    return [(b, int(rng.integers(Hkv))) for b in sorted(bs)]
+
+
+@pytest.mark.parametrize("cid", [2, 3, 4])
+def test_verify_full_size_sampled(cid):
+    """Full-size workload in the benchmark's launch configuration; sampled (sequence, KV head) pairs."""
+    dev = gpu_or_skip()
+    c = wl.CONFIGS[cid]
+    kv_len = wl.lengths(c)
+    k, v = wl.kv_cache(c, dev, kv_len=kv_len)
+    q = wl.queries(c, dev)
+    out, lse = ops.verify_attn(q, k, v, kv_len.to(dev))
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all())
+    G, D = c["Hq"] // c["Hkv"], c["D"]
+    for b, h in _sampled_pairs(kv_len, c["Hkv"]):
+        L = int(kv_len[b])
+        ref, ref_lse = ref_attention(q[b:b + 1, :, h * G:(h + 1) * G], k[b:b + 1, h:h + 1, :L],
+                                     v[b:b + 1, h:h + 1, :L], kv_len[b:b + 1], 1.0 / math.sqrt(D))
+        assert_attention_close(out[b:b + 1, :, h * G:(h + 1) * G], ref, "out[b=%d,h=%d]" % (b, h))
+        assert_lse_close(lse[b:b + 1, :, h * G:(h + 1) * G], ref_lse)
+    del k, v
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("cid", [2, 3])
+def test_draft_full_size_sampled(cid):
+    dev = gpu_or_skip()
+    c = wl.CONFIGS[cid]
+    K = c["K"]
+    dlen = torch.full((c["B"],), K, dtype=torch.int32)
+    kd, vd = wl.kv_cache(c, dev, kv_len=dlen, cap=K, layer=7)
+    qd = wl.draft_queries(c, dev)
+    out, lse = ops.draft_attn(qd, kd, vd, dlen.to(dev))
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    G, D = c["Hq"] // c["Hkv"], c["D"]
+    for b, h in _sampled_pairs(dlen, c["Hkv"]):
+        ref, ref_lse = ref_draft(qd[b:b + 1, :, h * G:(h + 1) * G], kd[b:b + 1, h:h + 1], vd[b:b + 1, h:h + 1],
+                                 dlen[b:b + 1], 1.0 / math.sqrt(D))
+        assert_attention_close(out[b:b + 1, h * G:(h + 1) * G], ref[:, 0])
+        assert_lse_close(lse[b:b + 1, h * G:(h + 1) * G], ref_lse[:, 0])

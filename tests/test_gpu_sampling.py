@@ -1,0 +1,152 @@
+"""GPU parity of the draft draw and of modified rejection sampling against the
+float64 oracle, plus the distribution identities checked directly on GPU draws.
+
+Decisions are compared per sequence and must be identical, except for
+sequences where the oracle reports a tested acceptance with |u*q - p| < 1e-6
+or a draw whose target u*Z lies within 1e-6*Z of a bucket edge."""
+import numpy as np
+import pytest
+import torch
+
+from _parity import SAMPLE_BAND, gpu_or_skip
+from long_context_speculative_split_gb300 import mgd, ops
+from long_context_speculative_split_gb300 import workloads as wl
+from oracle.sampling import draft_draw as ref_draw
+from oracle.sampling import rejection_sample as ref_reject
+from oracle.sampling import softmax
+
+pytestmark = pytest.mark.gpu
+CHI2_15DOF_P1E3 = 37.697
+
+
+def _compare_round(t, d, u, dev, min_frac=0.9):
+    B, gp1, V = t.shape
+    gamma = gp1 - 1
+    tok = ops.draft_draw(d.to(dev), u.to(dev))
+    rtok, rmarg = ref_draw(d, u)
+    tok_c = tok.cpu().numpy()
+    ok_draw = rmarg >= SAMPLE_BAND
+    assert np.array_equal(tok_c[ok_draw], rtok[ok_draw])
+    # the verify step reads the GPU's draft tokens; the oracle is given the same tokens
+    out, nacc = ops.rejection_sample(t.to(dev), d.to(dev), tok, u.to(dev))
+    ref = ref_reject(t, d, tok_c, u)
+    safe = np.ones(B, dtype=bool)
+    with np.errstate(invalid="ignore"):
+        safe &= ~np.any(ref["accept_margin"] < SAMPLE_BAND, axis=1)
+        safe &= ~(ref["draw_margin"] < SAMPLE_BAND)
+    out_c, nacc_c = out.cpu().numpy(), nacc.cpu().numpy()
+    assert safe.mean() >= min_frac
+    assert np.array_equal(nacc_c[safe], ref["num_accepted"][safe])
+    assert np.array_equal(out_c[safe], ref["out_tokens"][safe])
+    # structure holds everywhere: accepted drafts copied, then one token, then -1
+    for b in range(B):
+        n = nacc_c[b]
+        assert np.array_equal(out_c[b, :n], tok_c[b, :n])
+        assert 0 <= out_c[b, n] < V
+        assert np.all(out_c[b, n + 1:] == -1)
+    return nacc_c
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3])
+def test_round_matches_oracle(cid):
+    dev = gpu_or_skip()
+    c = wl.CONFIGS[cid]
+    t, d = wl.logits(c, "cpu")
+    u = wl.uniforms(c, "cpu")
+    _compare_round(t, d, u, dev)
+
+
+def test_odd_vocab_and_many_sequences():
+    dev = gpu_or_skip()
+    c = dict(wl.CONFIGS[2], B=300, V=4099, gamma=5, sigma=2.0, sigma_n=1.0)
+    t, d = wl.logits(c, "cpu", seed=4)
+    u = wl.uniforms(c, "cpu", seed=4)
+    _compare_round(t, d, u, dev)
+
+
+def test_single_row_draft_draw():
+    dev = gpu_or_skip()
+    c = wl.CONFIGS[2]
+    _, d = wl.logits(c, "cpu", seed=1)
+    u = wl.uniforms(c, "cpu", seed=1)
+    tok = torch.full((c["B"], c["gamma"]), -7, dtype=torch.int32, device=dev)
+    ops.draft_draw(d.to(dev), u.to(dev), draft_tokens=tok, row=1)
+    rt, rm = ref_draw(d, u)
+    tc = tok.cpu().numpy()
+    assert np.all(tc[:, 0] == -7) and np.all(tc[:, 2] == -7)
+    ok = rm[:, 1] >= SAMPLE_BAND
+    assert np.array_equal(tc[ok, 1], rt[ok, 1])
+
+
+def _chi2(counts, probs):
+    e = counts.sum() * probs
+    return float(np.sum((counts - e) ** 2 / e))
+
+
+def test_chi_square_first_output_is_target():
+    dev = gpu_or_skip()
+    V, gamma, n = 16, 2, 1_000_000
+    g = torch.Generator().manual_seed(11)
+    tl = torch.randn((gamma + 1, V), generator=g) * 1.5
+    dl = tl[:gamma] + torch.randn((gamma, V), generator=g)
+    T = tl.expand(n, gamma + 1, V).contiguous().to(dev)
+    Dd = dl.expand(n, gamma, V).contiguous().to(dev)
+    u = torch.rand((n, gamma + 1, 3), generator=g).to(dev)
+    tok = ops.draft_draw(Dd, u)
+    out, _ = ops.rejection_sample(T, Dd, tok, u)
+    c_out = np.bincount(out[:, 0].cpu().numpy(), minlength=V).astype(np.float64)
+    c_dr = np.bincount(tok[:, 0].cpu().numpy(), minlength=V).astype(np.float64)
+    assert _chi2(c_out, softmax(tl[0].double().numpy())) < CHI2_15DOF_P1E3
+    assert _chi2(c_dr, softmax(dl[0].double().numpy())) < CHI2_15DOF_P1E3
+    assert _chi2(c_out, softmax(dl[0].double().numpy())) > 10 * CHI2_15DOF_P1E3
+
+
+def test_omega_closed_form_on_gpu():
+    dev = gpu_or_skip()
+    V, gamma, n, alpha = 16, 3, 1_000_000, 0.9
+    rng = np.random.default_rng(12)
+    ps, qs = [], []
+    for _ in range(gamma + 1):
+        c = rng.dirichlet(np.ones(V)) * alpha
+        a = np.zeros(V)
+        b = np.zeros(V)
+        a[:8] = rng.dirichlet(np.ones(8))
+        b[8:] = rng.dirichlet(np.ones(8))
+        ps.append(c + (1 - alpha) * a)
+        qs.append(c + (1 - alpha) * b)
+    tl = torch.tensor(np.log(np.stack(ps)), dtype=torch.float32)
+    dl = torch.tensor(np.log(np.stack(qs[:gamma])), dtype=torch.float32)
+    T = tl.expand(n, gamma + 1, V).contiguous().to(dev)
+    Dd = dl.expand(n, gamma, V).contiguous().to(dev)
+    u = torch.rand((n, gamma + 1, 3), generator=torch.Generator().manual_seed(13)).to(dev)
+    tok = ops.draft_draw(Dd, u)
+    _, nacc = ops.rejection_sample(T, Dd, tok, u)
+    x = nacc.double().cpu().numpy() + 1
+    omega = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+    assert abs(x.mean() - omega) < 4 * x.std() / np.sqrt(n)
+
+
+def test_equal_distributions_accept_everything():
+    dev = gpu_or_skip()
+    c = dict(wl.CONFIGS[2], B=64, V=5000)
+    t, _ = wl.logits(c, "cpu", seed=2)
+    d = t[:, :c["gamma"]].contiguous()
+    u = wl.uniforms(c, "cpu", seed=2)
+    nacc = _compare_round(t, d, u, dev)
+    assert np.all(nacc == c["gamma"])
+
+
+def test_invalid_draft_token_raises_device_flag():
+    dev = gpu_or_skip()
+    c = dict(wl.CONFIGS[1], B=4, V=100)
+    t, d = wl.logits(c, dev)
+    u = wl.uniforms(c, dev)
+    tok = torch.tensor([[0, 1, 2], [5, 100, 1], [-1, 0, 0], [3, 3, 3]], dtype=torch.int32, device=dev)
+    ws = ops.workspace(mgd.mgd_spec_workspace_size(4, 3, 100), dev)
+    out, nacc = ops.rejection_sample(t, d, tok, u, ws=ws)
+    assert mgd.mgd_workspace_errors(ws) & mgd.MGD_DEVERR_TOKEN
+    n = nacc.cpu().numpy()
+    assert n[1] <= 1 and n[2] == 0
+    o = out.cpu().numpy()
+    for b in range(4):
+        assert 0 <= o[b, n[b]] < 100

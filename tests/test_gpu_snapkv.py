@@ -1,0 +1,99 @@
+"""GPU parity of SnapKV draft-cache selection against the float64 oracle.
+
+Index sets must match except at positions whose oracle score lies within 1e-5
+(relative) of the K-th kept score; the gathered rows must equal the source
+rows bit for bit; draft_len must equal min(K, L)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from _parity import assert_index_sets_match, gpu_or_skip
+from long_context_speculative_split_gb300 import ops
+from long_context_speculative_split_gb300 import workloads as wl
+from oracle.snapkv import max_pool, select_indices, snapkv_select as ref_select, window_scores
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_pair(res, k, v, b, h, L, W, P, K, ref_scores_row, D):
+    pooled = np.zeros(ref_scores_row.shape)
+    n = L - W
+    pooled[:n] = max_pool(ref_scores_row, n, P)
+    ref_idx = select_indices(pooled, L, W, K)
+    n_top = len(ref_idx) - W
+    kth = np.min(pooled[ref_idx[:n_top]]) if 0 < n_top < n else np.nan
+    Keff = min(K, L)
+    got = res["sel_idx"][b, h].cpu().numpy()
+    assert int(res["draft_len"][b]) == Keff
+    assert np.all(got[Keff:] == -1)
+    ndiff = assert_index_sets_match(got[:Keff], ref_idx, pooled, kth)
+    idx = torch.from_numpy(got[:Keff].astype(np.int64)).to(k.device)
+    assert torch.equal(res["k_draft"][b, h, :Keff], k[b, h, idx])
+    assert torch.equal(res["v_draft"][b, h, :Keff], v[b, h, idx])
+    if res["scores"] is not None and n > 0:
+        gs = res["scores"][b, h, :n].double().cpu().numpy()
+        np.testing.assert_allclose(gs, pooled[:n], rtol=1e-4, atol=1e-9)
+    return ndiff
+
+
+def test_tiny_config_float32_full():
+    dev = gpu_or_skip()
+    c = wl.CONFIGS[1]
+    kv_len = wl.lengths(c)
+    k, v = wl.kv_cache(c, dev, kv_len=kv_len)
+    qw = wl.window_queries(c, dev)
+    res = ops.snapkv_select(qw, k, v, kv_len.to(dev), c["W"], c["pool"], c["K"], want_scores=True)
+    torch.cuda.synchronize()
+    ref = ref_select(qw, k, v, kv_len, c["W"], c["pool"], c["K"], 1.0 / math.sqrt(c["D"]))
+    for b in range(c["B"]):
+        _check_pair(res, k, v, b, 0, int(kv_len[b]), c["W"], c["pool"], c["K"], ref["scores"][b, 0], c["D"])
+
+
+CASES = [
+    # B, Hq, Hkv, D, lens, cap, W, P, K
+    (2, 32, 8, 128, [700, 300], 700, 32, 7, 128),
+    (2, 8, 2, 64, [100, 40], 128, 16, 5, 200),       # K >= L: every row kept
+    (1, 8, 2, 128, [32], 64, 32, 3, 64),             # L == W: only the window
+    (2, 64, 8, 128, [1000, 999], 1000, 32, 7, 256),  # 256 window rows -> two row groups
+    (3, 32, 8, 128, [5000, 4000, 2500], 5000, 32, 7, 512),
+    (1, 32, 8, 128, [777], 800, 8, 1, 100),          # no pooling, short window
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "L%s_W%d_P%d_K%d_G%d" % ("-".join(map(str, c[4])), c[6], c[7],
+                                                                                c[8], c[1] // c[2]))
+def test_bf16_cases_match_oracle(case):
+    dev = gpu_or_skip()
+    B, Hq, Hkv, D, lens, cap, W, P, K = case
+    cfg = dict(B=B, Hq=Hq, Hkv=Hkv, D=D, dtype="bf16", lens=lens, W=W, hh=0.01, gamma=1)
+    kv_len = torch.tensor(lens, dtype=torch.int32)
+    k, v = wl.kv_cache(cfg, dev, seed=3, kv_len=kv_len, cap=cap)
+    qw = wl.window_queries(cfg, dev, seed=3)
+    res = ops.snapkv_select(qw, k, v, kv_len.to(dev), W, P, K, want_scores=True)
+    torch.cuda.synchronize()
+    s = window_scores(qw, k, kv_len, W, 1.0 / math.sqrt(D))
+    for b in range(B):
+        for h in range(Hkv):
+            _check_pair(res, k, v, b, h, lens[b], W, P, K, s[b, h], D)
+
+
+@pytest.mark.parametrize("cid", [2, 3])
+def test_full_size_sampled(cid):
+    dev = gpu_or_skip()
+    c = wl.CONFIGS[cid]
+    kv_len = wl.lengths(c)
+    k, v = wl.kv_cache(c, dev, kv_len=kv_len)
+    qw = wl.window_queries(c, dev)
+    res = ops.snapkv_select(qw, k, v, kv_len.to(dev), c["W"], c["pool"], c["K"], want_scores=True)
+    torch.cuda.synchronize()
+    G = c["Hq"] // c["Hkv"]
+    rng = np.random.default_rng(cid)
+    for b, h in [(0, 0), (c["B"] - 1, c["Hkv"] - 1), (int(rng.integers(c["B"])), int(rng.integers(c["Hkv"])))]:
+        L = int(kv_len[b])
+        s = window_scores(qw[b:b + 1, :, h * G:(h + 1) * G], k[b:b + 1, h:h + 1, :L], kv_len[b:b + 1], c["W"],
+                          1.0 / math.sqrt(c["D"]))
+        _check_pair(res, k, v, b, h, L, c["W"], c["pool"], c["K"], s[0, 0], c["D"])
+    del k, v
+    torch.cuda.empty_cache()
