@@ -3,7 +3,11 @@ float64 oracle, plus the distribution identities checked directly on GPU draws.
 
 Decisions are compared per sequence and must be identical, except for
 sequences where the oracle reports a tested acceptance with |u*q - p| < 1e-6
-or a draw whose target u*Z lies within 1e-6*Z of a bucket edge."""
+or a draw whose target u*Z lies within 1e-6*Z of a bucket edge.  For those,
+the decisions before the first position inside the band must still agree.
+At vocab 128256 the drafted tokens have p, q of order 1e-4, so the absolute
+1e-6 band holds about 1-2 % of the tests per position: a quarter of the
+sequences may fall back to the prefix check."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +23,7 @@ pytestmark = pytest.mark.gpu
 CHI2_15DOF_P1E3 = 37.697
 
 
-def _compare_round(t, d, u, dev, min_frac=0.9):
+def _compare_round(t, d, u, dev, min_frac=0.75):
     B, gp1, V = t.shape
     gamma = gp1 - 1
     tok = ops.draft_draw(d.to(dev), u.to(dev))
@@ -30,14 +34,21 @@ def _compare_round(t, d, u, dev, min_frac=0.9):
     # the verify step reads the GPU's draft tokens; the oracle is given the same tokens
     out, nacc = ops.rejection_sample(t.to(dev), d.to(dev), tok, u.to(dev))
     ref = ref_reject(t, d, tok_c, u)
-    safe = np.ones(B, dtype=bool)
-    with np.errstate(invalid="ignore"):
-        safe &= ~np.any(ref["accept_margin"] < SAMPLE_BAND, axis=1)
-        safe &= ~(ref["draw_margin"] < SAMPLE_BAND)
     out_c, nacc_c = out.cpu().numpy(), nacc.cpu().numpy()
-    assert safe.mean() >= min_frac
-    assert np.array_equal(nacc_c[safe], ref["num_accepted"][safe])
-    assert np.array_equal(out_c[safe], ref["out_tokens"][safe])
+    with np.errstate(invalid="ignore"):
+        ambiguous = ref["accept_margin"] < SAMPLE_BAND          # [B, gamma], False where untested
+    first_amb = np.where(ambiguous.any(axis=1), ambiguous.argmax(axis=1), gamma + 1)
+    full = first_amb > gamma
+    # every sequence: identical decisions up to the first position inside the band
+    pre_ref = np.minimum(ref["num_accepted"], first_amb)
+    pre_gpu = np.minimum(nacc_c, first_amb)
+    assert np.array_equal(pre_gpu, pre_ref)
+    # sequences without an ambiguous test: identical acceptance count, identical
+    # correction / bonus token unless that draw itself lies inside the band
+    assert np.array_equal(nacc_c[full], ref["num_accepted"][full])
+    draw_ok = full & ~(ref["draw_margin"] < SAMPLE_BAND)
+    assert np.array_equal(out_c[draw_ok], ref["out_tokens"][draw_ok])
+    assert draw_ok.mean() >= min_frac
     # structure holds everywhere: accepted drafts copied, then one token, then -1
     for b in range(B):
         n = nacc_c[b]
