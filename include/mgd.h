@@ -191,6 +191,39 @@ mgd_status mgd_spec_sample(const float *target_logits, const float *draft_logits
                            int mode, int row, int32_t *out_tokens, int32_t *num_accepted,
                            void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------ *
+ * Allocation-free speculative sampling.  The papers have no counterpart to
+ * this call; it exists for callers that cannot allocate device memory, such
+ * as code running under a host framework that owns all device memory through
+ * its own pool, or a serving loop whose memory is planned once at start-up
+ * and must not call cudaMalloc (which can synchronise the device and fail
+ * late) on the per-token path.  Such callers cannot hand mgd_spec_sample a
+ * workspace, so this variant keeps its scratch in a fixed device array of
+ * MGD_NOALLOC_SCRATCH_BYTES owned by the library: every GPU that loads
+ * libmgd.so holds that array until the process exits.
+ *
+ * Arguments, results and arithmetic are those of mgd_spec_sample without
+ * `ws` / `ws_bytes`; inputs and outputs are still caller-provided device
+ * memory.  The call allocates nothing.
+ *   - Limit: the scratch it needs, mgd_spec_workspace_size(B, gamma, V), must
+ *     fit in MGD_NOALLOC_SCRATCH_BYTES (B * (2*gamma+1) * ceil(V/16384) * 8
+ *     + 256 bytes; e.g. B <= 1820 at gamma = 4, V = 128256); larger requests
+ *     return MGD_ERR_UNSUPPORTED with an explanation in mgd_last_error().
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents
+ *     (the error word at its start is cleared by each call).  Calls that
+ *     overlap on the GPU (different streams or host threads) race on it and
+ *     must be serialised by the caller.  The device error word of this
+ *     variant is not readable through mgd_workspace_errors.
+ * ------------------------------------------------------------------------ */
+#define MGD_NOALLOC_SCRATCH_BYTES (1u << 20)
+mgd_status mgd_spec_sample_noalloc(const float *target_logits, const float *draft_logits,
+                                   int32_t *draft_tokens, const float *u, int B, int gamma, int V,
+                                   int mode, int row, int32_t *out_tokens, int32_t *num_accepted,
+                                   void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -116,6 +116,10 @@ mgd_status run_attention(const void *q, const void *k, const void *v, const int3
 
 }  // namespace
 
+// Sets the calling thread's mgd_last_error() text (for entry points defined in
+// other translation units).
+void record_error(const char *msg) { g_last_error = msg; }
+
 int current_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||

@@ -38,7 +38,11 @@ SIGNATURES = {
                                  _f32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "mgd_spec_workspace_size": (_sz, [_i32] * 3),
     "mgd_spec_sample": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "mgd_spec_sample_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
 }
+
+# Bytes of the library-owned scratch array used by mgd_spec_sample_noalloc.
+MGD_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lib = None
 
@@ -154,3 +158,15 @@ def mgd_spec_sample(target_logits, draft_logits, draft_tokens, u, B, gamma, V, m
     _check(load().mgd_spec_sample(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(u), B, gamma,
                                   V, mode, row, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws), ws_bytes,
                                   _stream(stream)))
+
+
+def mgd_spec_sample_noalloc(target_logits, draft_logits, draft_tokens, u, B, gamma, V, mode, row, out_tokens,
+                            num_accepted, stream=None):
+    """mgd_spec_sample without a workspace, for callers that may not allocate device memory.
+
+    Its scratch is a fixed library-owned device array (MGD_NOALLOC_SCRATCH_BYTES) shared by
+    every call, so calls that overlap on the GPU must be serialised by the caller.
+    """
+    _check(load().mgd_spec_sample_noalloc(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(u),
+                                          B, gamma, V, mode, row, _ptr(out_tokens), _ptr(num_accepted),
+                                          _stream(stream)))
