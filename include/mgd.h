@@ -62,6 +62,7 @@ typedef enum {
 #define MGD_DEVERR_SNAP_LEN 0x2u   /* kv_len[b] < W or > kv_cap in mgd_snapkv_select */
 #define MGD_DEVERR_TOKEN    0x4u   /* a draft token id outside [0, V) */
 #define MGD_DEVERR_TIMEOUT  0x8u   /* a bounded wait inside a kernel gave up (never expected) */
+#define MGD_DEVERR_COMMIT   0x10u  /* mgd_commit_round: num_accepted, kv_len or draft_len out of range */
 
 const char *mgd_status_string(mgd_status s);
 /* Detail text of the last non-OK status returned on the calling thread ("" if none). */
@@ -190,6 +191,32 @@ mgd_status mgd_spec_sample(const float *target_logits, const float *draft_logits
                            int32_t *draft_tokens, const float *u, int B, int gamma, int V,
                            int mode, int row, int32_t *out_tokens, int32_t *num_accepted,
                            void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Commit / rollback after a verification round.  [SD-Serving] "Eine
+ * Verifizierungsrunde verstehen": candidates after the first rejection are
+ * discarded; [MagicDec] appendix A.1: the draft reads the compressed KV built
+ * at prefill, so tokens committed since then are appended to it.  The pages
+ * give no layout; this call follows the verify convention (kv_len includes the
+ * T = gamma + 1 verify rows: the last committed token, then the gamma drafts):
+ *   - with n = num_accepted[b], rows kv_len-T .. kv_len-T+n are kept and the
+ *     rest rolled back: kv_len[b] -= gamma - n;
+ *   - those n + 1 rows (K and V of every KV head) are copied to the draft cache
+ *     at draft_len[b] .. draft_len[b] + n, and draft_len[b] += n + 1.
+ *   num_accepted [B] int32 (device, e.g. from mgd_spec_sample);
+ *   kv_len, draft_len [B] int32, updated in place;
+ *   k, v [B, Hkv, kv_cap, D] and k_draft, v_draft [B, Hkv, draft_cap, D] in
+ *   `dtype`, strides in elements as for mgd_verify_attn (rows contiguous).
+ * A sequence with n outside [0, gamma], kv_len outside [T, kv_cap] or
+ * draft_len + n + 1 > draft_cap is left unchanged and flagged
+ * (MGD_DEVERR_COMMIT).  Byte copies and integer updates only.
+ * ------------------------------------------------------------------------ */
+size_t mgd_commit_workspace_size(int B);
+mgd_status mgd_commit_round(const int32_t *num_accepted, int B, int gamma, int Hkv, int D, mgd_dtype dtype,
+                            int32_t *kv_len, const void *k, const void *v, int kv_cap,
+                            int64_t kv_batch_stride, int64_t kv_head_stride, void *k_draft, void *v_draft,
+                            int draft_cap, int64_t draft_batch_stride, int64_t draft_head_stride,
+                            int32_t *draft_len, void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------ *
  * Allocation-free speculative sampling.  The papers have no counterpart to

@@ -146,6 +146,21 @@ int encode_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Hkv, int
   return static_cast<int>(r);
 }
 
+int encode_qwin_tensor_map(CUtensorMap *map, const void *base, int B, int W, int Hq, int D, int G) {
+  EncodeFn fn = encode_fn();
+  if (!fn || G > 256 || W > 256) return -1;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(W),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2,
+                                 static_cast<cuuint64_t>(W) * Hq * D * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(W), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return static_cast<int>(r);
+}
+
 }  // namespace mgd
 
 using namespace mgd;
@@ -258,12 +273,14 @@ mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, co
   a.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (in_dtype == MGD_BF16) {
-    CUtensorMap km;
+    CUtensorMap km, qm;
     if (encode_kv_tensor_map(&km, k, B, Hkv, kv_cap, D, kv_batch_stride, kv_head_stride) != 0)
       return fail(MGD_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    e = launch_snapkv(plan, a, 0, &km);
+    const bool tc05 = snap_tc05_eligible(plan) &&
+                      encode_qwin_tensor_map(&qm, q_win, B, W, Hq, D, Hq / Hkv) == 0;
+    e = launch_snapkv(plan, a, 0, &km, tc05 ? &qm : nullptr);
   } else {
-    e = launch_snapkv(plan, a, 1, nullptr);
+    e = launch_snapkv(plan, a, 1, nullptr, nullptr);
   }
   return e == cudaSuccess ? ok() : cuda_fail(e, "snapkv launch");
 }
@@ -301,6 +318,41 @@ mgd_status mgd_spec_sample(const float *target_logits, const float *draft_logits
   a.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_spec(plan, a);
   return e == cudaSuccess ? ok() : cuda_fail(e, "spec_sample launch");
+}
+
+size_t mgd_commit_workspace_size(int B) {
+  (void)B;
+  return kAlign;
+}
+
+mgd_status mgd_commit_round(const int32_t *num_accepted, int B, int gamma, int Hkv, int D, mgd_dtype dtype,
+                            int32_t *kv_len, const void *k, const void *v, int kv_cap, int64_t kv_batch_stride,
+                            int64_t kv_head_stride, void *k_draft, void *v_draft, int draft_cap,
+                            int64_t draft_batch_stride, int64_t draft_head_stride, int32_t *draft_len, void *ws,
+                            size_t ws_bytes, void *stream) {
+  if (B < 0) return fail(MGD_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
+  if (gamma < 1 || gamma > 16) return fail(MGD_ERR_UNSUPPORTED, "gamma must be in [1, 16] (got %d)", gamma);
+  if (Hkv < 1 || D < 1) return fail(MGD_ERR_INVALID_ARG, "need Hkv >= 1 and D >= 1");
+  if (dtype != MGD_BF16 && dtype != MGD_F32) return fail(MGD_ERR_INVALID_ARG, "bad dtype %d", dtype);
+  const int esz = (dtype == MGD_F32) ? 4 : 2;
+  if ((D * esz) % 16 != 0) return fail(MGD_ERR_UNSUPPORTED, "rows must be a multiple of 16 bytes");
+  if (kv_cap < 1 || draft_cap < 1) return fail(MGD_ERR_INVALID_ARG, "capacities must be >= 1");
+  if (kv_head_stride < static_cast<int64_t>(kv_cap) * D || kv_batch_stride < kv_head_stride * Hkv ||
+      draft_head_stride < static_cast<int64_t>(draft_cap) * D || draft_batch_stride < draft_head_stride * Hkv)
+    return fail(MGD_ERR_INVALID_ARG, "strides smaller than the capacities they hold");
+  if ((kv_head_stride * esz) % 16 || (kv_batch_stride * esz) % 16 || (draft_head_stride * esz) % 16 ||
+      (draft_batch_stride * esz) % 16)
+    return fail(MGD_ERR_INVALID_ARG, "strides must be multiples of 16 bytes");
+  if (B == 0) return ok();
+  if (!num_accepted || !kv_len || !k || !v || !k_draft || !v_draft || !draft_len || !ws)
+    return fail(MGD_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_draft) || !aligned16(v_draft) || !aligned16(ws))
+    return fail(MGD_ERR_INVALID_ARG, "k, v, k_draft, v_draft and ws must be 16-byte aligned");
+  if (ws_bytes < kAlign) return fail(MGD_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, kAlign);
+  cudaError_t e = launch_commit(num_accepted, B, gamma, Hkv, D, esz, kv_len, k, v, kv_cap, kv_batch_stride,
+                                kv_head_stride, k_draft, v_draft, draft_cap, draft_batch_stride, draft_head_stride,
+                                draft_len, ws, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "commit launch");
 }
 
 }  // extern "C"

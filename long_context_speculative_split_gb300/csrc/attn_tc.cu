@@ -59,8 +59,12 @@ struct Layout {
   static constexpr int kBoxes = D / 64;
   static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;  // K boxes then V boxes
   static constexpr int kOStride = 68;                          // epilogue row stride (64 cols + 4)
+  static constexpr int kQStride = D + 8;                       // query row stride in bf16 (16 B pad)
+  // One buffer serves two phases of a unit: the bf16 query rows while its tiles
+  // are processed, then the float32 merge of the 4 warps in its epilogue.
+  static constexpr int kEpiBytes = (32 * kOStride * 4 > 32 * kQStride * 2) ? 32 * kOStride * 4 : 32 * kQStride * 2;
   static constexpr int off_epi = kStages * kStageBytes;
-  static constexpr int off_m = off_epi + 32 * kOStride * 4;  // float [4][32]
+  static constexpr int off_m = off_epi + kEpiBytes;  // float [4][32]
   static constexpr int off_l = off_m + 4 * 32 * 4;           // float [4][32]
   static constexpr int off_rowM = off_l + 4 * 32 * 4;        // float [32]
   static constexpr int off_rowL = off_rowM + 32 * 4;         // float [32]
@@ -72,7 +76,7 @@ struct Layout {
 };
 
 template <int D, int NT, int MINB>
-__global__ void __maxnreg__(MINB == 2 ? 200 : 255)
+__global__ void __launch_bounds__(kThreads, MINB)
     attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                    const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ kv_len,
                    float *__restrict__ out_f32, __nv_bfloat16 *__restrict__ out_bf16, float *__restrict__ lse_out,
@@ -81,6 +85,7 @@ __global__ void __maxnreg__(MINB == 2 ? 200 : 255)
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float *sm_O = reinterpret_cast<float *>(smem + Lay::off_epi);
+  __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem + Lay::off_epi);
   float *sm_m = reinterpret_cast<float *>(smem + Lay::off_m);
   float *sm_l = reinterpret_cast<float *>(smem + Lay::off_l);
   float *sm_rowM = reinterpret_cast<float *>(smem + Lay::off_rowM);
@@ -134,6 +139,15 @@ __global__ void __maxnreg__(MINB == 2 ? 200 : 255)
       if (start >= L) continue;
       const int end = min(start + p.C, L);
       const int ntiles = (end - start + kTileKeys - 1) / kTileKeys;
+      {  // warm L2 with this unit's query rows; the consumers load them at its first tile
+        const int rg = pair % p.RG;
+        const int r_hi = min(p.rows, rg * 32 + 32);
+        for (int qg = rg * 32; qg < r_hi; ++qg) {
+          const __nv_bfloat16 *qr = q + ((static_cast<size_t>(b) * p.T + qg / p.G) * p.Hq + hkv * p.G + qg % p.G) * D;
+          for (int off = 0; off < D * 2; off += 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(qr) + off));
+        }
+      }
       for (int t = 0; t < ntiles; ++t) {
         if (!mbar_wait(&empty[stage], phase ^ 1u)) {
           raise_error(hdr, 0x8u);
@@ -172,7 +186,6 @@ __global__ void __maxnreg__(MINB == 2 ? 200 : 255)
   constexpr int MT = D / 16;  // m16 tiles over D (PV) == k16 steps over D (QK)
 
   float acc[MT][NT][4];
-  uint32_t qf[MT][NT][2];
   float m_run[NT][2], l_run[NT][2];
   int lim[NT][2];
 
@@ -195,7 +208,19 @@ __global__ void __maxnreg__(MINB == 2 ? 200 : 255)
     const int start = chunk * p.C;
 
     if (md.tile == 0) {
-      // ---- new unit: query fragments (B operand of S^T = K Q^T), state reset
+      // ---- new unit: stage its 32 query rows (zero padded) in shared memory for
+      //      the B operand of S^T = K Q^T, and reset the running state
+      for (int i = threadIdx.x; i < 32 * (D / 8); i += kConsumerWarps * 32) {
+        const int r = i / (D / 8), c = i % (D / 8);
+        const int qg = rg * 32 + r;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (qg < p.rows) {
+          const int t = qg / p.G, g = qg % p.G;
+          val = *reinterpret_cast<const uint4 *>(q + ((static_cast<size_t>(b) * p.T + t) * p.Hq + hkv * p.G + g) * D +
+                                                 8 * c);
+        }
+        *reinterpret_cast<uint4 *>(sQ + r * Lay::kQStride + 8 * c) = val;
+      }
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
 #pragma unroll
@@ -205,25 +230,12 @@ __global__ void __maxnreg__(MINB == 2 ? 200 : 255)
           m_run[j][e] = -INFINITY;
           l_run[j][e] = 0.f;
         }
-        const int qg = rg * 32 + 8 * j + gid;
-        const __nv_bfloat16 *qrow = nullptr;
-        if (qg < p.rows) {
-          const int t = qg / p.G, g = qg % p.G;
-          qrow = q + ((static_cast<size_t>(b) * p.T + t) * p.Hq + hkv * p.G + g) * D;
-        }
 #pragma unroll
-        for (int kk = 0; kk < MT; ++kk) {
-          if (qrow) {
-            qf[kk][j][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tig);
-            qf[kk][j][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 8 + 2 * tig);
-          } else {
-            qf[kk][j][0] = 0u;
-            qf[kk][j][1] = 0u;
-          }
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) acc[kk][j][c] = 0.f;
-        }
+          for (int c = 0; c < 4; ++c) acc[mt][j][c] = 0.f;
       }
+      named_bar(1, kConsumerWarps * 32);
     }
 
     unsigned char *st = smem + stage * Lay::kStageBytes;
@@ -237,13 +249,20 @@ __global__ void __maxnreg__(MINB == 2 ? 200 : 255)
         for (int c = 0; c < 4; ++c) s[j][c] = 0.f;
       const uint32_t kbase = smem_addr(st);
       const int kr = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+      // B fragments of two n8 row tiles per ldmatrix.x4: rows 16*jp + (lane&7) + 8*(lane>>4)
+      const uint32_t qaddr = smem_addr(sQ) + 2u * (((lane & 7) + 8 * (lane >> 4)) * Lay::kQStride + 8 * ((lane >> 3) & 1));
 #pragma unroll
       for (int kk = 0; kk < MT; ++kk) {
         const int d = 16 * kk + 8 * (lane >> 4);
         uint32_t a0, a1, a2, a3;
         ldsm_x4(kbase + (d >> 6) * kBoxBytes + swz128(kr, (d & 63) >> 3), a0, a1, a2, a3);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) mma_bf16_16816(s[j], a0, a1, a2, a3, qf[kk][j][0], qf[kk][j][1]);
+        for (int jp = 0; jp < (NT + 1) / 2; ++jp) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(qaddr + 2u * (16 * jp * Lay::kQStride + 16 * kk), b0, b1, b2, b3);
+          mma_bf16_16816(s[2 * jp], a0, a1, a2, a3, b0, b1);
+          if (2 * jp + 1 < NT) mma_bf16_16816(s[2 * jp + 1], a0, a1, a2, a3, b2, b3);
+        }
       }
       // ---- scale, mask, online softmax (exp2 domain)
       const bool need_mask = key0 + 15 > L - p.T;
@@ -421,12 +440,22 @@ __global__ void __maxnreg__(MINB == 2 ? 200 : 255)
     if (*sm_flag) {
       __threadfence();
       const size_t pb0 = static_cast<size_t>(pair) * p.nchunk * 32;
+      // all chunk lse values at once (independent loads), then per-row weights
+      float *sm_w = sm_O;  // [nch_b][32]; the epilogue buffer is free again
+      for (int i = threadIdx.x; i < nch_b * 32; i += kConsumerWarps * 32)
+        sm_w[i] = ((i & 31) < rows_valid) ? __ldcg(part_l + pb0 + i) : -INFINITY;
+      named_bar(1, kConsumerWarps * 32);
       if (threadIdx.x < rows_valid) {
         const int r = threadIdx.x;
         float M = -INFINITY;
-        for (int c = 0; c < nch_b; ++c) M = fmaxf(M, __ldcg(part_l + pb0 + c * 32 + r));
+        for (int c = 0; c < nch_b; ++c) M = fmaxf(M, sm_w[c * 32 + r]);
         float W = 0.f;
-        for (int c = 0; c < nch_b; ++c) W += expf(__ldcg(part_l + pb0 + c * 32 + r) - M);
+        for (int c = 0; c < nch_b; ++c) {
+          const float w = expf(sm_w[c * 32 + r] - M);
+          sm_w[c * 32 + r] = w;
+          W += w;
+        }
+        for (int c = 0; c < nch_b; ++c) sm_w[c * 32 + r] /= W;
         sm_rowM[r] = M;
         sm_rowL[r] = W;
       }
@@ -434,15 +463,22 @@ __global__ void __maxnreg__(MINB == 2 ? 200 : 255)
       for (int i = threadIdx.x; i < rows_valid * (D / 4); i += kConsumerWarps * 32) {
         const int r = i / (D / 4), dq = i % (D / 4);
         const float M = sm_rowM[r];
-        const float inv = 1.f / sm_rowL[r];
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < nch_b; ++c) {
-          const float w = expf(__ldcg(part_l + pb0 + c * 32 + r) - M) * inv;
-          const float4 x = __ldcg(reinterpret_cast<const float4 *>(part_o + (pb0 + c * 32 + r) * D + 4 * dq));
-          o.x += w * x.x;
-          o.y += w * x.y;
-          o.z += w * x.z;
-          o.w += w * x.w;
+        for (int c0 = 0; c0 < nch_b; c0 += 8) {  // 8 independent loads in flight per thread
+          float4 x[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            x[u] = (c0 + u < nch_b)
+                       ? __ldcg(reinterpret_cast<const float4 *>(part_o + (pb0 + (c0 + u) * 32 + r) * D + 4 * dq))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float w = (c0 + u < nch_b) ? sm_w[(c0 + u) * 32 + r] : 0.f;
+            o.x += w * x[u].x;
+            o.y += w * x[u].y;
+            o.z += w * x[u].z;
+            o.w += w * x[u].w;
+          }
         }
         const int qg = rg * 32 + r;
         const int t = qg / p.G, g = qg % p.G;
@@ -468,6 +504,8 @@ cudaError_t launch_one(const AttnPlan &pl, const AttnArgs &a, const CUtensorMap 
   auto kern = attn_tc_kernel<D, NT, MINB>;
   const int smem = Layout<D>::alloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   KParams kp;
   kp.T = pl.T;
@@ -534,11 +572,14 @@ AttnPlan plan_attention(int B, int T, int Hq, int Hkv, int D, int kv_cap, int sm
   p.NT = (p.rows_pg + 7) / 8;
   p.pairs = B * Hkv * p.RG;
   const int slots = attn_tc_min_blocks(p.NT) * sm_count;
-  // Largest chunk that still leaves >= 6 units per persistent CTA; at most 64
-  // chunks per pair (the merge keeps one weight per chunk).
-  int C = 4096;
+  // Largest power-of-two chunk (<= 16384 keys) that still leaves >= 3 units per
+  // persistent CTA: every unit pays a query load, an epilogue and (when the
+  // sequence is split) a partial write and merge, so fewer, longer units win
+  // until the last wave's imbalance dominates.  At most 64 chunks per pair
+  // (the merge keeps one weight per chunk in shared memory).
+  int C = 16384;
   const int cmin = std::max(256, ((kv_cap + 63) / 64 + 63) / 64 * 64);
-  while (C > cmin && static_cast<long long>(p.pairs) * ((kv_cap + C - 1) / C) < 6LL * slots) C /= 2;
+  while (C > cmin && static_cast<long long>(p.pairs) * ((kv_cap + C - 1) / C) < 3LL * slots) C /= 2;
   if (C < cmin) C = cmin;
   p.C = C;
   p.nchunk = (kv_cap + C - 1) / C;

@@ -96,7 +96,16 @@ struct SnapArgs {
   void *ws;
   cudaStream_t stream;
 };
-cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, const CUtensorMap *kmap);
+// kmap: K tensor map (bf16 path); qmap: window-query tensor map, non-null only
+// when the tcgen05 scoring kernel is eligible (snap_tc05_eligible).
+cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, const CUtensorMap *kmap,
+                          const CUtensorMap *qmap);
+bool snap_tc05_eligible(const SnapPlan &p);
+cudaError_t launch_snap_score_tc05(const SnapPlan &p, const SnapArgs &a, const CUtensorMap &kmap,
+                                   const CUtensorMap &qmap);
+// 4-D bf16 tensor map over window queries [B, W, Hq, D] with one box per
+// (64 columns, G heads, W rows): the 128-byte-swizzled W*G x 64 tile of a KV head.
+int encode_qwin_tensor_map(CUtensorMap *map, const void *base, int B, int W, int Hq, int D, int G);
 
 // ------------------------------------------------------------------ sampling
 struct SpecPlan {
@@ -120,5 +129,11 @@ struct SpecArgs {
   cudaStream_t stream;
 };
 cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a);
+
+// ------------------------------------------------------------------ commit / rollback
+cudaError_t launch_commit(const int32_t *num_accepted, int B, int gamma, int Hkv, int D, int esz, int32_t *kv_len,
+                          const void *k, const void *v, int kv_cap, int64_t kv_bstride, int64_t kv_hstride,
+                          void *k_draft, void *v_draft, int draft_cap, int64_t d_bstride, int64_t d_hstride,
+                          int32_t *draft_len, void *ws, cudaStream_t stream);
 
 }  // namespace mgd

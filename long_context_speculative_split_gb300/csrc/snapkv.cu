@@ -550,7 +550,8 @@ SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W) {
   return p;
 }
 
-cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, const CUtensorMap *kmap) {
+cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, const CUtensorMap *kmap,
+                          const CUtensorMap *qmap) {
   cudaError_t e = cudaMemsetAsync(a.ws, 0, kAlign, a.stream);
   if (e != cudaSuccess) return e;
   unsigned char *ws = static_cast<unsigned char *>(a.ws);
@@ -590,6 +591,9 @@ cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, cons
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+  } else if (qmap != nullptr && snap_tc05_eligible(p)) {
+    e = launch_snap_score_tc05(p, a, *kmap, *qmap);
+    if (e != cudaSuccess) return e;
   } else {
     if (p.RG > 1) {
       e = cudaMemsetAsync(ws + p.off_scores, 0, p.off_pooled - p.off_scores, a.stream);
@@ -601,6 +605,9 @@ cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, cons
   do {                                                                                                      \
     auto kern = snap_score_tc<DD, PP>;                                                                      \
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ScoreLayout<DD>::alloc);    \
+    if (e != cudaSuccess) return e;                                                                         \
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,                          \
+                             cudaSharedmemCarveoutMaxShared);                                               \
     if (e != cudaSuccess) return e;                                                                         \
     kern<<<units, kScoreThreads, ScoreLayout<DD>::alloc, a.stream>>>(*kmap, q, a.kv_len, ws, kp);           \
     e = cudaGetLastError();                                                                                 \

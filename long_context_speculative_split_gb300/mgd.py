@@ -18,6 +18,7 @@ MGD_OK, MGD_ERR_INVALID_ARG, MGD_ERR_UNSUPPORTED, MGD_ERR_WORKSPACE, MGD_ERR_CUD
 MGD_BF16, MGD_F32 = 0, 1
 MGD_VERIFY, MGD_DRAW_DRAFT = 0, 1
 MGD_DEVERR_KV_LEN, MGD_DEVERR_SNAP_LEN, MGD_DEVERR_TOKEN, MGD_DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+MGD_DEVERR_COMMIT = 0x10
 
 _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 
@@ -38,6 +39,9 @@ SIGNATURES = {
                                  _f32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "mgd_spec_workspace_size": (_sz, [_i32] * 3),
     "mgd_spec_sample": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "mgd_commit_workspace_size": (_sz, [_i32]),
+    "mgd_commit_round": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _i64, _i64, _vp, _vp, _i32,
+                                _i64, _i64, _vp, _vp, _sz, _vp]),
     "mgd_spec_sample_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
 }
 
@@ -158,6 +162,19 @@ def mgd_spec_sample(target_logits, draft_logits, draft_tokens, u, B, gamma, V, m
     _check(load().mgd_spec_sample(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(u), B, gamma,
                                   V, mode, row, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws), ws_bytes,
                                   _stream(stream)))
+
+
+def mgd_commit_workspace_size(B):
+    return load().mgd_commit_workspace_size(B)
+
+
+def mgd_commit_round(num_accepted, B, gamma, Hkv, D, dtype, kv_len, k, v, kv_cap, kv_batch_stride, kv_head_stride,
+                     k_draft, v_draft, draft_cap, draft_batch_stride, draft_head_stride, draft_len, ws, ws_bytes,
+                     stream=None):
+    _check(load().mgd_commit_round(_ptr(num_accepted), B, gamma, Hkv, D, dtype, _ptr(kv_len), _ptr(k), _ptr(v),
+                                   kv_cap, kv_batch_stride, kv_head_stride, _ptr(k_draft), _ptr(v_draft), draft_cap,
+                                   draft_batch_stride, draft_head_stride, _ptr(draft_len), _ptr(ws), ws_bytes,
+                                   _stream(stream)))
 
 
 def mgd_spec_sample_noalloc(target_logits, draft_logits, draft_tokens, u, B, gamma, V, mode, row, out_tokens,

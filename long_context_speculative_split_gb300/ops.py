@@ -122,3 +122,17 @@ def rejection_sample(target_logits, draft_logits, draft_tokens, u, ws=None, out_
     mgd.mgd_spec_sample(target_logits, draft_logits, draft_tokens, u, B, gamma, V, mgd.MGD_VERIFY, -1, out_tokens,
                         num_accepted, ws, ws.numel(), stream)
     return out_tokens, num_accepted
+
+
+def commit_round(num_accepted, gamma, kv_len, k, v, k_draft, v_draft, draft_len, ws=None, stream=None):
+    """Keep accepted verify rows, roll back the rest, append the kept rows to the draft cache (in place)."""
+    B, Hkv, cap, D = k.shape
+    if k_draft.stride(3) != 1 or k_draft.stride(2) != D or k_draft.stride() != v_draft.stride():
+        raise ValueError("draft K and V must share strides with contiguous rows of D elements")
+    sb, sh = _kv_strides(k, v, D)
+    if ws is None:
+        ws = workspace(mgd.mgd_commit_workspace_size(B), k.device)
+    mgd.mgd_commit_round(num_accepted, B, gamma, Hkv, D, _dtype_code(k), kv_len, k, v, cap, sb, sh, k_draft,
+                         v_draft, k_draft.shape[2], k_draft.stride(0), k_draft.stride(1), draft_len, ws, ws.numel(),
+                         stream)
+    return kv_len, draft_len

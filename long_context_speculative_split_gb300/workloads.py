@@ -18,6 +18,11 @@ Every tensor has its own sub-seed derived from (seed, tensor id, layer).
 """
 import torch
 
+# Draft-logit noise of the 32-layer round workload: the value at which the mean
+# acceptance sum_x min(p, q) of its seeded logits is 0.9, found by bisection with
+# the float64 oracle (tests/golden/calibrate_round_sigma.py -> round_sigma.json).
+ROUND_SIGMA_N = 0.25557936727955166
+
 CONFIGS = {
     1: dict(name="tiny_b2", B=2, Hq=4, Hkv=1, D=64, dtype="f32", lens=[512, 300], gamma=3, W=16, pool=5, K=64,
             V=1000, sigma=2.0, sigma_n=None, hh=0.0),
@@ -28,7 +33,7 @@ CONFIGS = {
     4: dict(name="ragged_b256_ctx4k_64k", B=256, Hq=32, Hkv=8, D=128, dtype="bf16", lens=(4096, 65536), gamma=2,
             W=32, pool=7, K=512, V=128256, sigma=3.0, sigma_n=0.5, hh=0.01),
     5: dict(name="round_b32_ctx16k_32layers", B=32, Hq=32, Hkv=8, D=128, dtype="bf16", lens=16384, gamma=3, W=32,
-            pool=7, K=512, V=128256, sigma=3.0, sigma_n=None, hh=0.01, layers=32),
+            pool=7, K=512, V=128256, sigma=3.0, sigma_n=ROUND_SIGMA_N, hh=0.01, layers=32),
 }
 
 _IDS = dict(k=1, v=2, q=3, qw=4, qd=5, hh=6, tl=7, dl=8, u=9, len=10)

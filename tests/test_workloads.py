@@ -49,3 +49,11 @@ def test_generators_are_deterministic_and_distinct():
     c2 = dict(wl.CONFIGS[2], B=2, V=50)
     t2, d2 = wl.logits(c2, "cpu")
     assert float((d2 - t2[:, :3]).std()) < 0.6 and float(t2.std()) > 2.5
+
+
+def test_round_sigma_matches_its_calibration():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "round_sigma.json")))
+    assert wl.CONFIGS[5]["sigma_n"] == g["sigma_n"]
+    assert abs(g["alpha_at_sigma_n"] - 0.9) < 1e-6
