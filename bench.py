@@ -494,11 +494,17 @@ def run_round(args):
 
 
 def load_traffic(cid):
-    """DRAM bytes per verify launch from the committed ncu summary, if it matches this kernel build."""
+    """DRAM bytes per verify launch from the committed ncu summary; None once the kernel source changed."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "verify_attention_traffic.json")
+    src = os.path.join(ROOT, "long_context_speculative_split_gb300", "csrc", "attn_tc.cu")
     try:
         with open(path) as f:
             d = json.load(f)
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        if d.get("kernel_source_sha256_16") != sha:
+            return None
         return d.get("config%d" % cid)
     except Exception:
         return None
