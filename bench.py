@@ -215,6 +215,42 @@ class Workload:
         if ev:
             ev[4].record()
 
+    def time_decode(self, reps=5):
+        """Plain decode attention (one query row) over the full cache: T_T of the speedup model."""
+        ops = self.ops
+        q1 = self.q[:, :1].contiguous()
+        out = torch.empty((self.B, 1, self.Hq, self.D), dtype=torch.float32, device=self.dev)
+        lse = torch.empty((self.B, 1, self.Hq), dtype=torch.float32, device=self.dev)
+        ws = ops.workspace(self.mgd.mgd_verify_workspace_size(self.B, 1, self.Hq, self.Hkv, self.D, self.cap),
+                           self.dev)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(2):
+            ops.verify_attn(q1, self.k, self.v, self.kv_len_d, ws=ws, out=out, lse=lse)
+        times = []
+        for _ in range(reps):
+            s.record()
+            ops.verify_attn(q1, self.k, self.v, self.kv_len_d, ws=ws, out=out, lse=lse)
+            e.record()
+            e.synchronize()
+            times.append(s.elapsed_time(e))
+        return statistics.median(times)
+
+    def time_streaming(self, reps=10):
+        """StreamingLLM-style draft-cache build (4 sinks + recent rows, same budget K)."""
+        ops = self.ops
+        out = dict(sel_idx=torch.empty_like(self.sel["sel_idx"]), k_draft=torch.empty_like(self.sel["k_draft"]),
+                   v_draft=torch.empty_like(self.sel["v_draft"]), draft_len=torch.empty_like(self.sel["draft_len"]))
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ops.streaming_select(self.k, self.v, self.kv_len_d, 4, self.K, out=out)
+        times = []
+        for _ in range(reps):
+            s.record()
+            ops.streaming_select(self.k, self.v, self.kv_len_d, 4, self.K, out=out)
+            e.record()
+            e.synchronize()
+            times.append(s.elapsed_time(e))
+        return statistics.median(times)
+
     def time_draft_only(self, reps=20):
         """Draft attention alone (one launch per rep), for its own roofline figure."""
         ops = self.ops
@@ -386,6 +422,8 @@ def run_ours(args):
     verify_gbs = w.bytes_verify / (verify_ms / 1e3) / 1e9
     draft_alone_ms = w.time_draft_only()
     draft_gbs = w.bytes_draft / (draft_alone_ms / 1e3) / 1e9
+    decode_ms = w.time_decode()
+    streaming_ms = w.time_streaming()
     e2e = None
     if not args.no_e2e:
         e_ms, h2d, d2h = run_e2e(w, max(1, min(args.steps, 5)), 1)
@@ -409,6 +447,9 @@ def run_ours(args):
             "snapkv_select": {"ms": snap_ms, "kv_gbs": w.bytes_snap / (snap_ms / 1e3) / 1e9},
             "rejection_sample": {"ms": spec_ms, "gbs": w.bytes_spec / (spec_ms / 1e3) / 1e9},
         },
+        "speedup_model": speedup_model(decode_ms, verify_ms, draft_alone_ms, snap_ms, w.gamma),
+        "next": {"streaming_select_ms": streaming_ms,
+                 "streaming_select_gbs": 2 * w.bytes_draft / (streaming_ms / 1e3) / 1e9},
         "gpu_launches": w.launches_per_step * args.steps,
         "device_error_flags": errs,
         "clocks": clk,
@@ -491,6 +532,23 @@ def run_round(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def speedup_model(t_decode, t_verify, t_draft, t_select, gamma):
+    """MagicDec notes, quick-read summary (Eq. 2 with Eq. 3's draft cost), restricted to attention:
+    Speedup = T_T * Omega(gamma, alpha) / (T_select(K) + gamma * T_D(K) + T_V(gamma)), with measured
+    attention times and Omega = (1 - alpha^(gamma+1)) / (1 - alpha).  Static selection runs once per
+    prefill, so it is shown both charged to every round and amortised away."""
+    out = {"T_T_decode_ms": t_decode, "T_V_verify_ms": t_verify, "T_D_draft_ms": t_draft,
+           "T_select_ms": t_select, "T_V_over_T_T": t_verify / t_decode, "T_D_over_T_T": t_draft / t_decode,
+           "scope": "attention only (no linear layers: no weights in scope)"}
+    for alpha in (0.8, 0.9):
+        om = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+        out["alpha_%.1f" % alpha] = {
+            "omega": om,
+            "speedup_selection_amortised": t_decode * om / (gamma * t_draft + t_verify),
+            "speedup_selection_every_round": t_decode * om / (t_select + gamma * t_draft + t_verify)}
+    return out
 
 
 def load_traffic(cid):

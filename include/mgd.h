@@ -193,6 +193,23 @@ mgd_status mgd_spec_sample(const float *target_logits, const float *draft_logits
                            void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * StreamingLLM-style draft cache.  [MagicDec] section 5.1 (the end-to-end runs
+ * draft over a StreamingLLM-style sparse KV) and 5.2 (SnapKV beats it).  The
+ * pages do not define it; this call keeps the first s = min(sink, K_eff)
+ * positions (attention sinks) and the last K_eff - s positions,
+ * K_eff = min(K, kv_len[b]), ascending, and gathers their rows.
+ *   k, v, kv_len as for mgd_verify_attn (1 <= kv_len[b] <= kv_cap);
+ *   sel_idx [B, Hkv, draft_cap] int32 (-1 after K_eff); k_draft, v_draft
+ *   [B, Hkv, draft_cap, D] contiguous; draft_len [B] = K_eff.
+ * Needs no workspace.  A sequence with kv_len outside [1, kv_cap] gets
+ * draft_len 0 and no kept rows.  Supported: 0 <= sink; 1 <= K <= draft_cap.
+ * ------------------------------------------------------------------------ */
+mgd_status mgd_streaming_select(const void *k, const void *v, const int32_t *kv_len, int B, int Hkv, int D,
+                                int kv_cap, int64_t kv_batch_stride, int64_t kv_head_stride, int sink, int K,
+                                mgd_dtype dtype, int32_t *sel_idx, void *k_draft, void *v_draft, int draft_cap,
+                                int32_t *draft_len, void *stream);
+
+/* ------------------------------------------------------------------------ *
  * Commit / rollback after a verification round.  [SD-Serving] "Eine
  * Verifizierungsrunde verstehen": candidates after the first rejection are
  * discarded; [MagicDec] appendix A.1: the draft reads the compressed KV built

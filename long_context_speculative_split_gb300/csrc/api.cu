@@ -276,7 +276,7 @@ mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, co
     CUtensorMap km, qm;
     if (encode_kv_tensor_map(&km, k, B, Hkv, kv_cap, D, kv_batch_stride, kv_head_stride) != 0)
       return fail(MGD_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    const bool tc05 = snap_tc05_eligible(plan) &&
+    const bool tc05 = snap_tc05_eligible(plan) && sm_scale > 0.f &&
                       encode_qwin_tensor_map(&qm, q_win, B, W, Hq, D, Hq / Hkv) == 0;
     e = launch_snapkv(plan, a, 0, &km, tc05 ? &qm : nullptr);
   } else {
@@ -318,6 +318,32 @@ mgd_status mgd_spec_sample(const float *target_logits, const float *draft_logits
   a.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_spec(plan, a);
   return e == cudaSuccess ? ok() : cuda_fail(e, "spec_sample launch");
+}
+
+mgd_status mgd_streaming_select(const void *k, const void *v, const int32_t *kv_len, int B, int Hkv, int D,
+                                int kv_cap, int64_t kv_batch_stride, int64_t kv_head_stride, int sink, int K,
+                                mgd_dtype dtype, int32_t *sel_idx, void *k_draft, void *v_draft, int draft_cap,
+                                int32_t *draft_len, void *stream) {
+  if (B < 0) return fail(MGD_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
+  if (Hkv < 1 || D < 1 || kv_cap < 1) return fail(MGD_ERR_INVALID_ARG, "need Hkv, D, kv_cap >= 1");
+  if (sink < 0 || K < 1 || draft_cap < K)
+    return fail(MGD_ERR_INVALID_ARG, "need sink >= 0 and 1 <= K <= draft_cap (got %d, %d, %d)", sink, K, draft_cap);
+  if (dtype != MGD_BF16 && dtype != MGD_F32) return fail(MGD_ERR_INVALID_ARG, "bad dtype %d", dtype);
+  const int esz = (dtype == MGD_F32) ? 4 : 2;
+  if ((D * esz) % 16 != 0) return fail(MGD_ERR_UNSUPPORTED, "rows must be a multiple of 16 bytes");
+  if (kv_head_stride < static_cast<int64_t>(kv_cap) * D || kv_batch_stride < kv_head_stride * Hkv)
+    return fail(MGD_ERR_INVALID_ARG, "strides smaller than the capacities they hold");
+  if ((kv_head_stride * esz) % 16 || (kv_batch_stride * esz) % 16)
+    return fail(MGD_ERR_INVALID_ARG, "strides must be multiples of 16 bytes");
+  if (B == 0) return ok();
+  if (!k || !v || !kv_len || !sel_idx || !k_draft || !v_draft || !draft_len)
+    return fail(MGD_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_draft) || !aligned16(v_draft))
+    return fail(MGD_ERR_INVALID_ARG, "k, v, k_draft and v_draft must be 16-byte aligned");
+  cudaError_t e = launch_streaming_select(k, v, kv_len, B, Hkv, D, esz, kv_cap, kv_batch_stride, kv_head_stride,
+                                          sink, K, sel_idx, k_draft, v_draft, draft_cap, draft_len,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "streaming select launch");
 }
 
 size_t mgd_commit_workspace_size(int B) {

@@ -136,4 +136,10 @@ cudaError_t launch_commit(const int32_t *num_accepted, int B, int gamma, int Hkv
                           void *k_draft, void *v_draft, int draft_cap, int64_t d_bstride, int64_t d_hstride,
                           int32_t *draft_len, void *ws, cudaStream_t stream);
 
+// ------------------------------------------------------------------ StreamingLLM-style cache
+cudaError_t launch_streaming_select(const void *k, const void *v, const int32_t *kv_len, int B, int Hkv, int D,
+                                    int esz, int kv_cap, int64_t bstride, int64_t hstride, int sink, int K,
+                                    int32_t *sel_idx, void *k_draft, void *v_draft, int draft_cap,
+                                    int32_t *draft_len, cudaStream_t stream);
+
 }  // namespace mgd

@@ -15,8 +15,8 @@
 // CTA = 10 warps: warp 0 issues TMA (the 128 window rows once, then 128-key K
 // tiles into a 2-stage ring), warp 1 owns the TMEM allocation and one thread
 // issues the MMAs (8 k-steps of K = 16 per tile) into a double-buffered
-// 2 x 128-column fp32 accumulator, warps 2..9 drain it (tcgen05.ld) -- each
-// TMEM lane quadrant is read by two warps that split the 128 columns.
+// 2 x 128-column fp32 accumulator, warps 2..9 drain it (tcgen05.ld) as two
+// groups of 4 warps taking alternate tiles, one warp per TMEM lane quadrant.
 // Operands are K-major bf16 with 128-byte swizzling, exactly the layout TMA
 // writes.  Used when W * G == 128 and D == 128 (the Llama-3.1-8B shape with a
 // 32-row window); other shapes use the mma.sync kernel in snapkv.cu.
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], kT5SoftWarps);
+      mbar_init(&acc_empty[a], kT5SoftWarps / 2);  // the 4 warps of the group draining buffer a
     }
     fence_mbar_init();
   }
@@ -235,76 +235,81 @@ __global__ void __launch_bounds__(kT5Threads, 2)
     }
   } else {
     // ------------------------------------------------------------------ softmax warps
-    const int qd = warp & 3;             // TMEM lane quadrant this warp may access
-    const int ch = (warp - 2) >> 2;      // which 64 of the 128 columns
-    const int tl = qd * 32 + lane;       // this thread's TMEM lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(qd * 32) << 16);
-    float m_run = -INFINITY, l_run = 0.f;
+    // Two groups of 4 warps take alternate tiles (group g drains accumulator
+    // buffer g); warp w of a group reads TMEM lane quadrant w % 4, all 128
+    // columns of its lane, in two halves of 64.
+    const int qd = warp & 3;
+    const int grp = (warp - 2) >> 2;
+    const int tl = qd * 32 + lane;  // this thread's TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(qd * 32) << 16) + grp * 128;
+    float m_run = -INFINITY, l_run = 0.f;                     // pass 1, exp2 domain
     const int pos = (PASS == 1) ? (L - p.W + tl / p.G) : 0;  // last key visible to window row tl
-    for (int t = 0; t < ntiles; ++t) {
-      const int a = t & 1;
-      if (!mbar_wait(&acc_full[a], (t >> 1) & 1u)) {
+    for (int t = grp; t < ntiles; t += 2) {
+      if (!mbar_wait(&acc_full[grp], (t >> 1) & 1u)) {
         raise_error(hdr, 0x8u);
         break;
       }
       tc_fence_after();
-      float v[2][32];
-      tmem_ld32(lane_addr + a * 128 + ch * 64, v[0]);
-      tmem_ld32(lane_addr + a * 128 + ch * 64 + 32, v[1]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[a]);
       const int kt0 = start + t * kT5Keys;
-      if (PASS == 1) {
-        // row tl, keys kt0 + ch*64 + c
-        const int k0 = kt0 + ch * 64;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            float x = v[i][c] * p.sl2;
-            if (k0 + 32 * i + c > pos) x = -INFINITY;
-            v[i][c] = x;
-            mx = fmaxf(mx, x);
-          }
-        const float mn = fmaxf(m_run, mx);
-        const float mu = (mn == -INFINITY) ? 0.f : mn;
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) acc += exp2f(v[i][c] - mu);
-        l_run = l_run * exp2f(m_run - mu) + acc;
-        m_run = mn;
-      } else {
-        // key kt0 + tl, window rows ch*64 + c
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const float4 lr = *reinterpret_cast<const float4 *>(&sm_lse[ch * 64 + 32 * i + c]);
-            acc += exp2f(v[i][c] * p.sl2 - lr.x) + exp2f(v[i][c + 1] * p.sl2 - lr.y) +
-                   exp2f(v[i][c + 2] * p.sl2 - lr.z) + exp2f(v[i][c + 3] * p.sl2 - lr.w);
-          }
-        if (ch == 1) sm_red[tl] = acc;
-        named_bar(1, kT5SoftWarps * 32);
-        if (ch == 0) {
-          const int key = kt0 + tl;
-          if (key < end) scores[(static_cast<size_t>(b) * p.Hkv + hkv) * p.kv_cap + key] = acc + sm_red[tl];
+      float acc2 = 0.f;  // pass 2: this key's probability sum
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float v[2][32];
+        tmem_ld32(lane_addr + h * 64, v[0]);
+        tmem_ld32(lane_addr + h * 64 + 32, v[1]);
+        if (h == 1) {  // both halves are in registers: hand the buffer back to the MMA thread
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[grp]);
         }
-        named_bar(1, kT5SoftWarps * 32);
+        if (PASS == 1) {
+          // row tl, keys kt0 + 64h + c; the window rows see every key before L - W
+          if (kt0 + kT5Keys - 1 > L - p.W) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (kt0 + 64 * h + 32 * i + c > pos) v[i][c] = -INFINITY;
+          }
+          float mx = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, v[i][c]);
+          const float mn = fmaxf(m_run, mx * p.sl2);  // sl2 > 0: the max commutes with the scale
+          const float mu = (mn == -INFINITY) ? 0.f : mn;
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) acc += exp2f(fmaf(v[i][c], p.sl2, -mu));
+          l_run = l_run * exp2f(m_run - mu) + acc;
+          m_run = mn;
+        } else {
+          // key kt0 + tl, window rows 64h + c
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              const float4 lr = *reinterpret_cast<const float4 *>(&sm_lse[64 * h + 32 * i + c]);
+              acc2 += exp2f(fmaf(v[i][c], p.sl2, -lr.x)) + exp2f(fmaf(v[i][c + 1], p.sl2, -lr.y)) +
+                      exp2f(fmaf(v[i][c + 2], p.sl2, -lr.z)) + exp2f(fmaf(v[i][c + 3], p.sl2, -lr.w));
+            }
+        }
+      }
+      if (PASS == 2) {
+        const int key = kt0 + tl;
+        if (key < end) scores[(static_cast<size_t>(b) * p.Hkv + hkv) * p.kv_cap + key] = acc2;
       }
     }
     if (PASS == 1) {
-      // combine the two column halves of each row, then write this chunk's (max, sum)
-      if (ch == 1) {
+      // combine the two groups' (max, sum) of each row, then write this chunk's partial
+      if (grp == 1) {
         sm_red[tl] = m_run;
         sm_red[128 + tl] = l_run;
       }
       named_bar(1, kT5SoftWarps * 32);
-      if (ch == 0) {
+      if (grp == 0) {
         const float m2 = sm_red[tl], l2 = sm_red[128 + tl];
         const float mn = fmaxf(m_run, m2);
         const float mu = (mn == -INFINITY) ? 0.f : mn;

@@ -121,13 +121,16 @@ struct DrawShared {
   int status;  // 0 ok, 1 total weight is zero
 };
 
-// Block-wide inverse-CDF draw (kFinThreads threads).  Returns the index, or -1
-// when the weights sum to zero.
+// Block-wide inverse-CDF draw (kFinThreads threads) over the index range
+// [r0, r1).  The target is u * (sum of the weights in the range) when
+// `target_in` < 0, else `target_in` (a running-sum value measured from r0).
+// Returns the index, or -1 when the weights of the range sum to zero.
 template <bool VEC4>
-__device__ int block_draw(const DrawSrc &src, int V, float u, DrawShared &sh) {
+__device__ int block_draw(const DrawSrc &src, int r0, int r1, float u, double target_in, DrawShared &sh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per = ((V + 32 * 128 - 1) / (32 * 128)) * 128;  // slice per warp, multiple of 128
-  const int lo = warp * per, hi = min(lo + per, V);
+  const int n = r1 - r0;
+  const int per = ((n + 32 * 128 - 1) / (32 * 128)) * 128;  // slice per warp, multiple of 128
+  const int lo = r0 + warp * per, hi = min(lo + per, r1);
   float sum = 0.f;
   int last = -1;
   for (int i = lo + 4 * lane; i < hi; i += 128) {
@@ -151,7 +154,7 @@ __device__ int block_draw(const DrawSrc &src, int V, float u, DrawShared &sh) {
     double Z = 0.0;
     for (int w = 0; w < 32; ++w) Z += static_cast<double>(sh.tot[w]);
     sh.status = (Z > 0.0) ? 0 : 1;
-    const double target = static_cast<double>(u) * Z;
+    const double target = (target_in < 0.0) ? static_cast<double>(u) * Z : target_in;
     double run = 0.0;
     int ws = -1;
     double base = 0.0;
@@ -232,6 +235,40 @@ __device__ int block_draw(const DrawSrc &src, int V, float u, DrawShared &sh) {
   return sh.idx;
 }
 
+// Draw from softmax(row) knowing the per-slice statistics of the row (slices of
+// `split` entries): the slice totals locate the slice holding u * Z, and only
+// that slice is scanned.
+template <bool VEC4>
+__device__ int draw_softmax_row(const float *row, const float2 *st, int nsplit, int split, int V, float M, float u,
+                                DrawShared &sh, double *s_pre, int *s_slice) {
+  if (threadIdx.x == 0) {
+    double Z = 0.0;
+    for (int s = 0; s < nsplit; ++s) Z += static_cast<double>(st[s].y) * exp2((st[s].x - M) * 1.4426950408889634);
+    const double target = static_cast<double>(u) * Z;
+    double run = 0.0;
+    int pick = nsplit - 1;
+    for (int s = 0; s < nsplit; ++s) {
+      const double ts = static_cast<double>(st[s].y) * exp2((st[s].x - M) * 1.4426950408889634);
+      if (ts > 0.0 && run + ts > target) {
+        pick = s;
+        break;
+      }
+      run += ts;
+    }
+    if (run > target) run = target;  // only when every later slice is empty
+    *s_pre = target - run;
+    *s_slice = pick;
+  }
+  __syncthreads();
+  const int s = *s_slice;
+  const double t = *s_pre;
+  DrawSrc src{row, nullptr, M, 1.f, 0.f, 0.f, 0};
+  const int r0 = s * split, r1 = min(V, r0 + split);
+  int tok = block_draw<VEC4>(src, r0, r1, u, t, sh);
+  if (tok < 0) tok = block_draw<VEC4>(src, 0, V, u, -1.0, sh);  // the slice held no mass: full scan
+  return tok;
+}
+
 __device__ __forceinline__ void merge_stats(const float2 *st, int nsplit, float &M, float &Z) {
   M = -INFINITY;
   for (int s = 0; s < nsplit; ++s) M = fmaxf(M, st[s].x);
@@ -248,7 +285,8 @@ __global__ void __launch_bounds__(kFinThreads) spec_finish_kernel(const float *_
                                                                    int32_t *__restrict__ num_accepted,
                                                                    const float2 *__restrict__ stats, WsHeader *hdr) {
   __shared__ float sM[33], sZ[33];
-  __shared__ int s_j;
+  __shared__ int s_j, s_slice;
+  __shared__ double s_pre;
   __shared__ DrawShared sh;
   const int b = blockIdx.x;
   const int g = sp.gamma, V = sp.V;
@@ -259,9 +297,10 @@ __global__ void __launch_bounds__(kFinThreads) spec_finish_kernel(const float *_
   if (mode == 1) {  // draft draw: row s uses draft row s, uniform slot 0
     for (int r = sp.r_begin; r < sp.r_begin + sp.nr; ++r) {
       const int s = r - g - 1;
-      DrawSrc src{row_ptr(target, draft, b, r, g, V), nullptr, sM[r], 1.f, 0.f, 0.f, 0};
       const float uu = u[(static_cast<size_t>(b) * (g + 1) + s) * 3 + 0];
-      const int tok = block_draw<VEC4>(src, V, uu, sh);
+      const int tok = draw_softmax_row<VEC4>(row_ptr(target, draft, b, r, g, V),
+                                             stats + (static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit, sp.nsplit,
+                                             sp.split, V, sM[r], uu, sh, &s_pre, &s_slice);
       if (threadIdx.x == 0) draft_tokens[static_cast<size_t>(b) * g + s] = tok;
       __syncthreads();
     }
@@ -298,14 +337,15 @@ __global__ void __launch_bounds__(kFinThreads) spec_finish_kernel(const float *_
   if (j < g) {
     DrawSrc src{row_ptr(target, draft, b, j, g, V), row_ptr(target, draft, b, g + 1 + j, g, V), sM[j],
                 1.f / sZ[j], sM[g + 1 + j], 1.f / sZ[g + 1 + j], 1};
-    tok = block_draw<VEC4>(src, V, uu, sh);
+    tok = block_draw<VEC4>(src, 0, V, uu, -1.0, sh);
     if (tok < 0) {  // the residual vanished through rounding: draw from p_j
       DrawSrc sp2{row_ptr(target, draft, b, j, g, V), nullptr, sM[j], 1.f, 0.f, 0.f, 0};
-      tok = block_draw<VEC4>(sp2, V, uu, sh);
+      tok = block_draw<VEC4>(sp2, 0, V, uu, -1.0, sh);
     }
-  } else {
-    DrawSrc src{row_ptr(target, draft, b, g, g, V), nullptr, sM[g], 1.f, 0.f, 0.f, 0};
-    tok = block_draw<VEC4>(src, V, uu, sh);
+  } else {  // bonus from p_gamma
+    tok = draw_softmax_row<VEC4>(row_ptr(target, draft, b, g, g, V),
+                                 stats + (static_cast<size_t>(b) * sp.nrows + g) * sp.nsplit, sp.nsplit, sp.split, V,
+                                 sM[g], uu, sh, &s_pre, &s_slice);
   }
   if (threadIdx.x == 0) {
     out_tokens[static_cast<size_t>(b) * (g + 1) + j] = tok;

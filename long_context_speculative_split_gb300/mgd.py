@@ -39,6 +39,8 @@ SIGNATURES = {
                                  _f32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "mgd_spec_workspace_size": (_sz, [_i32] * 3),
     "mgd_spec_sample": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "mgd_streaming_select": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _i32, _i32, _vp, _vp,
+                                    _vp, _i32, _vp, _vp]),
     "mgd_commit_workspace_size": (_sz, [_i32]),
     "mgd_commit_round": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _i64, _i64, _vp, _vp, _i32,
                                 _i64, _i64, _vp, _vp, _sz, _vp]),
@@ -162,6 +164,13 @@ def mgd_spec_sample(target_logits, draft_logits, draft_tokens, u, B, gamma, V, m
     _check(load().mgd_spec_sample(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(u), B, gamma,
                                   V, mode, row, _ptr(out_tokens), _ptr(num_accepted), _ptr(ws), ws_bytes,
                                   _stream(stream)))
+
+
+def mgd_streaming_select(k, v, kv_len, B, Hkv, D, kv_cap, kv_batch_stride, kv_head_stride, sink, K, dtype, sel_idx,
+                         k_draft, v_draft, draft_cap, draft_len, stream=None):
+    _check(load().mgd_streaming_select(_ptr(k), _ptr(v), _ptr(kv_len), B, Hkv, D, kv_cap, kv_batch_stride,
+                                       kv_head_stride, sink, K, dtype, _ptr(sel_idx), _ptr(k_draft), _ptr(v_draft),
+                                       draft_cap, _ptr(draft_len), _stream(stream)))
 
 
 def mgd_commit_workspace_size(B):

@@ -136,3 +136,19 @@ def commit_round(num_accepted, gamma, kv_len, k, v, k_draft, v_draft, draft_len,
                          v_draft, k_draft.shape[2], k_draft.stride(0), k_draft.stride(1), draft_len, ws, ws.numel(),
                          stream)
     return kv_len, draft_len
+
+
+def streaming_select(k, v, kv_len, sink, K, draft_cap=None, out=None, stream=None):
+    """StreamingLLM-style draft cache: first `sink` rows plus the most recent ones, min(K, L) in total."""
+    B, Hkv, cap, D = k.shape
+    sb, sh = _kv_strides(k, v, D)
+    cap_d = K if draft_cap is None else draft_cap
+    dev = k.device
+    if out is None:
+        out = dict(sel_idx=torch.empty((B, Hkv, cap_d), dtype=torch.int32, device=dev),
+                   k_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
+                   v_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
+                   draft_len=torch.empty((B,), dtype=torch.int32, device=dev))
+    mgd.mgd_streaming_select(k, v, kv_len, B, Hkv, D, cap, sb, sh, sink, K, _dtype_code(k), out["sel_idx"],
+                             out["k_draft"], out["v_draft"], cap_d, out["draft_len"], stream)
+    return out
