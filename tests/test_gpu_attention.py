@@ -127,7 +127,8 @@ def test_out_of_range_length_raises_device_flag_and_spares_others():
 def _sampled_pairs(kv_len, Hkv, n=3, seed=0):
     L = kv_len.numpy()
     rng = np.random.default_rng(seed)
-    bs = {int(np.argmax(L)), int(np.argmin(L))}
+    # longest, shortest, and the last sequence (the end of the persistent unit order)
+    bs = {int(np.argmax(L)), int(np.argmin(L)), len(L) - 1}
     while len(bs) < n:
         bs.add(int(rng.integers(len(L))))
     return [(b, int(rng.integers(Hkv))) for b in sorted(bs)]
@@ -172,3 +173,55 @@ def test_draft_full_size_sampled(cid):
                                  dlen[b:b + 1], 1.0 / math.sqrt(D))
         assert_attention_close(out[b:b + 1, h * G:(h + 1) * G], ref[:, 0])
         assert_lse_close(lse[b:b + 1, h * G:(h + 1) * G], ref_lse[:, 0])
+
+
+def _torch_attention(q, k, v, L, scale):
+    """Float32 torch math on the GPU for one sequence: q [T, Hq, D], k/v [Hkv, L, D] -> [T, Hq, D]."""
+    T, Hq, D = q.shape
+    Hkv = k.shape[0]
+    G = Hq // Hkv
+    kk = k[:, :L].float().repeat_interleave(G, dim=0)          # [Hq, L, D]
+    vv = v[:, :L].float().repeat_interleave(G, dim=0)
+    s = torch.einsum("thd,hld->htl", q.float(), kk) * scale     # [Hq, T, L]
+    pos = torch.arange(L, device=q.device)
+    lim = L - T + torch.arange(T, device=q.device)
+    s = s.masked_fill(pos[None, None, :] > lim[None, :, None], float("-inf"))
+    return torch.einsum("htl,hld->thd", torch.softmax(s, dim=-1), vv)
+
+
+def test_verify_ragged_every_sequence():
+    """Ragged batch 256 x U[4096, 65536] (the benchmark's launch configuration): every
+    sequence checked, so no unit of the persistent schedule can go missing unnoticed."""
+    dev = gpu_or_skip()
+    c = wl.CONFIGS[4]
+    kv_len = wl.lengths(c)
+    k, v = wl.kv_cache(c, dev, kv_len=kv_len)
+    q = wl.queries(c, dev)
+    out, _ = ops.verify_attn(q, k, v, kv_len.to(dev))
+    torch.cuda.synchronize()
+    scale = 1.0 / math.sqrt(c["D"])
+    worst_abs, num, den = 0.0, 0.0, 0.0
+    for b in range(c["B"]):
+        ref = _torch_attention(q[b], k[b], v[b], int(kv_len[b]), scale)
+        d = (out[b] - ref).double()
+        worst_abs = max(worst_abs, float(d.abs().max()))
+        num += float((d ** 2).sum())
+        den += float((ref.double() ** 2).sum())
+    assert worst_abs <= 2e-2 and (num / den) ** 0.5 <= 1e-3, (worst_abs, (num / den) ** 0.5)
+    del k, v
+    torch.cuda.empty_cache()
+
+
+def test_draft_split_units_match_oracle():
+    """512 (sequence, KV head) pairs with 2048-row draft caches: on a 152-SM part the planner
+    cuts every pair into two 1024-key units whose partials are merged (ragged second units of
+    176..1024 keys); every output is compared with the oracle."""
+    dev = gpu_or_skip()
+    B, Hq, Hkv, D, cap = 64, 32, 8, 128, 2048
+    g = torch.Generator().manual_seed(77)
+    lens = torch.randint(1200, cap + 1, (B,), generator=g).tolist()
+    q, k, v, dlen = _case(B, 1, Hq, Hkv, D, lens, cap, seed=78)
+    out, lse = ops.draft_attn(q.to(dev), k.to(dev), v.to(dev), dlen.to(dev))
+    ref, ref_lse = ref_draft(q, k, v, dlen, 1.0 / math.sqrt(D))
+    assert_attention_close(out, ref[:, 0])
+    assert_lse_close(lse, ref_lse[:, 0])
