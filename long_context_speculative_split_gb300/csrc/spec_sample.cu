@@ -10,21 +10,25 @@
 //
 // Two kernels per call:
 //   1. spec_stats: (max, sum of exp) of every logit row the mode needs, each
-//      row split over several CTAs (HBM stream, float4 loads);
-//   2. spec_finish: one CTA per sequence merges the row statistics, walks the
-//      acceptance chain (u1 * q(x) < p(x)), then draws the correction / bonus
-//      (or, in draft mode, the draft token) by inverse CDF: 32 warps each sum
-//      a contiguous slice of the weights, a double-precision prefix over the
-//      32 slice totals finds the slice holding u * Z, and that warp rescans
-//      its slice with warp scans to find the first index whose running sum
-//      exceeds u * Z.
+//      row split over several small CTAs (HBM stream, float4 loads, full
+//      occupancy);
+//   2. spec_finish: one CTA of 1024 threads per sequence merges the row
+//      statistics, tests all candidates at once (u1 * q(x) < p(x)) and keeps
+//      the prefix before the first rejection, then draws the correction /
+//      bonus (or, in draft mode, the draft token) by inverse CDF in two
+//      levels: 32 warps each sum a contiguous slice of the weights, a
+//      double-precision prefix over the 32 slice totals finds the slice
+//      holding u * Z, and the whole block scans that slice to find the first
+//      index whose running sum exceeds u * Z.  Softmax draws start from the
+//      statistics slice that holds u * Z, so only that slice is read.
 #include "common.cuh"
 
 namespace mgd {
 namespace {
 
 constexpr int kStatThreads = 256;
-constexpr int kFinThreads = 1024;
+constexpr int kThreads = 1024;  // finish kernel
+constexpr int kWarps = kThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct StatParams {
@@ -104,61 +108,101 @@ struct DrawSrc {
   int mode;
 };
 
-__device__ __forceinline__ float draw_weight(const DrawSrc &s, int i) {
-  const float pa = exp2f((__ldg(s.a + i) - s.Ma) * kLog2e);
+__device__ __forceinline__ float weight_of(const DrawSrc &s, float a, float c) {
+  const float pa = exp2f((a - s.Ma) * kLog2e);
   if (s.mode == 0) return pa;
-  const float pc = exp2f((__ldg(s.c + i) - s.Mc) * kLog2e);
+  const float pc = exp2f((c - s.Mc) * kLog2e);
   return fmaxf(0.f, pa * s.ia - pc * s.ic);
 }
 
+// Weights of entries i..i+3 (zero at or past `hi`).  With VEC4, i is a
+// multiple of 4 and the rows are 16-byte aligned.
+template <bool VEC4>
+__device__ __forceinline__ void weights4(const DrawSrc &s, int i, int hi, float (&w)[4]) {
+  float a[4], c[4] = {0.f, 0.f, 0.f, 0.f};
+  if (VEC4 && i + 3 < hi) {
+    const float4 fa = __ldg(reinterpret_cast<const float4 *>(s.a + i));
+    a[0] = fa.x;
+    a[1] = fa.y;
+    a[2] = fa.z;
+    a[3] = fa.w;
+    if (s.mode == 1) {
+      const float4 fc = __ldg(reinterpret_cast<const float4 *>(s.c + i));
+      c[0] = fc.x;
+      c[1] = fc.y;
+      c[2] = fc.z;
+      c[3] = fc.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[e] = weight_of(s, a[e], c[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (i + e < hi) {
+        a[e] = __ldg(s.a + i + e);
+        if (s.mode == 1) c[e] = __ldg(s.c + i + e);
+        w[e] = weight_of(s, a[e], c[e]);
+      } else {
+        w[e] = 0.f;
+      }
+    }
+  }
+}
+
 struct DrawShared {
-  float tot[32];
-  int last[32];
+  float tot[kWarps];
+  int last[kWarps];
+  float wsum[kWarps];
+  float trel[kWarps];
   double base;
   double target;
+  double chunk;
   int wstar;
+  int tidx;  // first thread of the block-wide scan holding the crossing
   int idx;
   int status;  // 0 ok, 1 total weight is zero
 };
 
-// Block-wide inverse-CDF draw (kFinThreads threads) over the index range
-// [r0, r1).  The target is u * (sum of the weights in the range) when
-// `target_in` < 0, else `target_in` (a running-sum value measured from r0).
-// Returns the index, or -1 when the weights of the range sum to zero.
+// Block-wide inverse-CDF draw over the index range [r0, r1).  The target is
+// u * (sum of the weights in the range) when `target_in` < 0, else
+// `target_in` (a running-sum value measured from r0).  Returns the index, or
+// -1 when the weights of the range sum to zero.
 template <bool VEC4>
 __device__ int block_draw(const DrawSrc &src, int r0, int r1, float u, double target_in, DrawShared &sh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = r1 - r0;
-  const int per = ((n + 32 * 128 - 1) / (32 * 128)) * 128;  // slice per warp, multiple of 128
-  const int lo = r0 + warp * per, hi = min(lo + per, r1);
-  float sum = 0.f;
-  int last = -1;
-  for (int i = lo + 4 * lane; i < hi; i += 128) {
+  const int per = ((n + kWarps * 128 - 1) / (kWarps * 128)) * 128;  // slice per warp, multiple of 128
+  {
+    const int lo = r0 + warp * per, hi = min(lo + per, r1);
+    float sum = 0.f;
+    int last = -1;
+#pragma unroll 4
+    for (int i = lo + 4 * lane; i < hi; i += 128) {
+      float w[4];
+      weights4<VEC4>(src, i, hi, w);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (i + e < hi) {
-        const float w = draw_weight(src, i + e);
-        sum += w;
-        if (w > 0.f) last = i + e;
+      for (int e = 0; e < 4; ++e) {
+        sum += w[e];
+        if (w[e] > 0.f) last = i + e;
       }
     }
-  }
-  sum = warp_sum_xor(sum, 1, 16);
-  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-  if (lane == 0) {
-    sh.tot[warp] = sum;
-    sh.last[warp] = last;
+    sum = warp_sum_xor(sum, 1, 16);
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    if (lane == 0) {
+      sh.tot[warp] = sum;
+      sh.last[warp] = last;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     double Z = 0.0;
-    for (int w = 0; w < 32; ++w) Z += static_cast<double>(sh.tot[w]);
+    for (int w = 0; w < kWarps; ++w) Z += static_cast<double>(sh.tot[w]);
     sh.status = (Z > 0.0) ? 0 : 1;
     const double target = (target_in < 0.0) ? static_cast<double>(u) * Z : target_in;
     double run = 0.0;
     int ws = -1;
     double base = 0.0;
-    for (int w = 0; w < 32; ++w) {
+    for (int w = 0; w < kWarps; ++w) {
       if (sh.tot[w] > 0.f && run + static_cast<double>(sh.tot[w]) > target) {
         ws = w;
         base = run;
@@ -166,71 +210,84 @@ __device__ int block_draw(const DrawSrc &src, int r0, int r1, float u, double ta
       }
       run += static_cast<double>(sh.tot[w]);
     }
-    if (ws < 0) {  // rounding pushed u*Z past the total: last slice with mass
-      for (int w = 31; w >= 0; --w)
+    if (ws < 0) {  // rounding pushed u*Z past the total: last slice with mass, its last entry
+      for (int w = kWarps - 1; w >= 0; --w)
         if (sh.tot[w] > 0.f) {
           ws = w;
           break;
         }
-      base = run;  // forces the fallback below
-      if (ws >= 0) base = target + 1.0;
+      base = target + 1.0;
     }
     sh.wstar = ws;
     sh.base = base;
     sh.target = target;
-    sh.idx = -1;
+    sh.idx = 0x7fffffff;
   }
   __syncthreads();
   if (sh.status != 0) return -1;
-  if (warp == sh.wstar) {
-    double run = sh.base;
-    const double target = sh.target;
-    int found = -1;
-    if (run <= target) {
-      for (int i0 = lo; i0 < hi && found < 0; i0 += 128) {
-        float w4[4];
-        float ls = 0.f;
+  // Second level: the whole block scans slice wstar, 4 * kThreads entries at a
+  // time.  Double precision is rare on this GPU, so one warp turns the running
+  // sum into a float target relative to each warp's start (clamped at 0);
+  // within a warp, thread t covers [excl_t, incl_t) and neighbours share their
+  // endpoints exactly, so a target inside the chunk is claimed by at least one
+  // thread, and the first claiming thread holds the crossing.
+  const int ws = sh.wstar;
+  const int lo = r0 + ws * per, hi = min(lo + per, r1);
+  if (sh.base <= sh.target) {
+    for (int c0 = lo; c0 < hi; c0 += 4 * kThreads) {
+      const int i = c0 + 4 * threadIdx.x;
+      float w[4];
+      weights4<VEC4>(src, i, hi, w);
+      const float ls = (w[0] + w[1]) + (w[2] + w[3]);
+      float incl = ls;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) excl = 0.f;
+      if (lane == 31) sh.wsum[warp] = incl;
+      __syncthreads();
+      if (warp == 0) {
+        const double x = static_cast<double>(sh.wsum[lane]);
+        double ix = x;  // inclusive prefix of the warp totals
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xffffffffu, ix, o);
+          if (lane >= o) ix += y;
+        }
+        double ex = __shfl_up_sync(0xffffffffu, ix, 1);
+        if (lane == 0) ex = 0.0;
+        sh.trel[lane] = fmaxf(0.f, static_cast<float>(sh.target - (sh.base + ex)));
+        if (lane == 31) sh.chunk = ix;
+        if (lane == 0) sh.tidx = 0x7fffffff;
+      }
+      __syncthreads();
+      const float trel = sh.trel[warp];
+      if (ls > 0.f && excl <= trel && incl > trel) atomicMin(&sh.tidx, static_cast<int>(threadIdx.x));
+      __syncthreads();
+      const int tsel = sh.tidx;
+      if (static_cast<int>(threadIdx.x) == tsel) {
+        float cacc = excl;
+        int pick = -1;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int i = i0 + 4 * lane + e;
-          w4[e] = (i < hi) ? draw_weight(src, i) : 0.f;
-          ls += w4[e];
+          cacc += w[e];
+          if (pick < 0 && w[e] > 0.f && cacc > trel) pick = i + e;
         }
-        float incl = ls;
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const bool cross = (run + static_cast<double>(incl)) > target;
-        const unsigned bal = __ballot_sync(0xffffffffu, cross);
-        if (bal) {
-          const int fl = __ffs(bal) - 1;
-          if (lane == fl) {
-            double c = run + static_cast<double>(incl - ls);
-            int pick = -1;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              c += static_cast<double>(w4[e]);
-              if (pick < 0 && w4[e] > 0.f && c > target) pick = i0 + 4 * lane + e;
+        if (pick < 0)  // the crossing is here but rounding moved it: last positive weight
+          for (int e = 3; e >= 0; --e)
+            if (w[e] > 0.f) {
+              pick = i + e;
+              break;
             }
-            if (pick < 0) {  // crossing straddled by rounding: last positive weight of this lane
-              for (int e = 3; e >= 0; --e)
-                if (w4[e] > 0.f) {
-                  pick = i0 + 4 * lane + e;
-                  break;
-                }
-            }
-            sh.idx = pick;
-          }
-          found = 1;
-        } else {
-          run += static_cast<double>(__shfl_sync(0xffffffffu, incl, 31));
-        }
+        sh.idx = pick;
       }
+      if (threadIdx.x == 0 && tsel == 0x7fffffff) sh.base += sh.chunk;  // next chunk
+      __syncthreads();
+      if (tsel != 0x7fffffff) break;
     }
-    __syncwarp();
-    if (lane == 0 && sh.idx < 0) sh.idx = sh.last[warp];
   }
+  if (threadIdx.x == 0 && sh.idx == 0x7fffffff) sh.idx = sh.last[ws];
   __syncthreads();
   return sh.idx;
 }
@@ -243,12 +300,12 @@ __device__ int draw_softmax_row(const float *row, const float2 *st, int nsplit, 
                                 DrawShared &sh, double *s_pre, int *s_slice) {
   if (threadIdx.x == 0) {
     double Z = 0.0;
-    for (int s = 0; s < nsplit; ++s) Z += static_cast<double>(st[s].y) * exp2((st[s].x - M) * 1.4426950408889634);
+    for (int s = 0; s < nsplit; ++s) Z += static_cast<double>(st[s].y * exp2f((st[s].x - M) * kLog2e));
     const double target = static_cast<double>(u) * Z;
     double run = 0.0;
     int pick = nsplit - 1;
     for (int s = 0; s < nsplit; ++s) {
-      const double ts = static_cast<double>(st[s].y) * exp2((st[s].x - M) * 1.4426950408889634);
+      const double ts = static_cast<double>(st[s].y * exp2f((st[s].x - M) * kLog2e));
       if (ts > 0.0 && run + ts > target) {
         pick = s;
         break;
@@ -277,20 +334,23 @@ __device__ __forceinline__ void merge_stats(const float2 *st, int nsplit, float 
 }
 
 template <bool VEC4>
-__global__ void __launch_bounds__(kFinThreads) spec_finish_kernel(const float *__restrict__ target,
-                                                                   const float *__restrict__ draft,
-                                                                   int32_t *__restrict__ draft_tokens,
-                                                                   const float *__restrict__ u, StatParams sp,
-                                                                   int mode, int32_t *__restrict__ out_tokens,
-                                                                   int32_t *__restrict__ num_accepted,
-                                                                   const float2 *__restrict__ stats, WsHeader *hdr) {
+__global__ void __launch_bounds__(kThreads, 1) spec_finish_kernel(const float *__restrict__ target,
+                                                               const float *__restrict__ draft,
+                                                               int32_t *__restrict__ draft_tokens,
+                                                               const float *__restrict__ u, StatParams sp, int mode,
+                                                               int32_t *__restrict__ out_tokens,
+                                                               int32_t *__restrict__ num_accepted,
+                                                               const float2 *__restrict__ stats, WsHeader *hdr) {
   __shared__ float sM[33], sZ[33];
-  __shared__ int s_j, s_slice;
+  __shared__ int s_last, s_slice;
+  __shared__ int s_tok[16];
+  __shared__ unsigned char s_ok[16], s_bad[16];
   __shared__ double s_pre;
   __shared__ DrawShared sh;
   const int b = blockIdx.x;
   const int g = sp.gamma, V = sp.V;
-  for (int r = sp.r_begin + threadIdx.x; r < sp.r_begin + sp.nr; r += kFinThreads)
+
+  for (int r = sp.r_begin + threadIdx.x; r < sp.r_begin + sp.nr; r += kThreads)
     merge_stats(stats + (static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit, sp.nsplit, sM[r], sZ[r]);
   __syncthreads();
 
@@ -307,31 +367,44 @@ __global__ void __launch_bounds__(kFinThreads) spec_finish_kernel(const float *_
     return;
   }
 
-  if (threadIdx.x == 0) {
-    int j = g;
-    for (int i = 0; i < g; ++i) {
-      const int x = draft_tokens[static_cast<size_t>(b) * g + i];
-      if (x < 0 || x >= V) {
-        raise_error(hdr, 0x4u);
-        j = i;
-        break;
-      }
+  // every candidate's test at once; the chain keeps the prefix before the first rejection
+  if (threadIdx.x < g) {
+    const int i = threadIdx.x;
+    const int x = draft_tokens[static_cast<size_t>(b) * g + i];
+    const bool bad = (x < 0 || x >= V);
+    bool acc = false;
+    if (!bad) {
       const float *t = row_ptr(target, draft, b, i, g, V);
       const float *d = row_ptr(target, draft, b, g + 1 + i, g, V);
       const float px = exp2f((t[x] - sM[i]) * kLog2e) / sZ[i];
       const float qx = exp2f((d[x] - sM[g + 1 + i]) * kLog2e) / sZ[g + 1 + i];
       const float u1 = u[(static_cast<size_t>(b) * (g + 1) + i) * 3 + 1];
-      if (!(u1 * qx < px)) {
+      acc = (u1 * qx < px);
+    }
+    s_tok[i] = x;
+    s_ok[i] = acc ? 1 : 0;
+    s_bad[i] = bad ? 1 : 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int j = g;
+    for (int i = 0; i < g; ++i) {
+      if (s_bad[i]) {
+        raise_error(hdr, 0x4u);
         j = i;
         break;
       }
-      out_tokens[static_cast<size_t>(b) * (g + 1) + i] = x;
+      if (!s_ok[i]) {
+        j = i;
+        break;
+      }
+      out_tokens[static_cast<size_t>(b) * (g + 1) + i] = s_tok[i];
     }
-    s_j = j;
+    s_last = j;
     num_accepted[b] = j;
   }
   __syncthreads();
-  const int j = s_j;
+  const int j = s_last;
   const float uu = u[(static_cast<size_t>(b) * (g + 1) + j) * 3 + 2];
   int tok;
   if (j < g) {
@@ -400,11 +473,11 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (vec4)
-    spec_finish_kernel<true><<<p.B, kFinThreads, 0, a.stream>>>(a.target, a.draft, a.draft_tokens, a.u, sp, a.mode,
-                                                               a.out_tokens, a.num_accepted, stats, hdr);
+    spec_finish_kernel<true><<<p.B, kThreads, 0, a.stream>>>(a.target, a.draft, a.draft_tokens, a.u, sp, a.mode,
+                                                             a.out_tokens, a.num_accepted, stats, hdr);
   else
-    spec_finish_kernel<false><<<p.B, kFinThreads, 0, a.stream>>>(a.target, a.draft, a.draft_tokens, a.u, sp, a.mode,
-                                                                a.out_tokens, a.num_accepted, stats, hdr);
+    spec_finish_kernel<false><<<p.B, kThreads, 0, a.stream>>>(a.target, a.draft, a.draft_tokens, a.u, sp, a.mode,
+                                                              a.out_tokens, a.num_accepted, stats, hdr);
   return cudaGetLastError();
 }
 
