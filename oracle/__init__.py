@@ -16,7 +16,8 @@ Sources (the pages this restates):
     quick-read summary (self-speculation over a compressed KV of budget K,
     Eq. 2/3 restated inline), section 3.1 (expected tokens per round
     Omega(gamma, alpha)), section 3.2 (verify and decode load the same KV),
-    section 4.4 (static selection such as SnapKV), appendix A.1 (the static
+    section 4.4 (static selection such as SnapKV; top-K attention's selection
+    cost), section 5.1 (StreamingLLM-style drafting), appendix A.1 (the static
     compressed KV is built at prefill and reused for drafting).
   * "Wann beschleunigt spekulatives Decoding das LLM-Serving?", section
     "Eine Verifizierungsrunde verstehen" (left-to-right acceptance, residual
@@ -29,6 +30,9 @@ Modules:
   snapkv     -- observation-window scores, max-pool, top-K + window, gather.
   sampling   -- softmax, inverse-CDF draw, draft draw, modified rejection
                 sampling.
+  commit     -- commit / rollback of the caches after a verification round.
+  streaming  -- StreamingLLM-style draft cache (attention sinks + recent rows).
+  topk       -- dynamic top-K attention drafting (one draft step).
 
 Pins: every function here is checked by ``tests/test_oracle_*.py`` against
 closed forms, hand-derived fixtures in ``tests/golden/``, high-precision brute
