@@ -255,6 +255,19 @@ class Workload:
         return self._per_launch_ms(lambda: ops.streaming_select(self.k, self.v, self.kv_len_d, 4, self.K, out=out),
                                    reps, flush_l2=True)
 
+    def time_topk_draft(self, reps=3):
+        """One dynamic top-K draft step (NEXT-4): select the K rows the draft query attends to most over
+        the full cache, then attend over them; compared with the static draft step and plain decode."""
+        ops = self.ops
+        q = self.qd[0]
+        out = dict(out=torch.empty_like(self.dout), lse=torch.empty_like(self.dlse),
+                   sel_idx=torch.empty_like(self.sel["sel_idx"]), k_draft=torch.empty_like(self.sel["k_draft"]),
+                   v_draft=torch.empty_like(self.sel["v_draft"]), draft_len=torch.empty_like(self.sel["draft_len"]))
+        ws = ops.workspace(self.mgd.mgd_topk_draft_workspace_size(self.B, self.Hq, self.Hkv, self.D, self.cap,
+                                                                  self.K), self.dev)
+        return self._per_launch_ms(lambda: ops.topk_draft_attn(q, self.k, self.v, self.kv_len_d, self.K, ws=ws,
+                                                                out=out), reps)
+
     def time_draft_only(self, reps=20):
         """Draft attention alone, for its own roofline figure.  Back-to-back launches cycle
         through copies of the draft cache totalling at least 256 MB (twice L2), so every
@@ -427,6 +440,7 @@ def run_ours(args):
     draft_gbs = w.bytes_draft / (draft_alone_ms / 1e3) / 1e9
     decode_ms = w.time_decode()
     streaming_ms = w.time_streaming()
+    topk_ms = w.time_topk_draft()
     e2e = None
     if not args.no_e2e:
         e_ms, h2d, d2h = run_e2e(w, max(1, min(args.steps, 5)), 1)
@@ -452,7 +466,10 @@ def run_ours(args):
         },
         "speedup_model": speedup_model(decode_ms, verify_ms, draft_alone_ms, snap_ms, w.gamma),
         "next": {"streaming_select_ms": streaming_ms,
-                 "streaming_select_gbs": 2 * w.bytes_draft / (streaming_ms / 1e3) / 1e9},
+                 "streaming_select_gbs": 2 * w.bytes_draft / (streaming_ms / 1e3) / 1e9,
+                 "topk_draft_step_ms": topk_ms,
+                 "topk_draft_over_static_draft": topk_ms / draft_alone_ms,
+                 "topk_draft_over_decode": topk_ms / decode_ms},
         "gpu_launches": w.launches_per_step * args.steps,
         "device_error_flags": errs,
         "clocks": clk,

@@ -210,6 +210,38 @@ mgd_status mgd_streaming_select(const void *k, const void *v, const int32_t *kv_
                                 int32_t *draft_len, void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * Dynamic top-K attention drafting (one draft step).  [MagicDec] section 4.4,
+ * first bullet (top-K attention reaches very high acceptance with a much
+ * smaller budget but is impractical because of its selection cost) and second
+ * bullet (dynamic selection searches the KV cache again for every query).
+ * The pages give no algorithm; this call is the SnapKV selection above with
+ * the draft query itself as a one-row window (W = 1, no pooling), followed by
+ * draft attention over the selected rows:
+ *   1. the draft query q[b, h] sits at position kv_len[b]-1 (its own K/V row
+ *      is the last cache row); its softmax probabilities over keys
+ *      0 .. kv_len[b]-1 are summed over the G = Hq/Hkv heads of a KV head;
+ *   2. keep K_eff = min(K, kv_len[b]) rows: the newest row plus the top
+ *      K_eff-1 earlier positions (ties -> lower position), ascending, and
+ *      gather them into k_draft / v_draft;
+ *   3. out[b, h] = softmax attention of q[b, h] over the kept rows.
+ *   q        [B, Hq, D] in_dtype;  k, v, kv_len as for mgd_verify_attn
+ *            (1 <= kv_len[b] <= kv_cap)
+ *   sel_idx, k_draft, v_draft, draft_len as for mgd_snapkv_select (outputs;
+ *            draft_cap >= K; the draft rows are contiguous)
+ *   out      [B, Hq, D] out_dtype;  lse [B, Hq] float32 or NULL (natural log)
+ *   ws       mgd_topk_draft_workspace_size(...) bytes
+ * Every call reads the whole K cache twice (the probabilities need each
+ * query's normaliser over all keys first): that is the selection cost.
+ * Supported: D in {64, 128}; in_dtype bf16 or float32; 1 <= K <= draft_cap.
+ * ------------------------------------------------------------------------ */
+size_t mgd_topk_draft_workspace_size(int B, int Hq, int Hkv, int D, int kv_cap, int draft_cap);
+mgd_status mgd_topk_draft_attn(const void *q, const void *k, const void *v, const int32_t *kv_len, int B, int Hq,
+                               int Hkv, int D, int kv_cap, int64_t kv_batch_stride, int64_t kv_head_stride, int K,
+                               float sm_scale, mgd_dtype in_dtype, int32_t *sel_idx, void *k_draft,
+                               void *v_draft, int draft_cap, int32_t *draft_len, void *out, mgd_dtype out_dtype,
+                               float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ *
  * Commit / rollback after a verification round.  [SD-Serving] "Eine
  * Verifizierungsrunde verstehen": candidates after the first rejection are
  * discarded; [MagicDec] appendix A.1: the draft reads the compressed KV built

@@ -285,6 +285,34 @@ mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, co
   return e == cudaSuccess ? ok() : cuda_fail(e, "snapkv launch");
 }
 
+size_t mgd_topk_draft_workspace_size(int B, int Hq, int Hkv, int D, int kv_cap, int draft_cap) {
+  if (B <= 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || kv_cap < 1 || draft_cap < 1) return kAlign;
+  return align_up(mgd_snapkv_workspace_size(B, Hq, Hkv, D, kv_cap, 1)) +
+         mgd_draft_workspace_size(B, Hq, Hkv, D, draft_cap);
+}
+
+// Selection (the SnapKV call with the draft query as a one-row window and no
+// pooling) into the caller's draft cache, then draft attention over it; the
+// workspace holds both calls' scratch one after the other.
+mgd_status mgd_topk_draft_attn(const void *q, const void *k, const void *v, const int32_t *kv_len, int B, int Hq,
+                               int Hkv, int D, int kv_cap, int64_t kv_batch_stride, int64_t kv_head_stride, int K,
+                               float sm_scale, mgd_dtype in_dtype, int32_t *sel_idx, void *k_draft,
+                               void *v_draft, int draft_cap, int32_t *draft_len, void *out, mgd_dtype out_dtype,
+                               float *lse, void *ws, size_t ws_bytes, void *stream) {
+  if (K < 1) return fail(MGD_ERR_INVALID_ARG, "budget K must be >= 1 (got %d)", K);
+  if (B > 0 && !out) return fail(MGD_ERR_INVALID_ARG, "null pointer argument");
+  const size_t need = mgd_topk_draft_workspace_size(B, Hq, Hkv, D, kv_cap, draft_cap);
+  if (B > 0 && ws_bytes < need) return fail(MGD_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  const size_t ws_sel = B > 0 ? align_up(mgd_snapkv_workspace_size(B, Hq, Hkv, D, kv_cap, 1)) : 0;
+  mgd_status st = mgd_snapkv_select(q, k, v, kv_len, B, Hq, Hkv, D, kv_cap, kv_batch_stride, kv_head_stride, 1, 1, K,
+                                    sm_scale, in_dtype, sel_idx, k_draft, v_draft, draft_cap, draft_len, nullptr,
+                                    ws, ws_sel, stream);
+  if (st != MGD_OK || B == 0) return st;
+  const int64_t dh = static_cast<int64_t>(draft_cap) * D;
+  return mgd_draft_attn(q, k_draft, v_draft, draft_len, B, Hq, Hkv, D, draft_cap, dh * Hkv, dh, sm_scale, in_dtype,
+                        out, out_dtype, lse, static_cast<unsigned char *>(ws) + ws_sel, ws_bytes - ws_sel, stream);
+}
+
 size_t mgd_spec_workspace_size(int B, int gamma, int V) {
   if (B <= 0 || gamma < 1 || V < 1) return kAlign;
   return plan_spec(B, gamma, V).ws_bytes;

@@ -37,6 +37,9 @@ SIGNATURES = {
     "mgd_snapkv_workspace_size": (_sz, [_i32] * 6),
     "mgd_snapkv_select": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _i32, _i32,
                                  _f32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "mgd_topk_draft_workspace_size": (_sz, [_i32] * 6),
+    "mgd_topk_draft_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _f32, _i32,
+                                   _vp, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp]),
     "mgd_spec_workspace_size": (_sz, [_i32] * 3),
     "mgd_spec_sample": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "mgd_streaming_select": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _i32, _i32, _vp, _vp,
@@ -140,6 +143,19 @@ def mgd_draft_attn(q, k_draft, v_draft, draft_len, B, Hq, Hkv, D, k_cap, kv_batc
     _check(load().mgd_draft_attn(_ptr(q), _ptr(k_draft), _ptr(v_draft), _ptr(draft_len), B, Hq, Hkv, D, k_cap,
                                  kv_batch_stride, kv_head_stride, sm_scale, in_dtype, _ptr(out), out_dtype,
                                  _ptr(lse), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def mgd_topk_draft_workspace_size(B, Hq, Hkv, D, kv_cap, draft_cap):
+    return load().mgd_topk_draft_workspace_size(B, Hq, Hkv, D, kv_cap, draft_cap)
+
+
+def mgd_topk_draft_attn(q, k, v, kv_len, B, Hq, Hkv, D, kv_cap, kv_batch_stride, kv_head_stride, K, sm_scale,
+                        in_dtype, sel_idx, k_draft, v_draft, draft_cap, draft_len, out, out_dtype, lse, ws, ws_bytes,
+                        stream=None):
+    _check(load().mgd_topk_draft_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_len), B, Hq, Hkv, D, kv_cap,
+                                      kv_batch_stride, kv_head_stride, K, sm_scale, in_dtype, _ptr(sel_idx),
+                                      _ptr(k_draft), _ptr(v_draft), draft_cap, _ptr(draft_len), _ptr(out), out_dtype,
+                                      _ptr(lse), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def mgd_snapkv_workspace_size(B, Hq, Hkv, D, kv_cap, W):

@@ -93,6 +93,35 @@ def snapkv_select(q_win, k, v, kv_len, W, pool, K, draft_cap=None, sm_scale=None
     return out
 
 
+def topk_draft_attn(q, k, v, kv_len, K, draft_cap=None, sm_scale=None, out_dtype=torch.float32, ws=None, out=None,
+                    stream=None):
+    """One dynamic top-K draft step: q [B,Hq,D] (or [B,1,Hq,D]) at position kv_len-1 selects the newest row plus
+    the K-1 earlier rows it attends to most (summed over the heads of a KV head) and attends over them.
+    Returns dict(out [B,Hq,D], lse [B,Hq], sel_idx, k_draft, v_draft, draft_len)."""
+    if q.dim() == 4:
+        q = q[:, 0]
+    B, Hq, D = q.shape
+    Hkv, cap = k.shape[1], k.shape[2]
+    sb, sh = _kv_strides(k, v, D)
+    cap_d = K if draft_cap is None else draft_cap
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
+    dev = q.device
+    if out is None:
+        out = dict(out=torch.empty((B, Hq, D), dtype=out_dtype, device=dev),
+                   lse=torch.empty((B, Hq), dtype=torch.float32, device=dev),
+                   sel_idx=torch.empty((B, Hkv, cap_d), dtype=torch.int32, device=dev),
+                   k_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
+                   v_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
+                   draft_len=torch.empty((B,), dtype=torch.int32, device=dev))
+    need = mgd.mgd_topk_draft_workspace_size(B, Hq, Hkv, D, cap, cap_d)
+    if ws is None:
+        ws = workspace(need, dev)
+    mgd.mgd_topk_draft_attn(q, k, v, kv_len, B, Hq, Hkv, D, cap, sb, sh, K, scale, _dtype_code(k), out["sel_idx"],
+                            out["k_draft"], out["v_draft"], cap_d, out["draft_len"], out["out"],
+                            _dtype_code(out["out"]), out["lse"], ws, ws.numel(), stream)
+    return out
+
+
 def draft_draw(draft_logits, u, draft_tokens=None, row=-1, ws=None, stream=None):
     """Fill draft_tokens [B, gamma] from softmax(draft_logits[b, s]) with u[b, s, 0] (row < 0: every s)."""
     B, gamma, V = draft_logits.shape

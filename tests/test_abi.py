@@ -112,6 +112,31 @@ def test_snapkv_rejects_bad_arguments_on_host(lib):
     assert call(sel_idx=None) == 1
 
 
+def test_topk_draft_rejects_bad_arguments_on_host(lib):
+    from long_context_speculative_split_gb300 import mgd
+
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, kv_len=FAKE, B=2, Hq=8, Hkv=2, D=128, kv_cap=4096,
+                 kv_batch_stride=2 * 4096 * 128, kv_head_stride=4096 * 128, K=256, sm_scale=0.1,
+                 in_dtype=mgd.MGD_BF16, sel_idx=FAKE, k_draft=FAKE, v_draft=FAKE, draft_cap=256, draft_len=FAKE,
+                 out=FAKE, out_dtype=mgd.MGD_F32, lse=None, ws=FAKE, ws_bytes=1 << 40, stream=0)
+        a.update(kw)
+        try:
+            mgd.mgd_topk_draft_attn(**a)
+            return 0
+        except mgd.MgdError as e:
+            return e.status
+    assert call(K=0) == 1
+    assert call(draft_cap=100) == 1   # draft_cap < K
+    assert call(D=80) == 2
+    assert call(out=None) == 1
+    assert call(ws_bytes=1024) == 3
+    assert call(B=0, q=None, k=None, v=None, kv_len=None, out=None, ws=None) == 0
+    small = mgd.mgd_topk_draft_workspace_size(2, 8, 2, 128, 4096, 256)
+    assert small > mgd.mgd_snapkv_workspace_size(2, 8, 2, 128, 4096, 1)
+    assert mgd.mgd_topk_draft_workspace_size(2, 8, 2, 128, 8192, 256) > small
+
+
 def test_spec_sample_rejects_bad_arguments_on_host(lib):
     from long_context_speculative_split_gb300 import mgd
 
