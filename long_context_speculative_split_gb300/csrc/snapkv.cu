@@ -401,7 +401,7 @@ __device__ unsigned block_excl_scan(unsigned v, unsigned *sm_warp, unsigned *tot
   return r;
 }
 
-__global__ void __launch_bounds__(kSelThreads)
+__global__ void __launch_bounds__(kSelThreads, 2)
     snap_select(const unsigned char *__restrict__ k, const unsigned char *__restrict__ v,
                 const int32_t *__restrict__ kv_len, SelParams sp, int32_t *__restrict__ sel_idx,
                 unsigned char *__restrict__ k_draft, unsigned char *__restrict__ v_draft,
@@ -476,27 +476,66 @@ __global__ void __launch_bounds__(kSelThreads)
       __syncthreads();
     }
   }
-  // ---- 3. ordered compaction: position of j = #(greater before j) + min(#(equal before j), krem)
+  // ---- 3. ordered compaction: position of j = #(greater before j) + min(#(equal before j), krem).
+  //         Each warp owns a contiguous segment, read 32 consecutive positions
+  //         at a time; ballots order the positions inside a warp and one scan
+  //         of the 32 warp totals orders the warps.
   const unsigned tau = prefix;
-  unsigned run_gt = 0u, run_eq = 0u;
-  for (int base = 0; base < n; base += kSelThreads) {
-    const int j = base + threadIdx.x;
-    unsigned gt = 0u, eq = 0u;
-    if (j < n) {
-      if (!partial) {
-        gt = (ktop >= n) ? 1u : 0u;  // keep all or nothing
-      } else {
+  const bool keep_all = !partial && ktop >= n;  // ktop >= n keeps the whole prefix, ktop <= 0 none of it
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int wseg = ((n + kSelThreads / 32 - 1) / (kSelThreads / 32) + 31) / 32 * 32;
+  const int w0 = min(n, warp * wseg), w1 = min(n, w0 + wseg);
+  auto classify = [&](int j, unsigned &gt, unsigned &eq) {
+    gt = 0u;
+    eq = 0u;
+    if (j < w1) {
+      if (partial) {
         const unsigned key = __float_as_uint(pooled[j]);
-        gt = key > tau;
-        eq = key == tau;
+        gt = key > tau ? 1u : 0u;
+        eq = key == tau ? 1u : 0u;
+      } else {
+        gt = keep_all ? 1u : 0u;
       }
     }
-    unsigned tot;
-    const unsigned pre = block_excl_scan((gt << 16) | eq, sm_warp, &tot);
-    const unsigned g_before = run_gt + (pre >> 16), e_before = run_eq + (pre & 0xffffu);
-    if (gt || (eq && e_before < krem)) sel[g_before + min(e_before, krem)] = j;
-    run_gt += tot >> 16;
-    run_eq += tot & 0xffffu;
+  };
+  unsigned gt_cnt = 0u, eq_cnt = 0u;
+  for (int jb = w0; jb < w1; jb += 32) {
+    unsigned gt, eq;
+    classify(jb + lane, gt, eq);
+    gt_cnt += __popc(__ballot_sync(0xffffffffu, gt));
+    eq_cnt += __popc(__ballot_sync(0xffffffffu, eq));
+  }
+  if (lane == 0) {
+    hist[warp] = gt_cnt;
+    hist[32 + warp] = eq_cnt;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scans of the 32 warp totals
+    unsigned g = hist[lane], e = hist[32 + lane];
+    unsigned gs = g, es = e;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y1 = __shfl_up_sync(0xffffffffu, gs, o);
+      const unsigned y2 = __shfl_up_sync(0xffffffffu, es, o);
+      if (lane >= o) {
+        gs += y1;
+        es += y2;
+      }
+    }
+    hist[64 + lane] = gs - g;
+    hist[96 + lane] = es - e;
+  }
+  __syncthreads();
+  unsigned g_before = hist[64 + warp], e_before = hist[96 + warp];
+  for (int jb = w0; jb < w1; jb += 32) {
+    const int j = jb + lane;
+    unsigned gt, eq;
+    classify(j, gt, eq);
+    const unsigned gb = __ballot_sync(0xffffffffu, gt), eb = __ballot_sync(0xffffffffu, eq);
+    const unsigned gpos = g_before + __popc(gb & lt_mask), epos = e_before + __popc(eb & lt_mask);
+    if (gt || (eq && epos < krem)) sel[gpos + min(epos, krem)] = j;
+    g_before += __popc(gb);
+    e_before += __popc(eb);
   }
   for (int w = threadIdx.x; w < sp.W; w += kSelThreads) sel[ktop + w] = n + w;
   for (int i = Keff + threadIdx.x; i < sp.draft_cap; i += kSelThreads) sel[i] = -1;
@@ -509,12 +548,28 @@ __global__ void __launch_bounds__(kSelThreads)
   const unsigned char *vs = v + b * sp.bstride_bytes + hkv * sp.hstride_bytes;
   unsigned char *kd = k_draft + pr * sp.draft_cap * sp.row_bytes;
   unsigned char *vd = v_draft + pr * sp.draft_cap * sp.row_bytes;
-  for (int i = threadIdx.x; i < Keff * vecs; i += kSelThreads) {
-    const int row = i / vecs, c = i % vecs;
-    const size_t src = static_cast<size_t>(sel[row]) * sp.row_bytes + c * 16;
-    const size_t dst = static_cast<size_t>(row) * sp.row_bytes + c * 16;
-    *reinterpret_cast<uint4 *>(kd + dst) = __ldg(reinterpret_cast<const uint4 *>(ks + src));
-    *reinterpret_cast<uint4 *>(vd + dst) = __ldg(reinterpret_cast<const uint4 *>(vs + src));
+  const int total = Keff * vecs;
+  for (int i0 = threadIdx.x; i0 < total; i0 += 2 * kSelThreads) {  // 4 loads in flight per thread
+    uint4 kx[2], vx[2];
+    size_t dst[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = i0 + u * kSelThreads;
+      if (i < total) {
+        const int row = i / vecs, c = i % vecs;
+        const size_t src = static_cast<size_t>(sel[row]) * sp.row_bytes + c * 16;
+        dst[u] = static_cast<size_t>(row) * sp.row_bytes + c * 16;
+        kx[u] = __ldg(reinterpret_cast<const uint4 *>(ks + src));
+        vx[u] = __ldg(reinterpret_cast<const uint4 *>(vs + src));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (i0 + u * kSelThreads < total) {
+        *reinterpret_cast<uint4 *>(kd + dst[u]) = kx[u];
+        *reinterpret_cast<uint4 *>(vd + dst[u]) = vx[u];
+      }
+    }
   }
 }
 
