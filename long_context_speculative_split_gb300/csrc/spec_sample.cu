@@ -53,25 +53,48 @@ __global__ void __launch_bounds__(kStatThreads) spec_stats_kernel(const float *_
   const float *x = row_ptr(target, draft, b, r, sp.gamma, sp.V);
   const int lo = s * sp.split;
   const int hi = min(lo + sp.split, sp.V);
+  // Rounds of 16 values per thread (all loads in flight), one update of the
+  // running max per round, then one FMA + exp2 + add per value.
   float m = -INFINITY, l = 0.f;
-  auto add = [&](float v) {
-    if (v > m) {
-      l = l * exp2f((m - v) * kLog2e) + 1.f;
-      m = v;
-    } else if (v != -INFINITY) {
-      l += exp2f((v - m) * kLog2e);
+  auto round16 = [&](const float (&v)[16]) {
+    float mx = v[0];
+#pragma unroll
+    for (int k = 1; k < 16; ++k) mx = fmaxf(mx, v[k]);
+    if (mx > m) {
+      l *= exp2f((m - mx) * kLog2e);  // 0 while m is -inf
+      m = mx;
+    }
+    if (m != -INFINITY) {
+      const float ml = m * kLog2e;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) l += exp2f(fmaf(v[k], kLog2e, -ml));
     }
   };
-  if (VEC4) {
-    for (int i = lo + 4 * threadIdx.x; i < hi; i += 4 * kStatThreads) {
-      const float4 v = __ldcs(reinterpret_cast<const float4 *>(x + i));
-      add(v.x);
-      add(v.y);
-      add(v.z);
-      add(v.w);
+  if (VEC4) {  // V % 4 == 0: a float4 is either wholly inside the slice or wholly past it
+    for (int i = lo + 4 * threadIdx.x; i < hi; i += 16 * kStatThreads) {
+      float v[16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int ii = i + u * 4 * kStatThreads;
+        const float4 f = (ii < hi) ? __ldcs(reinterpret_cast<const float4 *>(x + ii))
+                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        v[4 * u] = f.x;
+        v[4 * u + 1] = f.y;
+        v[4 * u + 2] = f.z;
+        v[4 * u + 3] = f.w;
+      }
+      round16(v);
     }
   } else {
-    for (int i = lo + threadIdx.x; i < hi; i += kStatThreads) add(__ldcs(x + i));
+    for (int i = lo + threadIdx.x; i < hi; i += 16 * kStatThreads) {
+      float v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int ii = i + u * kStatThreads;
+        v[u] = (ii < hi) ? __ldcs(x + ii) : -INFINITY;
+      }
+      round16(v);
+    }
   }
   // block reduce of (m, l)
   __shared__ float sm[2][kStatThreads / 32];
