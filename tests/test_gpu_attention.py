@@ -27,14 +27,14 @@ def _case(B, T, Hq, Hkv, D, lens, cap, seed, dtype=torch.bfloat16, hh=True):
 
 
 CASES = [
-    # B, T, Hq, Hkv, D, lens, cap
-    (2, 4, 32, 8, 128, [1000, 77], 1000),          # G*T = 16 rows, several chunks + merge
+    # B, T, Hq, Hkv, D, lens, cap  (few pairs: one wave of whole-sequence units)
+    (2, 4, 32, 8, 128, [1000, 77], 1000),          # G*T = 16 rows
     (3, 5, 32, 8, 128, [4101, 64, 129], 4101),     # 20 rows, ragged tails, one-tile and tile+1
     (2, 1, 8, 2, 128, [513, 1], 513),              # draft form, a single key
     (2, 3, 32, 8, 64, [300, 3], 300),              # head_dim 64, kv_len == T
     (1, 8, 16, 4, 128, [2000], 2048),              # 32 rows (four n8 tiles)
     (2, 5, 64, 8, 128, [700, 650], 700),           # 40 rows -> two row groups
-    (2, 2, 4, 4, 128, [5000, 4999], 5000),         # MHA (G=1), many chunks
+    (2, 2, 4, 4, 128, [5000, 4999], 5000),         # MHA (G=1)
     (1, 4, 32, 8, 128, [64], 64),                  # exactly one tile
     (1, 4, 32, 8, 128, [65], 128),                 # one key into the second tile
 ]
@@ -48,6 +48,23 @@ def test_verify_bf16_matches_oracle(case):
     q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=sum(lens) + T)
     out, lse = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev))
     torch.cuda.synchronize()
+    ref, ref_lse = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(D))
+    assert_attention_close(out, ref)
+    assert_lse_close(lse, ref_lse)
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv", [(40, 4, 32, 8), (82, 2, 4, 4)], ids=["G4_T4_320pairs", "MHA_T2_328pairs"])
+def test_verify_split_units_and_merges_match_oracle(B, T, Hq, Hkv):
+    """More (sequence, KV head) pairs than CTA slots on a 152-SM part: short units of 256 keys,
+    several per sequence (ragged lengths, ragged last units), merged by the last CTA of each
+    sequence; every output is compared with the oracle."""
+    dev = gpu_or_skip()
+    D, cap = 128, 1000
+    g = torch.Generator().manual_seed(B)
+    lens = torch.randint(T, cap + 1, (B,), generator=g).tolist()
+    lens[0] = cap
+    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=B + T)
+    out, lse = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev))
     ref, ref_lse = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(D))
     assert_attention_close(out, ref)
     assert_lse_close(lse, ref_lse)
