@@ -18,6 +18,8 @@
 //                        head, row group, key chunk); K tiles arrive through
 //                        TMA; pass 1 computes each window row's log-sum-exp,
 //                        pass 2 sums the probabilities per prefix key;
+//   snap_score_kr<PASS>  the same two passes for windows of <= 32 rows, with
+//                        the keys of a tile spread over the warps;
 //   snap_score_simt      the same two passes on CUDA cores (float32 inputs);
 //   snap_select          max-pool, 3-pass radix select of the K_eff-W-th
 //                        largest pooled score, ordered compaction, gather.
@@ -294,6 +296,225 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
               make_float2(m_run[mt][hf], l);
         }
       }
+  }
+}
+
+// ---------------------------------------------------------------- small windows
+// Windows of at most 32 rows (W * G <= 32, e.g. the draft query alone as a
+// one-row window): S^T = K Qw^T with the keys on the M side, so each consumer
+// warp takes 16 keys of every 64-key tile for all rows (NT n8 row tiles) and a
+// short window costs the same per key as a long one.  Pass 1: per row, an
+// online (max, sum) over the keys (a max across the 8 key lanes, sums reduced
+// at the end); pass 2: per key, the sum over rows of exp2(s - lse_row) (a sum
+// across the 4 row lanes).
+template <int D>
+struct KrLayout {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStageBytes = kBoxes * kBoxBytes;  // 64 keys
+  static constexpr int kQStride = D + 8;                  // bf16 per staged row (bank-conflict padding)
+  static constexpr int off_q = kScoreStages * kStageBytes;
+  static constexpr int off_lse = off_q + 32 * kQStride * 2;  // float [32]
+  static constexpr int off_red = off_lse + 32 * 4;           // float2 [4][32]
+  static constexpr int off_bar = off_red + 4 * 32 * 8;
+  static constexpr int bytes = off_bar + 2 * kScoreStages * 8;
+  static constexpr int alloc = bytes + 1024;
+};
+
+template <int D, int NT, int PASS>
+__global__ void __launch_bounds__(kScoreThreads, 2)
+    snap_score_kr(const __grid_constant__ CUtensorMap kmap, const __nv_bfloat16 *__restrict__ qw,
+                  const int32_t *__restrict__ kv_len, unsigned char *__restrict__ ws, SnapK p) {
+  using Lay = KrLayout<D>;
+  constexpr int KK = D / 16;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __nv_bfloat16 *sQ = reinterpret_cast<__nv_bfloat16 *>(smem + Lay::off_q);
+  float *sm_lse = reinterpret_cast<float *>(smem + Lay::off_lse);
+  float2 *sm_red = reinterpret_cast<float2 *>(smem + Lay::off_red);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::off_bar);
+  uint64_t *empty = full + kScoreStages;
+  WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+  float2 *part = reinterpret_cast<float2 *>(ws + p.off_part);
+  float *scores = reinterpret_cast<float *>(ws + p.off_scores);
+
+  const int chunk = blockIdx.x % p.nchunk;
+  const int pair = blockIdx.x / p.nchunk;  // one row group (rows <= 32)
+  const int hkv = pair % p.Hkv;
+  const int b = pair / p.Hkv;
+  const int L = kv_len[b];
+  if (L < p.W || L > p.kv_cap) {
+    if (threadIdx.x == 0 && chunk == 0 && hkv == 0) raise_error(hdr, 0x2u);
+    return;
+  }
+  const int kend = (PASS == 1) ? L : L - p.W;
+  const int start = chunk * p.C;
+  if (start >= kend) return;
+  const int end = min(start + p.C, kend);
+  const int ntiles = (end - start + 63) / 64;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScoreStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    fence_mbar_init();
+  }
+  // window rows r = w * G + g staged in shared memory (zero rows past p.rows)
+  for (int i = threadIdx.x; i < 32 * (D / 8); i += kScoreThreads) {
+    const int r = i / (D / 8), c = i % (D / 8);
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (r < p.rows) {
+      const int w = r / p.G, g = r % p.G;
+      x = *reinterpret_cast<const uint4 *>(qw + ((static_cast<size_t>(b) * p.W + w) * p.Hq + hkv * p.G + g) * D + 8 * c);
+    }
+    *reinterpret_cast<uint4 *>(sQ + r * Lay::kQStride + 8 * c) = x;
+  }
+  if (PASS == 2 && threadIdx.x < 32) {  // log2-sum-exp of every row from the pass-1 partials
+    const int r = threadIdx.x;
+    float v = INFINITY;  // padding rows: probability 0
+    if (r < p.rows) {
+      const int nch1 = (L + p.C - 1) / p.C;
+      const float2 *pp = part + static_cast<size_t>(pair) * p.nchunk * kRowsPerCta + r;
+      float M = -INFINITY;
+      for (int c = 0; c < nch1; ++c) M = fmaxf(M, pp[c * kRowsPerCta].x);
+      float S = 0.f;
+      for (int c = 0; c < nch1; ++c) {
+        const float2 x = pp[c * kRowsPerCta];
+        if (x.y > 0.f) S += x.y * exp2f(x.x - M);
+      }
+      v = M + log2f(S);
+    }
+    sm_lse[r] = v;
+  }
+  __syncthreads();
+
+  if (warp == 4) {  // producer
+    if (lane != 0) return;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = 0; t < ntiles; ++t) {
+      if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+        raise_error(hdr, 0x8u);
+        return;
+      }
+      mbar_arrive_expect_tx(&full[stage], Lay::kStageBytes);
+#pragma unroll
+      for (int h = 0; h < Lay::kBoxes; ++h)
+        tma_load_4d(smem + stage * Lay::kStageBytes + h * kBoxBytes, &kmap, &full[stage], h * 64, start + 64 * t,
+                    hkv, b);
+      if (++stage == kScoreStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    return;
+  }
+
+  const int gid = lane >> 2, tig = lane & 3;
+  int lim[NT][2];      // pass 1: last key row (j, e) sees; -1 for padding rows
+  float lr[NT][2];     // pass 2: log2-sum-exp of row (j, e)
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 8 * j + 2 * tig + e;
+      lim[j][e] = (r < p.rows) ? (L - p.W + r / p.G) : -1;
+      lr[j][e] = (PASS == 2) ? sm_lse[r] : 0.f;
+      m_run[j][e] = -INFINITY;
+      l_run[j][e] = 0.f;
+    }
+  const uint32_t qaddr = smem_addr(sQ) + 2u * (((lane & 7) + 8 * (lane >> 4)) * Lay::kQStride + 8 * ((lane >> 3) & 1));
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int t = 0; t < ntiles; ++t) {
+    if (!mbar_wait(&full[stage], phase)) {
+      raise_error(hdr, 0x8u);
+      break;  // still meets the end-of-unit barrier below
+    }
+    const uint32_t kbase = smem_addr(smem + stage * Lay::kStageBytes);
+    const int key0 = start + 64 * t + warp * 16;
+    float s[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s[j][c] = 0.f;
+    const int kr = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+    for (int kk = 0; kk < KK; ++kk) {
+      const int d = 16 * kk + 8 * (lane >> 4);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kbase + (d >> 6) * kBoxBytes + swz128(kr, (d & 63) >> 3), a0, a1, a2, a3);
+#pragma unroll
+      for (int jp = 0; jp < (NT + 1) / 2; ++jp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(qaddr + 2u * (16 * jp * Lay::kQStride + 16 * kk), b0, b1, b2, b3);
+        mma_bf16_16816(s[2 * jp], a0, a1, a2, a3, b0, b1);
+        if (2 * jp + 1 < NT) mma_bf16_16816(s[2 * jp + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == kScoreStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    const int k_lo = key0 + gid, k_hi = key0 + gid + 8;  // accumulator rows gid / gid + 8
+    if (PASS == 1) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float v0 = (k_lo <= lim[j][e]) ? s[j][e] * p.sl2 : -INFINITY;
+          const float v1 = (k_hi <= lim[j][e]) ? s[j][2 + e] * p.sl2 : -INFINITY;
+          const float mx = warp_max_xor(fmaxf(v0, v1), 4, 16);
+          const float mn = fmaxf(m_run[j][e], mx);
+          const float mu = (mn == -INFINITY) ? 0.f : mn;
+          l_run[j][e] = l_run[j][e] * exp2f(m_run[j][e] - mu) + exp2f(v0 - mu) + exp2f(v1 - mu);
+          m_run[j][e] = mn;
+        }
+    } else {
+      float a_lo = 0.f, a_hi = 0.f;
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          a_lo += exp2f(s[j][e] * p.sl2 - lr[j][e]);
+          a_hi += exp2f(s[j][2 + e] * p.sl2 - lr[j][e]);
+        }
+      a_lo = warp_sum_xor(a_lo, 1, 2);
+      a_hi = warp_sum_xor(a_hi, 1, 2);
+      if (tig == 0) {
+        float *dst = scores + static_cast<size_t>(pair) * p.kv_cap;
+        if (k_lo < end) dst[k_lo] = a_lo;
+        if (k_hi < end) dst[k_hi] = a_hi;
+      }
+    }
+  }
+
+  if (PASS == 1) {
+    // (max, sum) of each row over this warp's keys, then over the 4 warps
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float l = warp_sum_xor(l_run[j][e], 4, 16);
+        if (gid == 0) sm_red[warp * 32 + 8 * j + 2 * tig + e] = make_float2(m_run[j][e], l);
+      }
+    named_bar(1, 128);
+    if (threadIdx.x < 8 * NT) {
+      const int r = threadIdx.x;
+      float M = -INFINITY;
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_red[w * 32 + r].x);
+      const float mu = (M == -INFINITY) ? 0.f : M;
+      float S = 0.f;
+      for (int w = 0; w < 4; ++w) {
+        const float2 x = sm_red[w * 32 + r];
+        if (x.y > 0.f) S += x.y * exp2f(x.x - mu);
+      }
+      part[(static_cast<size_t>(pair) * p.nchunk + chunk) * kRowsPerCta + r] = make_float2(M, S);
+    }
   }
 }
 
@@ -649,6 +870,35 @@ cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, cons
   } else if (qmap != nullptr && snap_tc05_eligible(p)) {
     e = launch_snap_score_tc05(p, a, *kmap, *qmap);
     if (e != cudaSuccess) return e;
+  } else if (p.rows <= 32) {
+    const int units = p.pairs * p.nchunk;
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q_win);
+    const int nt = (p.rows <= 8) ? 1 : (p.rows <= 16) ? 2 : 4;
+#define MGD_KR(DD, NTT, PP)                                                                               \
+  do {                                                                                                    \
+    auto kern = snap_score_kr<DD, NTT, PP>;                                                               \
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KrLayout<DD>::alloc);     \
+    if (e != cudaSuccess) return e;                                                                       \
+    kern<<<units, kScoreThreads, KrLayout<DD>::alloc, a.stream>>>(*kmap, q, a.kv_len, ws, kp);            \
+    e = cudaGetLastError();                                                                               \
+    if (e != cudaSuccess) return e;                                                                       \
+  } while (0)
+#define MGD_KR_PASSES(DD, NTT) \
+  do {                         \
+    MGD_KR(DD, NTT, 1);        \
+    MGD_KR(DD, NTT, 2);        \
+  } while (0)
+    if (p.D == 128) {
+      if (nt == 1) MGD_KR_PASSES(128, 1);
+      else if (nt == 2) MGD_KR_PASSES(128, 2);
+      else MGD_KR_PASSES(128, 4);
+    } else {
+      if (nt == 1) MGD_KR_PASSES(64, 1);
+      else if (nt == 2) MGD_KR_PASSES(64, 2);
+      else MGD_KR_PASSES(64, 4);
+    }
+#undef MGD_KR_PASSES
+#undef MGD_KR
   } else {
     if (p.RG > 1) {
       e = cudaMemsetAsync(ws + p.off_scores, 0, p.off_pooled - p.off_scores, a.stream);
