@@ -282,9 +282,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
           const float mx = warp_max_xor(fmaxf(v0, v1), 4, 16);
           const float mnew = fmaxf(m_run[j][e], mx);
           const float muse = (mnew == -INFINITY) ? 0.f : mnew;
-          alpha[e] = exp2f(m_run[j][e] - muse);
-          const float p0 = exp2f(v0 - muse);
-          const float p1 = exp2f(v1 - muse);
+          alpha[e] = ex2(m_run[j][e] - muse);
+          const float p0 = ex2(v0 - muse);
+          const float p1 = ex2(v1 - muse);
           l_run[j][e] = l_run[j][e] * alpha[e] + p0 + p1;
           m_run[j][e] = mnew;
           s[j][e] = p0;

@@ -31,6 +31,14 @@ __device__ __forceinline__ void raise_error(WsHeader *hdr, unsigned bit) {
   atomicOr(&hdr->err, bit);
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32): results below
+// 2^-126 flush to zero, which no softmax sum here can notice.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- shared memory
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -282,8 +282,8 @@ __global__ void __launch_bounds__(kT5Threads, 2)
 #pragma unroll
           for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int c = 0; c < 32; ++c) acc += exp2f(fmaf(v[i][c], p.sl2, -mu));
-          l_run = l_run * exp2f(m_run - mu) + acc;
+            for (int c = 0; c < 32; ++c) acc += ex2(fmaf(v[i][c], p.sl2, -mu));
+          l_run = l_run * ex2(m_run - mu) + acc;
           m_run = mn;
         } else {
           // key kt0 + tl, window rows 64h + c
@@ -292,8 +292,8 @@ __global__ void __launch_bounds__(kT5Threads, 2)
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
               const float4 lr = *reinterpret_cast<const float4 *>(&sm_lse[64 * h + 32 * i + c]);
-              acc2 += exp2f(fmaf(v[i][c], p.sl2, -lr.x)) + exp2f(fmaf(v[i][c + 1], p.sl2, -lr.y)) +
-                      exp2f(fmaf(v[i][c + 2], p.sl2, -lr.z)) + exp2f(fmaf(v[i][c + 3], p.sl2, -lr.w));
+              acc2 += ex2(fmaf(v[i][c], p.sl2, -lr.x)) + ex2(fmaf(v[i][c + 1], p.sl2, -lr.y)) +
+                      ex2(fmaf(v[i][c + 2], p.sl2, -lr.z)) + ex2(fmaf(v[i][c + 3], p.sl2, -lr.w));
             }
         }
       }

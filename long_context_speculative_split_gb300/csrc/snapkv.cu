@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
           const float mx = warp_max_xor(fmaxf(v0, v1), 4, 16);
           const float mn = fmaxf(m_run[j][e], mx);
           const float mu = (mn == -INFINITY) ? 0.f : mn;
-          l_run[j][e] = l_run[j][e] * exp2f(m_run[j][e] - mu) + exp2f(v0 - mu) + exp2f(v1 - mu);
+          l_run[j][e] = l_run[j][e] * ex2(m_run[j][e] - mu) + ex2(v0 - mu) + ex2(v1 - mu);
           m_run[j][e] = mn;
         }
     } else {
@@ -480,8 +480,8 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
       for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          a_lo += exp2f(s[j][e] * p.sl2 - lr[j][e]);
-          a_hi += exp2f(s[j][2 + e] * p.sl2 - lr[j][e]);
+          a_lo += ex2(s[j][e] * p.sl2 - lr[j][e]);
+          a_hi += ex2(s[j][2 + e] * p.sl2 - lr[j][e]);
         }
       a_lo = warp_sum_xor(a_lo, 1, 2);
       a_hi = warp_sum_xor(a_hi, 1, 2);

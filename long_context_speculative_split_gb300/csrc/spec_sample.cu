@@ -61,13 +61,13 @@ __global__ void __launch_bounds__(kStatThreads) spec_stats_kernel(const float *_
 #pragma unroll
     for (int k = 1; k < 16; ++k) mx = fmaxf(mx, v[k]);
     if (mx > m) {
-      l *= exp2f((m - mx) * kLog2e);  // 0 while m is -inf
+      l *= ex2((m - mx) * kLog2e);  // 0 while m is -inf
       m = mx;
     }
     if (m != -INFINITY) {
       const float ml = m * kLog2e;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) l += exp2f(fmaf(v[k], kLog2e, -ml));
+      for (int k = 0; k < 16; ++k) l += ex2(fmaf(v[k], kLog2e, -ml));
     }
   };
   if (VEC4) {  // V % 4 == 0: a float4 is either wholly inside the slice or wholly past it
