@@ -219,17 +219,21 @@ class Workload:
 
     def _per_launch_ms(self, fn, reps, flush_l2=False):
         """Average device time of `reps` back-to-back calls between two events on the launching
-        stream (median of 3 trials).  Back to back, each call's host overhead overlaps the
-        previous launch instead of appearing as idle GPU time; with `flush_l2` a 512 MB write
-        evicts L2 first (the host queues the launches while it runs)."""
+        stream (median of 3 trials).  A short GPU sleep ahead of the first event keeps the stream
+        busy while the host queues every call (a call costs tens of microseconds of host time,
+        more than a small kernel runs), so the events bracket device work only: each launch,
+        its workspace reset and the gaps between them.  With `flush_l2` a 512 MB write evicts
+        L2 first."""
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for _ in range(2):
             fn()
         flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=self.dev) if flush_l2 else None
+        sleep_cycles = int(2.1e9 * (2e-3 + reps * 60e-6))  # covers the host's queueing of `reps` calls
         times = []
         for _ in range(3):
             if flush is not None:
                 flush.fill_(1.0)
+            torch.cuda._sleep(sleep_cycles)
             s.record()
             for _ in range(reps):
                 fn()
