@@ -651,31 +651,37 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   const int ktop = Keff - sp.W;
   const int r = sp.pool / 2;
 
-  // ---- 1. max-pool (and the optional copy out)
+  const bool partial = (ktop > 0 && ktop < n);
+  // ---- 1. max-pool (and the optional copy out), with the first radix
+  //         pass's histogram of the top 11 bits
+  for (int i = threadIdx.x; i < 2048; i += kSelThreads) hist[i] = 0u;
+  __syncthreads();
   for (int j = threadIdx.x; j < n; j += kSelThreads) {
     float m = s[j];
     const int lo = max(0, j - r), hi = min(n - 1, j + r);
     for (int t = lo; t <= hi; ++t) m = fmaxf(m, s[t]);
     pooled[j] = m;
     if (scores_out) scores_out[pr * sp.kv_cap + j] = m;
+    if (partial) atomicAdd(&hist[__float_as_uint(m) >> 21], 1u);
   }
   __syncthreads();
 
   // ---- 2. radix select of the ktop-th largest pooled value (scores are >= 0,
   //         so their IEEE bit patterns order like the values)
   unsigned prefix = 0u, mask = 0u, krem = static_cast<unsigned>(ktop);
-  const bool partial = (ktop > 0 && ktop < n);
   if (partial) {
     for (int pass = 0; pass < 3; ++pass) {
       const int shift = (pass == 0) ? 21 : (pass == 1) ? 10 : 0;
       const int nb = (pass == 2) ? 1024 : 2048;
-      for (int i = threadIdx.x; i < nb; i += kSelThreads) hist[i] = 0u;
-      __syncthreads();
-      for (int j = threadIdx.x; j < n; j += kSelThreads) {
-        const unsigned key = __float_as_uint(pooled[j]);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+      if (pass > 0) {  // pass 0's histogram came with the pooling
+        for (int i = threadIdx.x; i < nb; i += kSelThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int j = threadIdx.x; j < n; j += kSelThreads) {
+          const unsigned key = __float_as_uint(pooled[j]);
+          if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+        }
+        __syncthreads();
       }
-      __syncthreads();
       // bins in descending order, two per thread
       const int b_hi = nb - 1 - 2 * threadIdx.x;
       const int b_lo = b_hi - 1;
