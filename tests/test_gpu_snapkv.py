@@ -79,18 +79,22 @@ def test_bf16_cases_match_oracle(case):
             _check_pair(res, k, v, b, h, lens[b], W, P, K, s[b, h], D)
 
 
-@pytest.mark.parametrize("cid", [2, 3])
+@pytest.mark.parametrize("cid", [2, 3, 4])
 def test_full_size_sampled(cid):
+    """Full-size workloads (config 4: ragged lengths 4k-64k at batch 256) with sampled pairs:
+    the first, the last, the longest sequence's and one random (sequence, KV head)."""
     dev = gpu_or_skip()
     c = wl.CONFIGS[cid]
     kv_len = wl.lengths(c)
-    k, v = wl.kv_cache(c, dev, kv_len=kv_len)
+    k, v = wl.kv_cache(c, dev, kv_len=kv_len, cap=wl.capacity(c))
     qw = wl.window_queries(c, dev)
     res = ops.snapkv_select(qw, k, v, kv_len.to(dev), c["W"], c["pool"], c["K"], want_scores=True)
     torch.cuda.synchronize()
     G = c["Hq"] // c["Hkv"]
     rng = np.random.default_rng(cid)
-    for b, h in [(0, 0), (c["B"] - 1, c["Hkv"] - 1), (int(rng.integers(c["B"])), int(rng.integers(c["Hkv"])))]:
+    pairs = [(0, 0), (c["B"] - 1, c["Hkv"] - 1), (int(np.argmax(kv_len.numpy())), 3),
+             (int(rng.integers(c["B"])), int(rng.integers(c["Hkv"])))]
+    for b, h in pairs:
         L = int(kv_len[b])
         s = window_scores(qw[b:b + 1, :, h * G:(h + 1) * G], k[b:b + 1, h:h + 1, :L], kv_len[b:b + 1], c["W"],
                           1.0 / math.sqrt(c["D"]))
