@@ -191,9 +191,9 @@ class Workload:
         self.bytes_draft = float((2 * Hkv * Keff * D * esz).sum())
         self.bytes_snap = float((2 * Hkv * L * D * esz).sum() + 4 * Hkv * Keff.sum() * D * esz)
         self.bytes_spec = float(B * (2 * self.gamma + 1) * self.V * 4)
-        # SnapKV (2 scoring passes + select), gamma x (draft attention + draw: statistics and finish),
-        # verify, rejection sample (statistics and finish)
-        self.launches_per_step = 3 + self.gamma * 1 + self.gamma * 2 + 1 + 2
+        # SnapKV (2 scoring passes + select), gamma x (draft attention + one-row draw), verify,
+        # rejection sample (statistics and finish)
+        self.launches_per_step = 3 + self.gamma * 1 + self.gamma * 1 + 1 + 2
 
     def step(self, ev=None):
         ops = self.ops

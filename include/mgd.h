@@ -282,8 +282,8 @@ mgd_status mgd_commit_round(const int32_t *num_accepted, int B, int gamma, int H
  * `ws` / `ws_bytes`; inputs and outputs are still caller-provided device
  * memory.  The call allocates nothing.
  *   - Limit: the scratch it needs, mgd_spec_workspace_size(B, gamma, V), must
- *     fit in MGD_NOALLOC_SCRATCH_BYTES (B * (2*gamma+1) * ceil(V/16384) * 8
- *     + 256 bytes; e.g. B <= 1820 at gamma = 4, V = 128256); larger requests
+ *     fit in MGD_NOALLOC_SCRATCH_BYTES (about B * ((2*gamma+1) * ceil(V/16384) * 8
+ *     + 4) + 512 bytes; e.g. B <= 1807 at gamma = 4, V = 128256); larger requests
  *     return MGD_ERR_UNSUPPORTED with an explanation in mgd_last_error().
  *   - The first call on a device (with that device current) looks up the
  *     array's device address with cudaGetSymbolAddress; make that first call

@@ -113,7 +113,7 @@ struct SpecPlan {
   int split;     // elements per statistics block
   int nsplit;    // ceil(V / split)
   int nrows;     // 2*gamma + 1 rows per sequence (gamma+1 target, gamma draft)
-  size_t off_stats, ws_bytes;
+  size_t off_tickets, off_stats, ws_bytes;
 };
 SpecPlan plan_spec(int B, int gamma, int V);
 

@@ -8,7 +8,9 @@
 // accepted one more target token is drawn.  The paragraph after it: this
 // preserves the target distribution.
 //
-// Two kernels per call:
+// A draft step's draw of one draft row is one kernel (spec_draw_row: the
+// statistics of every slice, then the CTA completing a sequence draws its
+// token from the slice holding u * Z).  Otherwise two kernels per call:
 //   1. spec_stats: (max, sum of exp) of every logit row the mode needs, each
 //      row split over several small CTAs (HBM stream, float4 loads, full
 //      occupancy);
@@ -43,18 +45,12 @@ __device__ __forceinline__ const float *row_ptr(const float *target, const float
   return draft + (static_cast<size_t>(b) * gamma + (r - gamma - 1)) * V;
 }
 
+// (max, sum of exp(x - max)) of x[lo, hi) over a kStatThreads block; the
+// result is valid in thread 0.  Rounds of 16 values per thread (all loads in
+// flight), one update of the running max per round, then one FMA + exp2 + add
+// per value.
 template <bool VEC4>
-__global__ void __launch_bounds__(kStatThreads) spec_stats_kernel(const float *__restrict__ target,
-                                                                   const float *__restrict__ draft, StatParams sp,
-                                                                   float2 *__restrict__ stats) {
-  const int b = blockIdx.x / sp.nr;
-  const int r = sp.r_begin + blockIdx.x % sp.nr;
-  const int s = blockIdx.y;
-  const float *x = row_ptr(target, draft, b, r, sp.gamma, sp.V);
-  const int lo = s * sp.split;
-  const int hi = min(lo + sp.split, sp.V);
-  // Rounds of 16 values per thread (all loads in flight), one update of the
-  // running max per round, then one FMA + exp2 + add per value.
+__device__ float2 slice_stats(const float *__restrict__ x, int lo, int hi) {
   float m = -INFINITY, l = 0.f;
   auto round16 = [&](const float (&v)[16]) {
     float mx = v[0];
@@ -112,13 +108,180 @@ __global__ void __launch_bounds__(kStatThreads) spec_stats_kernel(const float *_
     sm[1][w] = l;
   }
   __syncthreads();
+  float2 r = make_float2(-INFINITY, 0.f);
   if (threadIdx.x == 0) {
     float M = -INFINITY;
     for (int i = 0; i < kStatThreads / 32; ++i) M = fmaxf(M, sm[0][i]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
     float Lt = 0.f;
     for (int i = 0; i < kStatThreads / 32; ++i) Lt += sm[1][i] * exp2f((sm[0][i] - Mu) * kLog2e);
-    stats[(static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit + s] = make_float2(M, Lt);
+    r = make_float2(M, Lt);
+  }
+  return r;
+}
+
+template <bool VEC4>
+__global__ void __launch_bounds__(kStatThreads) spec_stats_kernel(const float *__restrict__ target,
+                                                                   const float *__restrict__ draft, StatParams sp,
+                                                                   float2 *__restrict__ stats) {
+  const int b = blockIdx.x / sp.nr;
+  const int r = sp.r_begin + blockIdx.x % sp.nr;
+  const int s = blockIdx.y;
+  const int lo = s * sp.split;
+  const float2 st = slice_stats<VEC4>(row_ptr(target, draft, b, r, sp.gamma, sp.V), lo, min(lo + sp.split, sp.V));
+  if (threadIdx.x == 0) stats[(static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit + s] = st;
+}
+
+// One draft-token draw of a single draft row per sequence (a draft step):
+// every CTA computes one slice's statistics; the CTA that completes a
+// sequence's statistics (atomic ticket) draws its token.  The slice totals
+// locate the slice holding u * Z; the block scans that slice: each thread sums
+// a contiguous segment, warp scans order the threads, one warp turns the
+// running double sum into a float target per warp, and the first thread whose
+// range [excl, incl) holds the target walks its segment.
+template <bool VEC4>
+__global__ void __launch_bounds__(kStatThreads) spec_draw_row_kernel(const float *__restrict__ draft,
+                                                                      int32_t *__restrict__ draft_tokens,
+                                                                      const float *__restrict__ u, StatParams sp,
+                                                                      float2 *__restrict__ stats,
+                                                                      unsigned *__restrict__ tickets) {
+  constexpr int kW = kStatThreads / 32;
+  __shared__ int s_last, s_slice, s_tidx, s_lastpos;
+  __shared__ float s_M, s_trel[kW], s_wsum[kW];
+  __shared__ double s_pre;
+  const int b = blockIdx.x, s = blockIdx.y;
+  const int r = sp.r_begin;                // unified row index of the draft row
+  const int row = r - sp.gamma - 1;        // its draft position
+  const int V = sp.V;
+  const float *x = draft + (static_cast<size_t>(b) * sp.gamma + row) * V;
+  const float2 *st_b = stats + (static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit;
+  {
+    const int lo = s * sp.split;
+    const float2 st = slice_stats<VEC4>(x, lo, min(lo + sp.split, V));
+    if (threadIdx.x == 0) {
+      stats[(static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit + s] = st;
+      __threadfence();
+      s_last = (atomicAdd(&tickets[b], 1u) == static_cast<unsigned>(sp.nsplit - 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {  // the slice holding u * Z (float exponentials, double sums)
+    float M = -INFINITY;
+    for (int q = 0; q < sp.nsplit; ++q) M = fmaxf(M, __ldcg(&st_b[q].x));
+    double Z = 0.0;
+    for (int q = 0; q < sp.nsplit; ++q) {
+      const float2 v = __ldcg(st_b + q);
+      Z += static_cast<double>(v.y * exp2f((v.x - M) * kLog2e));
+    }
+    const double tgt = static_cast<double>(u[(static_cast<size_t>(b) * (sp.gamma + 1) + row) * 3 + 0]) * Z;
+    double run = 0.0;
+    int pick = -1;
+    for (int q = 0; q < sp.nsplit; ++q) {
+      const float2 v = __ldcg(st_b + q);
+      const double ts = static_cast<double>(v.y * exp2f((v.x - M) * kLog2e));
+      if (ts > 0.0 && run + ts > tgt) {
+        pick = q;
+        break;
+      }
+      run += ts;
+    }
+    if (pick < 0) {  // rounding pushed u * Z past the total: the last slice with mass, its end
+      for (int q = sp.nsplit - 1; q >= 0 && pick < 0; --q)
+        if (__ldcg(&st_b[q].y) > 0.f) pick = q;
+      run = tgt + 1.0;
+    }
+    s_M = M;
+    s_slice = pick;
+    s_pre = tgt - run;  // target measured from the slice start (negative: take its last entry)
+    s_tidx = 0x7fffffff;
+    s_lastpos = -1;
+  }
+  __syncthreads();
+  const int pick_slice = s_slice;
+  int tok = -1;
+  if (pick_slice >= 0) {
+    const float M = s_M;
+    const int lo = pick_slice * sp.split, hi = min(lo + sp.split, V);
+    const int seg = ((hi - lo + kStatThreads - 1) / kStatThreads + 3) / 4 * 4;  // contiguous entries per thread
+    const int j0 = min(hi, lo + static_cast<int>(threadIdx.x) * seg), j1 = min(hi, j0 + seg);
+    // 16 entries per batch, all loads in flight (segments start on a multiple of 4)
+    auto load16 = [&](int jb, float (&v)[16]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int jj = jb + 4 * q;
+        if (VEC4 && jj + 3 < j1) {
+          const float4 f = __ldg(reinterpret_cast<const float4 *>(x + jj));
+          v[4 * q] = f.x;
+          v[4 * q + 1] = f.y;
+          v[4 * q + 2] = f.z;
+          v[4 * q + 3] = f.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[4 * q + e] = (jj + e < j1) ? __ldg(x + jj + e) : -INFINITY;
+        }
+      }
+    };
+    float tsum = 0.f;
+    int lastpos = -1;
+#pragma unroll 1
+    for (int jb = j0; jb < j1; jb += 16) {
+      float v[16];
+      load16(jb, v);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float w = exp2f((v[k] - M) * kLog2e);
+        tsum += w;
+        if (w > 0.f) lastpos = jb + k;
+      }
+    }
+    float incl = tsum;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.f;
+    if (lane == 31) s_wsum[warp] = incl;
+    if (lastpos >= 0) atomicMax(&s_lastpos, lastpos);
+    __syncthreads();
+    if (warp == 0) {  // per-warp float targets from a double scan of the warp totals
+      const double x0 = (lane < kW) ? static_cast<double>(s_wsum[lane]) : 0.0;
+      double ix = x0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, ix, o);
+        if (lane >= o) ix += y;
+      }
+      if (lane < kW) s_trel[lane] = fmaxf(0.f, static_cast<float>(s_pre - (ix - x0)));
+    }
+    __syncthreads();
+    const float trel = s_trel[warp];
+    if (tsum > 0.f && excl <= trel && incl > trel && s_pre >= 0.0) atomicMin(&s_tidx, static_cast<int>(threadIdx.x));
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) == s_tidx) {
+      float c = excl;
+      int p = -1;
+#pragma unroll 1
+      for (int jb = j0; jb < j1 && p < 0; jb += 16) {
+        float v[16];
+        load16(jb, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float w = exp2f((v[k] - M) * kLog2e);
+          c += w;
+          if (p < 0 && w > 0.f && c > trel) p = jb + k;
+        }
+      }
+      s_lastpos = (p >= 0) ? p : lastpos;  // the crossing is here; rounding: this segment's last positive weight
+    }
+    __syncthreads();
+    tok = s_lastpos;  // no claim: the target lies past the slice's scanned total (rounding): its last entry
+  }
+  if (threadIdx.x == 0) {
+    draft_tokens[static_cast<size_t>(b) * sp.gamma + row] = tok;
+    tickets[b] = 0u;  // left clean for the next call on this workspace (the call also clears it first)
   }
 }
 
@@ -459,13 +622,14 @@ SpecPlan plan_spec(int B, int gamma, int V) {
   p.split = 16384;
   p.nsplit = (V + p.split - 1) / p.split;
   p.nrows = 2 * gamma + 1;
-  p.off_stats = kAlign;
+  p.off_tickets = kAlign;
+  p.off_stats = align_up(p.off_tickets + sizeof(unsigned) * static_cast<size_t>(B));
   p.ws_bytes = align_up(p.off_stats + sizeof(float2) * static_cast<size_t>(B) * p.nrows * p.nsplit);
   return p;
 }
 
 cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
-  cudaError_t e = cudaMemsetAsync(a.ws, 0, kAlign, a.stream);
+  cudaError_t e = cudaMemsetAsync(a.ws, 0, p.off_stats, a.stream);  // header and tickets
   if (e != cudaSuccess) return e;
   StatParams sp;
   sp.B = p.B;
@@ -488,6 +652,16 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   WsHeader *hdr = static_cast<WsHeader *>(a.ws);
   const bool vec4 = (p.V % 4) == 0 && (reinterpret_cast<uintptr_t>(a.draft) % 16) == 0 &&
                     (a.target == nullptr || (reinterpret_cast<uintptr_t>(a.target) % 16) == 0);
+  if (a.mode == 1 && a.row >= 0) {  // one draft row: statistics and draw in one launch
+    unsigned *tickets = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(a.ws) + p.off_tickets);
+    const dim3 g(p.B, p.nsplit);
+    if (vec4)
+      spec_draw_row_kernel<true><<<g, kStatThreads, 0, a.stream>>>(a.draft, a.draft_tokens, a.u, sp, stats, tickets);
+    else
+      spec_draw_row_kernel<false><<<g, kStatThreads, 0, a.stream>>>(a.draft, a.draft_tokens, a.u, sp, stats,
+                                                                     tickets);
+    return cudaGetLastError();
+  }
   dim3 g1(p.B * sp.nr, p.nsplit);
   if (vec4)
     spec_stats_kernel<true><<<g1, kStatThreads, 0, a.stream>>>(a.target, a.draft, sp, stats);

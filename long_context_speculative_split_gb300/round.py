@@ -16,7 +16,7 @@ layer by layer, on synthetic per-layer queries:
 
 The per-layer SnapKV draft caches are selected once in ``prepare()`` (not
 part of the round).  ``capture()`` records the round in a CUDA graph so the
-(gamma+1)*L + 2*gamma + 2 kernel launches replay without host overhead.
+(gamma+1)*L + gamma + 2 kernel launches replay without host overhead.
 """
 import torch
 
@@ -76,7 +76,7 @@ class SpeculationRound:
     @property
     def launches(self):
         """Kernels of this library launched per round."""
-        return self.gamma * self.layers + 2 * self.gamma + self.layers + 2  # draws and sampling: 2 kernels each
+        return self.gamma * self.layers + self.gamma + self.layers + 2  # one-row draws: 1 kernel; sampling: 2
 
     def run(self):
         for s in range(self.gamma):
