@@ -189,11 +189,12 @@ class Workload:
         self.bytes_verify = float((2 * Hkv * L * D * esz).sum())
         Keff = torch.clamp(L, max=K)
         self.bytes_draft = float((2 * Hkv * Keff * D * esz).sum())
-        self.bytes_snap = float((2 * Hkv * L * D * esz).sum() + 4 * Hkv * Keff.sum() * D * esz)
+        # K read once (both scoring passes of a slice share one HBM read) + the gather (K and V rows read and written)
+        self.bytes_snap = float((Hkv * L * D * esz).sum() + 4 * Hkv * Keff.sum() * D * esz)
         self.bytes_spec = float(B * (2 * self.gamma + 1) * self.V * 4)
-        # SnapKV (2 scoring passes + select), gamma x (draft attention + one-row draw), verify,
+        # SnapKV (one-read scorer + select), gamma x (draft attention + one-row draw), verify,
         # rejection sample (statistics and finish)
-        self.launches_per_step = 3 + self.gamma * 1 + self.gamma * 1 + 1 + 2
+        self.launches_per_step = 2 + self.gamma * 1 + self.gamma * 1 + 1 + 2
 
     def step(self, ev=None):
         ops = self.ops

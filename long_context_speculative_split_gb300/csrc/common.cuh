@@ -23,8 +23,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Every spin-wait in this library gives up after this long, raises
-// MGD_DEVERR_TIMEOUT and lets the kernel return.  No wait depends on another
-// CTA, so a correct kernel never comes close.
+// MGD_DEVERR_TIMEOUT and lets the kernel return.  The only waits on other
+// CTAs are the SnapKV scorer's (for slices other running CTAs have already
+// claimed, microseconds apart), so a correct kernel never comes close.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ void raise_error(WsHeader *hdr, unsigned bit) {
@@ -37,6 +38,13 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction (the three-input form of PTX max.f32, sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // ---------------------------------------------------------------- shared memory
@@ -94,6 +102,27 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
       "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+// L2 eviction-priority policies for loads that carry a cache hint: evict_last
+// for data the CTA will read again soon, evict_first for a last read.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// tma_load_4d with an L2 cache-hint policy.
+__device__ __forceinline__ void tma_load_4d_hint(void *dst, const void *tmap, uint64_t *bar, int c0, int c1, int c2,
+                                                 int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
       : "memory");
 }
 // Order this thread's generic-proxy shared-memory writes before later

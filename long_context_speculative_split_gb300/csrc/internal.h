@@ -71,11 +71,18 @@ int encode_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Hkv, int
                          int64_t batch_stride, int64_t head_stride);
 
 // ------------------------------------------------------------------ SnapKV
+// Keys per job of the one-read tcgen05 scorer (12 tiles of 128 keys): small
+// enough that the slices open at once (one per resident CTA) mostly stay in L2
+// until their pass 2 re-reads them, large enough that the per-job exchange
+// stays a small share of the job (measured: 1280 / 1536 / 1792 / 2048 keys).
+constexpr int kSnapSliceKeys = 1536;
+
 struct SnapPlan {
   int B, Hq, Hkv, D, kv_cap, W, G, rows, RG;
-  int C;       // keys per scoring unit (multiple of 64)
+  int C;       // keys per scoring unit (multiple of 64; kSnapSliceKeys for the tcgen05 scorer)
   int nchunk;  // ceil(kv_cap / C)
   int pairs;   // B * Hkv
+  size_t off_cnt;  // unsigned [pairs]: slices published per pair (zeroed with the header on every call)
   size_t off_part, off_scores, off_pooled, ws_bytes;
 };
 SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W);

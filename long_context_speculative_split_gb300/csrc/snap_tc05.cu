@@ -1,7 +1,8 @@
-// SnapKV window scores on the 5th-generation tensor cores (tcgen05 + TMEM).
+// SnapKV window scores on the 5th-generation tensor cores (tcgen05 + TMEM),
+// both passes in one persistent kernel that streams K from HBM once.
 //
 // MagicDec notes, section 4.4 (SnapKV as the static selector) and appendix A.1
-// (selection at prefill).  Steps 1 of the selection (see snapkv.cu): the W
+// (selection at prefill).  Step 1 of the selection (see snapkv.cu): the W
 // window queries of a KV head (W * G = 128 rows) attend causally over the
 // context; pass 1 gets each row's log-sum-exp, pass 2 sums each prefix key's
 // probabilities over the 128 rows.  Both passes are dense contractions
@@ -12,27 +13,58 @@
 //   pass 2: S^T = K Qw^T  (TMEM lane = key, column = window row): every thread
 //           owns one key and sums exp2(s - lse_row) over the rows in registers.
 //
-// CTA = 10 warps: warp 0 issues TMA (the 128 window rows once, then 128-key K
-// tiles into a 2-stage ring), warp 1 owns the TMEM allocation and one thread
-// issues the MMAs (8 k-steps of K = 16 per tile) into a double-buffered
-// 2 x 128-column fp32 accumulator, warps 2..9 drain it (tcgen05.ld) as two
-// groups of 4 warps taking alternate tiles, one warp per TMEM lane quadrant.
-// Operands are K-major bf16 with 128-byte swizzling, exactly the layout TMA
-// writes.  Used when W * G == 128 and D == 128 (the Llama-3.1-8B shape with a
-// 32-row window); other shapes use the mma.sync kernel in snapkv.cu.
+// One read of K.  The work is cut into jobs = (sequence, KV head, slice of
+// kSnapSliceKeys keys).  A CTA runs pass 1 over its slice, publishes the
+// slice's per-row (max, sum) and counts it in a per-(sequence, head) counter,
+// waits until every slice of that (sequence, head) has done the same (they
+// were claimed at nearly the same moment by other CTAs, since jobs are handed
+// out in order from one atomic counter), merges the partials into the rows'
+// log-sum-exp, and then runs pass 2 over the same slice.  Between the two
+// reads of a tile the whole GPU fetches only about one slice per CTA from
+// HBM, so most second reads come from L2 instead of HBM.
+//
+// Progress: a CTA waits only for slices that other CTAs have already claimed
+// (its producer claims the next job only after the current job's exchange is
+// complete), and every claimed slice reaches its publish step without waiting
+// on anything; a CTA that is not resident has claimed nothing.  So the waits
+// end as long as more CTAs are resident than a pair has slices (22 at 32k
+// keys, 43 at 64k; the grid is two per SM).  Every wait is bounded
+// (kWaitLimitNs) and raises MGD_DEVERR_TIMEOUT instead of hanging.
+//
+// L2: pass-1 tile loads carry an evict_last hint and pass-2 loads (the last
+// read) evict_first, so the slices between their two reads (one per CTA)
+// keep their place against the rest of the stream.
+//
+// CTA = 10 warps, 2 CTAs per SM: warp 0 claims jobs and issues TMA (the 128
+// window rows of the job, then its 128-key K tiles -- pass 1's, then the same
+// tiles again for pass 2 -- into a 2-stage ring), warp 1 owns the TMEM
+// allocation and one thread issues the MMAs (8 k-steps of K = 16 per tile)
+// into a double-buffered 2 x 128-column fp32 accumulator, warps 2..9 drain it
+// (tcgen05.ld) as two groups of 4 warps taking alternate tiles, one warp per
+// TMEM lane quadrant, and do the exchange.  Operands are K-major bf16 with
+// 128-byte swizzling, exactly the layout TMA writes.  Used when W * G == 128
+// and D == 128 (the Llama-3.1-8B shape with a 32-row window); other shapes use
+// the kernels in snapkv.cu.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace mgd {
 namespace {
 
 constexpr int kT5Keys = 128;
-constexpr int kT5Stages = 2;
-constexpr int kT5Threads = 320;
-constexpr int kT5SoftWarps = 8;
+constexpr int kT5Groups = 2;                // softmax groups of 4 warps, one TMEM accumulator each
+constexpr int kT5Stages = 2;                // K tiles in flight
+constexpr int kT5CtasPerSm = 2;
+constexpr int kT5SoftWarps = 4 * kT5Groups;
+constexpr int kT5Threads = 64 + 32 * kT5SoftWarps;
 constexpr int kT5Half = 128 * 128;          // one 64-column (128 B) atom column of 128 rows
 constexpr int kT5TileBytes = 2 * kT5Half;   // 128 rows x 128 bf16
-constexpr uint32_t kT5TmemCols = 256;       // two 128-column accumulators
+constexpr uint32_t kT5TmemCols = 128 * kT5Groups;  // one 128-column accumulator per group
+static_assert(kT5Groups == 2 || kT5Groups == 4, "tcgen05.alloc takes a power-of-two column count");
+constexpr int kExchThread = 64;             // first softmax thread: job broadcast and exchange
 constexpr float kLog2e = 1.4426950408889634f;
+static_assert(kSnapSliceKeys % kT5Keys == 0, "slices are whole tiles");
 
 // Instruction descriptor of tcgen05.mma kind::f16: D f32, A and B bf16, both
 // K-major, M = 128, N = 128.
@@ -41,18 +73,19 @@ constexpr uint32_t kIdescM128N128 = (1u << 4) | (1u << 7) | (1u << 10) | ((128u 
 struct T5Layout {
   static constexpr int off_q = 0;                                   // 32 KB window rows
   static constexpr int off_k = kT5TileBytes;                        // kT5Stages x 32 KB
-  static constexpr int off_bar = off_k + kT5Stages * kT5TileBytes;  // 16 mbarriers
-  static constexpr int off_tmem = off_bar + 16 * 8;
-  static constexpr int off_lse = off_tmem + 16;                     // float [128]
-  static constexpr int off_red = off_lse + 128 * 4;                 // float [2][128]
-  static constexpr int bytes = off_red + 2 * 128 * 4;
+  static constexpr int off_bar = off_k + kT5Stages * kT5TileBytes;  // 24 mbarriers
+  static constexpr int off_tmem = off_bar + 24 * 8;
+  static constexpr int off_job = off_tmem + 16;                     // int [2] ring, [2] broadcast, abort
+  static constexpr int off_lse = off_job + 32;                      // float [128]
+  static constexpr int off_red = off_lse + 128 * 4;                 // float [groups][2][128]
+  static constexpr int bytes = off_red + kT5Groups * 2 * 128 * 4;
   static constexpr int alloc = bytes + 1024;
 };
 
 struct T5Params {
-  int W, G, Hq, Hkv, C, nchunk, kv_cap;
+  int W, G, Hkv, nslice, kv_cap, units;
   float sl2;
-  size_t off_part, off_scores;
+  size_t off_cnt, off_part, off_scores;
 };
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
@@ -98,51 +131,168 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int PASS>
-__global__ void __launch_bounds__(kT5Threads, 2)
-    snap_score_tc05(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                    const int32_t *__restrict__ kv_len, unsigned char *__restrict__ ws, T5Params p) {
+// One job: slice `slice` (kSnapSliceKeys keys from `start`) of (sequence b,
+// KV head hkv).  nt1 / nt2 = 128-key tiles of pass 1 (keys < L) and pass 2
+// (prefix keys < L - W); ns = slices of the pair that hold pass-1 keys.
+struct SliceJob {
+  int b, hkv, pair, slice, L, start, end2, nt1, nt2, ns;
+  bool valid;
+};
+__device__ __forceinline__ SliceJob slice_job(int u, const int32_t *__restrict__ kv_len, const T5Params &p) {
+  SliceJob j;
+  j.pair = u / p.nslice;
+  j.slice = u - j.pair * p.nslice;
+  j.b = j.pair / p.Hkv;
+  j.hkv = j.pair - j.b * p.Hkv;
+  j.L = kv_len[j.b];
+  j.valid = j.L >= p.W && j.L <= p.kv_cap;
+  j.start = j.slice * kSnapSliceKeys;
+  const int end1 = min(j.start + kSnapSliceKeys, j.L);
+  j.end2 = min(j.start + kSnapSliceKeys, j.L - p.W);
+  j.nt1 = (j.valid && end1 > j.start) ? (end1 - j.start + kT5Keys - 1) / kT5Keys : 0;
+  j.nt2 = (j.valid && j.end2 > j.start) ? (j.end2 - j.start + kT5Keys - 1) / kT5Keys : 0;
+  j.ns = j.valid ? (j.L + kSnapSliceKeys - 1) / kSnapSliceKeys : 0;
+  return j;
+}
+
+// Pass 1 on one accumulator tile: window row tl against keys kt0 .. kt0+127
+// (keys after `pos`, the row's last visible key, masked when the tile reaches
+// the window at `wstart`), folded into the row's running (max, sum) in the
+// exp2 domain.  Hands the accumulator back once both halves are in registers.
+__device__ __forceinline__ void pass1_tile(uint32_t lane_addr, int kt0, int wstart, int pos, float sl2,
+                                           uint64_t *acc_empty, int lane, float &m_run, float &l_run) {
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    float v[2][32];
+    tmem_ld32(lane_addr + h * 64, v[0]);
+    tmem_ld32(lane_addr + h * 64 + 32, v[1]);
+    if (h == 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+    if (kt0 + kT5Keys - 1 > wstart) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (kt0 + 64 * h + 32 * i + c > pos) v[i][c] = -INFINITY;
+    }
+    // the 64 values as 32 pairs: four 3-input max chains, then paired (f32x2)
+    // scale-and-shift and sums, two exponentials per pair
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mx[j & 3] = fmax3(mx[j & 3], v[j >> 4][(j & 15) * 2], v[j >> 4][(j & 15) * 2 + 1]);
+    const float mn = fmaxf(m_run, fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * sl2);  // sl2 > 0
+    const float mu = (mn == -INFINITY) ? 0.f : mn;
+    const float2 s2 = make_float2(sl2, sl2), nm = make_float2(-mu, -mu);
+    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float2 x = __ffma2_rn(make_float2(v[j >> 4][(j & 15) * 2], v[j >> 4][(j & 15) * 2 + 1]), s2, nm);
+      acc[j & 1] = __fadd2_rn(acc[j & 1], make_float2(ex2(x.x), ex2(x.y)));
+    }
+    l_run = l_run * ex2(m_run - mu) + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
+    m_run = mn;
+  }
+}
+
+// Pass 2 on one accumulator tile: key tl against the 128 window rows; returns
+// sum over rows of exp2(s * sl2 - lse_row), with -lse in shared memory.
+__device__ __forceinline__ float pass2_tile(uint32_t lane_addr, const float *sm_nlse, float sl2, uint64_t *acc_empty,
+                                            int lane) {
+  float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  const float2 s2 = make_float2(sl2, sl2);
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    float v[2][32];
+    tmem_ld32(lane_addr + h * 64, v[0]);
+    tmem_ld32(lane_addr + h * 64 + 32, v[1]);
+    if (h == 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const float4 nl = *reinterpret_cast<const float4 *>(&sm_nlse[64 * h + 32 * i + c]);
+        const float2 x0 = __ffma2_rn(make_float2(v[i][c], v[i][c + 1]), s2, make_float2(nl.x, nl.y));
+        const float2 x1 = __ffma2_rn(make_float2(v[i][c + 2], v[i][c + 3]), s2, make_float2(nl.z, nl.w));
+        acc[0] = __fadd2_rn(acc[0], make_float2(ex2(x0.x), ex2(x0.y)));
+        acc[1] = __fadd2_rn(acc[1], make_float2(ex2(x1.x), ex2(x1.y)));
+      }
+  }
+  return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+}
+
+// A bounded wait that also gives up at once after any other wait of the CTA
+// gave up; a failure raises the timeout bit and sets the CTA's abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, WsHeader *hdr,
+                                              volatile int *abort_flag) {
+  if (*abort_flag) return false;
+  if (mbar_wait(bar, parity)) return true;
+  raise_error(hdr, 0x8u);
+  *abort_flag = 1;
+  return false;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
+    snap_score_fused(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                     const int32_t *__restrict__ kv_len, unsigned char *__restrict__ ws, T5Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T5Layout::off_bar);
-  uint64_t *q_full = bars + 0;
-  uint64_t *full = bars + 1;          // [kT5Stages]
-  uint64_t *empty = bars + 3;         // [kT5Stages]
-  uint64_t *acc_full = bars + 5;      // [2]
-  uint64_t *acc_empty = bars + 7;     // [2]
+  uint64_t *q_full = bars + 0;      // window rows of the job landed
+  uint64_t *q_empty = bars + 1;     // every MMA of the previous job done: the rows may be replaced
+  uint64_t *full = bars + 2;                    // [kT5Stages] K tile landed
+  uint64_t *empty = full + kT5Stages;           // [kT5Stages] K tile consumed by its MMAs
+  uint64_t *acc_full = empty + kT5Stages;       // [kT5Groups] accumulator written
+  uint64_t *acc_empty = acc_full + kT5Groups;   // [kT5Groups] accumulator drained by its group
+  uint64_t *job_full = acc_empty + kT5Groups;   // [2] job ring slot written
+  uint64_t *job_empty = job_full + 2;           // [2] job ring slot read by the MMA thread and the softmax warps
+  uint64_t *xchg = job_empty + 2;               // this job's exchange is complete (the producer may claim the next one)
+  uint64_t *mma_done = xchg + 1;                // final: every MMA issued has completed
+  static_assert(2 + 2 * kT5Stages + 2 * kT5Groups + 6 <= 24, "mbarrier slots");
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + T5Layout::off_tmem);
-  float *sm_lse = reinterpret_cast<float *>(smem + T5Layout::off_lse);
+  // [0..1] job ring (producer -> MMA thread and exchange thread), [2..3] the
+  // exchange thread's broadcast to the softmax warps, double-buffered so that
+  // a slot is rewritten only after every thread passed the next job's barrier
+  volatile int *sm_job = reinterpret_cast<volatile int *>(smem + T5Layout::off_job);
+  volatile int *abort_flag = sm_job + 4;
+  float *sm_nlse = reinterpret_cast<float *>(smem + T5Layout::off_lse);  // minus each row's log2-sum-exp
   float *sm_red = reinterpret_cast<float *>(smem + T5Layout::off_red);
   WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
-  float2 *part = reinterpret_cast<float2 *>(ws + p.off_part);
+  unsigned *cnt = reinterpret_cast<unsigned *>(ws + p.off_cnt);  // [pairs] slices published
+  float2 *part = reinterpret_cast<float2 *>(ws + p.off_part);    // [pairs][nslice][128] (max, sum)
   float *scores = reinterpret_cast<float *>(ws + p.off_scores);
-
-  const int chunk = blockIdx.x % p.nchunk;
-  const int pair = blockIdx.x / p.nchunk;
-  const int hkv = pair % p.Hkv;
-  const int b = pair / p.Hkv;
-  const int L = kv_len[b];
-  if (L < p.W || L > p.kv_cap) {
-    if (threadIdx.x == 0 && chunk == 0 && hkv == 0) raise_error(hdr, 0x2u);
-    return;
-  }
-  const int kend = (PASS == 1) ? L : L - p.W;
-  const int start = chunk * p.C;
-  if (start >= kend) return;
-  const int end = min(start + p.C, kend);
-  const int ntiles = (end - start + kT5Keys - 1) / kT5Keys;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kT5Stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kT5Groups; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], kT5SoftWarps / 2);  // the 4 warps of the group draining buffer a
+      mbar_init(&acc_empty[a], 4);  // the 4 warps of the group draining buffer a
     }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&job_full[a], 1);
+      mbar_init(&job_empty[a], 2);  // the MMA thread and the exchange thread
+    }
+    mbar_init(xchg, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {  // the whole warp allocates the accumulator columns
@@ -151,171 +301,227 @@ __global__ void __launch_bounds__(kT5Threads, 2)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (PASS == 2 && threadIdx.x >= 64 && threadIdx.x < 64 + 128) {
-    // log2-sum-exp of each window row from the pass-1 partials of all chunks
-    const int r = threadIdx.x - 64;
-    const int nch1 = (L + p.C - 1) / p.C;
-    const float2 *pp = part + static_cast<size_t>(pair) * p.nchunk * 128 + r;
-    float M = -INFINITY;
-    for (int c = 0; c < nch1; ++c) M = fmaxf(M, pp[c * 128].x);
-    float S = 0.f;
-    for (int c = 0; c < nch1; ++c) {
-      const float2 x = pp[c * 128];
-      if (x.y > 0.f) S += x.y * exp2f(x.x - M);
-    }
-    sm_lse[r] = M + log2f(S);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  bool ok = true;
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ jobs + TMA
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
-      mbar_arrive_expect_tx(q_full, kT5TileBytes);
-      for (int h = 0; h < 2; ++h)
-        tma_load_4d(smem + T5Layout::off_q + h * kT5Half, &qmap, q_full, 64 * h, hkv * p.G, 0, b);
-      int stage = 0;
+      tma_prefetch_desc(&qmap);
+      // pass-1 tiles stay in L2 for their second read; pass-2 reads are the last
+      const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+      int stage = 0, qn = 0;
       uint32_t phase = 0;
-      for (int t = 0; t < ntiles && ok; ++t) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u)) {
-          raise_error(hdr, 0x8u);
-          ok = false;
-          break;
+      int issued = 0;  // K tiles issued; tile i went to stage i % kT5Stages in phase i / kT5Stages
+      for (int j = 0;; ++j) {
+        const int js = j & 1;
+        // the slot is free and the previous job's exchange is complete
+        if (!wait_or_abort(&job_empty[js], ((j >> 1) & 1u) ^ 1u, hdr, abort_flag) || (j > 0 && !wait_or_abort(xchg, (j - 1) & 1u, hdr, abort_flag))) break;
+        int u = static_cast<int>(atomicAdd(&hdr->next_unit, 1u));
+        if (u >= p.units) u = -1;
+        sm_job[js] = u;
+        mbar_arrive(&job_full[js]);
+        if (u < 0) break;
+        const SliceJob jb = slice_job(u, kv_len, p);
+        if (!jb.valid && jb.slice == 0 && jb.hkv == 0) raise_error(hdr, 0x2u);
+        if (jb.nt1 == 0) continue;
+        // The job's window rows replace the previous job's once all of that
+        // job's MMAs are done; its first K tiles go out before that wait, so
+        // their HBM latency overlaps the previous job's last tiles.
+        const int nt = jb.nt1 + jb.nt2;
+        bool ok = true;
+        for (int i = 0; i <= nt; ++i) {
+          if (i == min(nt, kT5Stages)) {  // the window rows, after the first tiles
+            if (!wait_or_abort(q_empty, (qn & 1u) ^ 1u, hdr, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(q_full, kT5TileBytes);
+            for (int h = 0; h < 2; ++h)
+              tma_load_4d(smem + T5Layout::off_q + h * kT5Half, &qmap, q_full, 64 * h, jb.hkv * p.G, 0, jb.b);
+            ++qn;
+          }
+          if (i == nt) break;
+          const int key0 = jb.start + (i < jb.nt1 ? i : i - jb.nt1) * kT5Keys;
+          if (!wait_or_abort(&empty[stage], phase ^ 1u, hdr, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kT5TileBytes);
+          unsigned char *st = smem + T5Layout::off_k + stage * kT5TileBytes;
+          for (int h = 0; h < 2; ++h)
+            for (int kh = 0; kh < 2; ++kh)
+              tma_load_4d_hint(st + h * kT5Half + kh * 8192, &kmap, &full[stage], 64 * h, key0 + 64 * kh, jb.hkv,
+                               jb.b, i < jb.nt1 ? keep : drop);
+          ++issued;
+          if (++stage == kT5Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        mbar_arrive_expect_tx(&full[stage], kT5TileBytes);
-        unsigned char *st = smem + T5Layout::off_k + stage * kT5TileBytes;
-        for (int h = 0; h < 2; ++h)
-          for (int kh = 0; kh < 2; ++kh)
-            tma_load_4d(st + h * kT5Half + kh * 8192, &kmap, &full[stage], 64 * h, start + t * kT5Keys + 64 * kh, hkv,
-                        b);
-        if (++stage == kT5Stages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (!ok) break;
       }
+      // every copy this thread issued has landed before the CTA moves on
+      for (int s = 0; s < kT5Stages && s < issued; ++s) {
+        const int last = s + kT5Stages * ((issued - 1 - s) / kT5Stages);  // the stage's last tile
+        mbar_wait(&full[s], static_cast<uint32_t>(last / kT5Stages) & 1u);
+      }
+      if (qn > 0) mbar_wait(q_full, static_cast<uint32_t>(qn - 1) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      if (!mbar_wait(q_full, 0)) {
-        raise_error(hdr, 0x8u);
-        ok = false;
-      }
       const uint32_t q_base = smem_addr(smem + T5Layout::off_q);
-      int stage = 0;
+      int stage = 0, qn = 0, t = 0;
       uint32_t phase = 0;
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const int a = t & 1;
-        const uint32_t aph = (t >> 1) & 1u;
-        if (!mbar_wait(&full[stage], phase) || !mbar_wait(&acc_empty[a], aph ^ 1u)) {
-          raise_error(hdr, 0x8u);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t k_base = smem_addr(smem + T5Layout::off_k + stage * kT5TileBytes);
-        const uint32_t a_base = (PASS == 1) ? q_base : k_base;
-        const uint32_t b_base = (PASS == 1) ? k_base : q_base;
+      for (int j = 0;; ++j) {
+        const int js = j & 1;
+        if (!wait_or_abort(&job_full[js], (j >> 1) & 1u, hdr, abort_flag)) break;
+        const int u = sm_job[js];
+        mbar_arrive(&job_empty[js]);
+        if (u < 0) break;
+        const SliceJob jb = slice_job(u, kv_len, p);
+        if (jb.nt1 == 0) continue;
+        if (!wait_or_abort(q_full, qn & 1u, hdr, abort_flag)) break;
+        ++qn;
+        bool ok = true;
+        for (int i = 0; i < jb.nt1 + jb.nt2; ++i, ++t) {
+          const int a = t % kT5Groups;
+          if (!wait_or_abort(&full[stage], phase, hdr, abort_flag) || !wait_or_abort(&acc_empty[a], ((t / kT5Groups) & 1u) ^ 1u, hdr, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_base = smem_addr(smem + T5Layout::off_k + stage * kT5TileBytes);
+          const bool p1 = i < jb.nt1;
+          const uint32_t a_base = p1 ? q_base : k_base;
+          const uint32_t b_base = p1 ? k_base : q_base;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kT5Half + (kk & 3) * 32;
-          umma_f16(tmem + a * 128, umma_desc(a_base + off), umma_desc(b_base + off), kIdescM128N128, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kT5Half + (kk & 3) * 32;
+            umma_f16(tmem + a * 128, umma_desc(a_base + off), umma_desc(b_base + off), kIdescM128N128,
+                     kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          umma_commit(&acc_full[a]);
+          if (++stage == kT5Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        umma_commit(&empty[stage]);
-        umma_commit(&acc_full[a]);
-        if (++stage == kT5Stages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (!ok) break;
+        umma_commit(q_empty);
       }
+      umma_commit(mma_done);  // arrives once every MMA issued above has completed
+      mbar_wait(mma_done, 0);
     }
   } else {
     // ------------------------------------------------------------------ softmax warps
-    // Two groups of 4 warps take alternate tiles (group g drains accumulator
-    // buffer g); warp w of a group reads TMEM lane quadrant w % 4, all 128
-    // columns of its lane, in two halves of 64.
+    // kT5Groups groups of 4 warps take the CTA's tiles round robin (group g
+    // drains accumulator buffer g); warp w of a group reads TMEM lane quadrant
+    // w % 4, all 128 columns of its lane, in two halves of 64.  All softmax
+    // threads take the same path through the job loop, so the named barriers
+    // below always see every one of them.
     const int qd = warp & 3;
     const int grp = (warp - 2) >> 2;
     const int tl = qd * 32 + lane;  // this thread's TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(qd * 32) << 16) + grp * 128;
-    float m_run = -INFINITY, l_run = 0.f;                     // pass 1, exp2 domain
-    const int pos = (PASS == 1) ? (L - p.W + tl / p.G) : 0;  // last key visible to window row tl
-    for (int t = grp; t < ntiles; t += 2) {
-      if (!mbar_wait(&acc_full[grp], (t >> 1) & 1u)) {
-        raise_error(hdr, 0x8u);
-        break;
-      }
-      tc_fence_after();
-      const int kt0 = start + t * kT5Keys;
-      float acc2 = 0.f;  // pass 2: this key's probability sum
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        float v[2][32];
-        tmem_ld32(lane_addr + h * 64, v[0]);
-        tmem_ld32(lane_addr + h * 64 + 32, v[1]);
-        if (h == 1) {  // both halves are in registers: hand the buffer back to the MMA thread
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[grp]);
-        }
-        if (PASS == 1) {
-          // row tl, keys kt0 + 64h + c; the window rows see every key before L - W
-          if (kt0 + kT5Keys - 1 > L - p.W) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-              for (int c = 0; c < 32; ++c)
-                if (kt0 + 64 * h + 32 * i + c > pos) v[i][c] = -INFINITY;
-          }
-          float mx = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, v[i][c]);
-          const float mn = fmaxf(m_run, mx * p.sl2);  // sl2 > 0: the max commutes with the scale
-          const float mu = (mn == -INFINITY) ? 0.f : mn;
-          float acc = 0.f;
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int c = 0; c < 32; ++c) acc += ex2(fmaf(v[i][c], p.sl2, -mu));
-          l_run = l_run * ex2(m_run - mu) + acc;
-          m_run = mn;
-        } else {
-          // key kt0 + tl, window rows 64h + c
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              const float4 lr = *reinterpret_cast<const float4 *>(&sm_lse[64 * h + 32 * i + c]);
-              acc2 += ex2(fmaf(v[i][c], p.sl2, -lr.x)) + ex2(fmaf(v[i][c + 1], p.sl2, -lr.y)) +
-                      ex2(fmaf(v[i][c + 2], p.sl2, -lr.z)) + ex2(fmaf(v[i][c + 3], p.sl2, -lr.w));
-            }
-        }
-      }
-      if (PASS == 2) {
-        const int key = kt0 + tl;
-        if (key < end) scores[(static_cast<size_t>(b) * p.Hkv + hkv) * p.kv_cap + key] = acc2;
-      }
-    }
-    if (PASS == 1) {
-      // combine the two groups' (max, sum) of each row, then write this chunk's partial
-      if (grp == 1) {
-        sm_red[tl] = m_run;
-        sm_red[128 + tl] = l_run;
+    const bool exch = threadIdx.x == kExchThread;
+    int t = 0;  // index of the job's first tile in the CTA's tile sequence
+    for (int j = 0;; ++j) {
+      const int js = j & 1;
+      if (exch) {
+        const bool got = wait_or_abort(&job_full[js], (j >> 1) & 1u, hdr, abort_flag);
+        sm_job[2 + js] = got ? sm_job[js] : -1;
+        mbar_arrive(&job_empty[js]);
       }
       named_bar(1, kT5SoftWarps * 32);
-      if (grp == 0) {
-        const float m2 = sm_red[tl], l2 = sm_red[128 + tl];
-        const float mn = fmaxf(m_run, m2);
-        const float mu = (mn == -INFINITY) ? 0.f : mn;
-        const float l = l_run * exp2f(m_run - mu) + l2 * exp2f(m2 - mu);
-        part[(static_cast<size_t>(pair) * p.nchunk + chunk) * 128 + tl] = make_float2(mn, l);
+      const int u = sm_job[2 + js];
+      if (u < 0) break;
+      const SliceJob jb = slice_job(u, kv_len, p);
+      // ---- pass 1 over the slice
+      float m_run = -INFINITY, l_run = 0.f;
+      const int pos = jb.L - p.W + tl / p.G;  // last key visible to window row tl
+      for (int i = (grp - t % kT5Groups + kT5Groups) % kT5Groups; i < jb.nt1; i += kT5Groups) {
+        // the accumulator reads are warp-collective: a warp skips a tile only as a whole
+        if (!__all_sync(0xffffffffu, wait_or_abort(&acc_full[grp], ((t + i) / kT5Groups) & 1u, hdr, abort_flag)))
+          continue;
+        tc_fence_after();
+        pass1_tile(lane_addr, jb.start + i * kT5Keys, jb.L - p.W, pos, p.sl2, &acc_empty[grp], lane, m_run, l_run);
       }
+      if (jb.nt1 > 0) {
+        // combine the groups' (max, sum) of each row into the slice's partial and publish it
+        if (grp > 0) {
+          sm_red[grp * 256 + tl] = m_run;
+          sm_red[grp * 256 + 128 + tl] = l_run;
+        }
+        named_bar(1, kT5SoftWarps * 32);
+        if (grp == 0) {
+          float mn = m_run;
+#pragma unroll
+          for (int g = 1; g < kT5Groups; ++g) mn = fmaxf(mn, sm_red[g * 256 + tl]);
+          const float mu = (mn == -INFINITY) ? 0.f : mn;
+          float l = l_run * exp2f(m_run - mu);
+#pragma unroll
+          for (int g = 1; g < kT5Groups; ++g) l += sm_red[g * 256 + 128 + tl] * exp2f(sm_red[g * 256 + tl] - mu);
+          part[(static_cast<size_t>(jb.pair) * p.nslice + jb.slice) * 128 + tl] = make_float2(mn, l);
+          __threadfence();
+        }
+        named_bar(1, kT5SoftWarps * 32);
+        if (exch) atomicAdd(&cnt[jb.pair], 1u);
+      }
+      if (jb.nt2 > 0) {
+        // wait for every slice of the pair, then merge their partials into -lse
+        if (exch && !*abort_flag) {
+          const unsigned need = static_cast<unsigned>(jb.ns);
+          if (ld_acquire_gpu(&cnt[jb.pair]) < need) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(&cnt[jb.pair]) < need) {
+              __nanosleep(64);  // up to a pair's worth of CTAs poll this counter
+              if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                raise_error(hdr, 0x8u);
+                *abort_flag = 1;
+                break;
+              }
+            }
+          }
+        }
+        named_bar(1, kT5SoftWarps * 32);
+        if (grp == 0) {  // merge the partials of every slice of row tl
+          const float2 *pp = part + static_cast<size_t>(jb.pair) * p.nslice * 128 + tl;
+          float M = -INFINITY, S = 0.f;
+          for (int s0 = 0; s0 < jb.ns; s0 += 8) {
+            float2 x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = (s0 + k < jb.ns) ? __ldcg(pp + (s0 + k) * 128) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (!(x[k].y > 0.f)) continue;
+              const float mn = fmaxf(M, x[k].x);
+              S = S * exp2f(M - mn) + x[k].y * exp2f(x[k].x - mn);
+              M = mn;
+            }
+          }
+          sm_nlse[tl] = -(M + log2f(S));
+        }
+        named_bar(1, kT5SoftWarps * 32);
+      }
+      if (exch) mbar_arrive(xchg);
+      // ---- pass 2 over the same slice (its tiles now come from L2)
+      const int t2 = t + jb.nt1;
+      float *srow = scores + static_cast<size_t>(jb.pair) * p.kv_cap;
+      for (int i = (grp - t2 % kT5Groups + kT5Groups) % kT5Groups; i < jb.nt2; i += kT5Groups) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(&acc_full[grp], ((t2 + i) / kT5Groups) & 1u, hdr, abort_flag)))
+          continue;
+        tc_fence_after();
+        const float sc = pass2_tile(lane_addr, sm_nlse, p.sl2, &acc_empty[grp], lane);
+        const int key = jb.start + i * kT5Keys + tl;
+        if (key < jb.end2) srow[key] = sc;
+      }
+      t = t2 + jb.nt2;
     }
   }
   tc_fence_before();
@@ -328,40 +534,31 @@ __global__ void __launch_bounds__(kT5Threads, 2)
 
 }  // namespace
 
-bool snap_tc05_eligible(const SnapPlan &p) { return p.D == 128 && p.rows == 128 && p.RG == 1 && p.C % 128 == 0; }
+bool snap_tc05_eligible(const SnapPlan &p) { return p.D == 128 && p.rows == 128 && p.RG == 1 && p.C == kSnapSliceKeys; }
 
 cudaError_t launch_snap_score_tc05(const SnapPlan &pl, const SnapArgs &a, const CUtensorMap &kmap,
                                    const CUtensorMap &qmap) {
   T5Params kp;
   kp.W = pl.W;
   kp.G = pl.G;
-  kp.Hq = pl.Hq;
   kp.Hkv = pl.Hkv;
-  kp.C = pl.C;
-  kp.nchunk = pl.nchunk;
+  kp.nslice = pl.nchunk;
   kp.kv_cap = pl.kv_cap;
+  kp.units = pl.pairs * pl.nchunk;
   kp.sl2 = a.sm_scale * kLog2e;
+  kp.off_cnt = pl.off_cnt;
   kp.off_part = pl.off_part;
   kp.off_scores = pl.off_scores;
-  const int units = pl.pairs * pl.nchunk;
-  unsigned char *ws = static_cast<unsigned char *>(a.ws);
-  cudaError_t e;
-#define MGD_T5(PP)                                                                                            \
-  do {                                                                                                        \
-    auto kern = snap_score_tc05<PP>;                                                                          \
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T5Layout::alloc);             \
-    if (e != cudaSuccess) return e;                                                                           \
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,                            \
-                             cudaSharedmemCarveoutMaxShared);                                                 \
-    if (e != cudaSuccess) return e;                                                                           \
-    kern<<<units, kT5Threads, T5Layout::alloc, a.stream>>>(kmap, qmap, a.kv_len, ws, kp);                     \
-    e = cudaGetLastError();                                                                                   \
-    if (e != cudaSuccess) return e;                                                                           \
-  } while (0)
-  MGD_T5(1);
-  MGD_T5(2);
-#undef MGD_T5
-  return cudaSuccess;
+  auto kern = snap_score_fused;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T5Layout::alloc);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  // persistent grid: two CTAs per SM (what the kernel's registers and shared
+  // memory allow); a CTA that only starts after others finished finds no job
+  const int grid = std::min(kp.units, kT5CtasPerSm * current_sm_count());
+  kern<<<grid, kT5Threads, T5Layout::alloc, a.stream>>>(kmap, qmap, a.kv_len, static_cast<unsigned char *>(a.ws), kp);
+  return cudaGetLastError();
 }
 
 }  // namespace mgd

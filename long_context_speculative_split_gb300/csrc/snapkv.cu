@@ -819,9 +819,11 @@ SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W) {
   const int cmin = std::max(256, ((kv_cap + 63) / 64 + 63) / 64 * 64);
   while (C > cmin && static_cast<long long>(p.pairs) * p.RG * ((kv_cap + C - 1) / C) < 8LL * slots) C /= 2;
   if (C < cmin) C = cmin;
+  if (D == 128 && p.rows == 128 && p.RG == 1) C = kSnapSliceKeys;  // the one-read tcgen05 scorer's slices
   p.C = C;
   p.nchunk = (kv_cap + C - 1) / C;
-  size_t off = kAlign;
+  p.off_cnt = kAlign;
+  size_t off = align_up(p.off_cnt + sizeof(unsigned) * static_cast<size_t>(p.pairs));
   p.off_part = off;
   off = align_up(off + sizeof(float2) * static_cast<size_t>(p.pairs) * p.RG * p.nchunk * kRowsPerCta);
   p.off_scores = off;
@@ -834,7 +836,7 @@ SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W) {
 
 cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, const CUtensorMap *kmap,
                           const CUtensorMap *qmap) {
-  cudaError_t e = cudaMemsetAsync(a.ws, 0, kAlign, a.stream);
+  cudaError_t e = cudaMemsetAsync(a.ws, 0, p.off_part, a.stream);  // header and per-pair counters
   if (e != cudaSuccess) return e;
   unsigned char *ws = static_cast<unsigned char *>(a.ws);
   SnapK kp;

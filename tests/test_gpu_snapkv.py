@@ -59,6 +59,9 @@ CASES = [
     (2, 64, 8, 128, [1000, 999], 1000, 32, 7, 256),  # 256 window rows -> two row groups
     (3, 32, 8, 128, [5000, 4000, 2500], 5000, 32, 7, 512),
     (1, 32, 8, 128, [777], 800, 8, 1, 100),          # no pooling, short window
+    # lengths at tile (128) and scoring-slice (1536) edges: a slice holding only window keys,
+    # a window that straddles a slice edge, a prefix of one key
+    (4, 32, 8, 128, [1537, 1568, 3112, 33], 3200, 32, 7, 256),
 ]
 
 
