@@ -77,6 +77,24 @@ int mgd_version(void);
  */
 mgd_status mgd_workspace_errors(const void *ws, void *stream, uint32_t *flags);
 
+/*
+ * Self-test of the device error path.  Every wait inside a libmgd kernel is
+ * bounded (2 s); one that gives up raises MGD_DEVERR_TIMEOUT in the
+ * workspace's error word and lets its kernel return, so the CUDA context
+ * stays usable.  This call launches one small kernel whose wait nothing ever
+ * satisfies, so it runs out on purpose:
+ *   which = 0: an mbarrier phase that nothing completes (the form of the
+ *              TMA, tensor-core and accumulator waits);
+ *   which = 1: a workspace counter that no CTA raises (the form of the
+ *              SnapKV scorer's wait for the other slices of a pair).
+ * Asynchronous on `stream`; the kernel takes about 2 s.  Afterwards
+ * mgd_workspace_errors(ws) reports MGD_DEVERR_TIMEOUT.  `ws`: device memory
+ * of at least MGD_SELFTEST_WS_BYTES.  Errors: MGD_ERR_INVALID_ARG (null ws,
+ * `which` not 0 or 1), MGD_ERR_WORKSPACE (ws_bytes too small), MGD_ERR_CUDA.
+ */
+#define MGD_SELFTEST_WS_BYTES 512u
+mgd_status mgd_selftest_bounded_wait(int which, void *ws, size_t ws_bytes, void *stream);
+
 /* ------------------------------------------------------------------------ *
  * Verify attention.  [MagicDec] section 3.2: verifying gamma draft tokens
  * and decoding read the same KV cache, so the target's verify pass is decode

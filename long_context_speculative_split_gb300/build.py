@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmgd.so")
-SOURCES = ["api.cu", "attn_tc.cu", "attn_simt.cu", "snapkv.cu", "snap_tc05.cu", "spec_sample.cu", "spec_noalloc.cu", "commit.cu", "streaming.cu"]
+SOURCES = ["api.cu", "attn_tc.cu", "attn_simt.cu", "snapkv.cu", "snap_tc05.cu", "spec_sample.cu", "spec_noalloc.cu", "commit.cu", "streaming.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 

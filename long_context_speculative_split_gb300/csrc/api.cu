@@ -193,6 +193,15 @@ mgd_status mgd_workspace_errors(const void *ws, void *stream, uint32_t *flags) {
   return MGD_OK;
 }
 
+mgd_status mgd_selftest_bounded_wait(int which, void *ws, size_t ws_bytes, void *stream) {
+  if (!ws) return fail(MGD_ERR_INVALID_ARG, "null workspace");
+  if (which != 0 && which != 1) return fail(MGD_ERR_INVALID_ARG, "which must be 0 or 1 (got %d)", which);
+  if (ws_bytes < MGD_SELFTEST_WS_BYTES)
+    return fail(MGD_ERR_WORKSPACE, "workspace %zu < %u bytes", ws_bytes, MGD_SELFTEST_WS_BYTES);
+  cudaError_t e = launch_selftest_wait(which, ws, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "self-test launch");
+}
+
 size_t mgd_verify_workspace_size(int B, int T, int Hq, int Hkv, int D, int kv_cap) {
   if (B <= 0 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || kv_cap < 1) return kAlign;
   return plan_attention(B, T, Hq, Hkv, D, kv_cap, current_sm_count()).ws_bytes;

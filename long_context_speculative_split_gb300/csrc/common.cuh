@@ -32,6 +32,24 @@ __device__ __forceinline__ void raise_error(WsHeader *hdr, unsigned bit) {
   atomicOr(&hdr->err, bit);
 }
 
+// Bounded spin until the counter at p (written by other CTAs) reaches `need`,
+// with acquire semantics at GPU scope and a short sleep between polls.
+// Returns false after kWaitLimitNs.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool spin_until_geq(const unsigned *p, unsigned need) {
+  if (ld_acquire_gpu(p) >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(p) < need) {
+    __nanosleep(64);
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
 // 2^x by the hardware approximation (PTX ex2.approx.ftz.f32): results below
 // 2^-126 flush to zero, which no softmax sum here can notice.
 __device__ __forceinline__ float ex2(float x) {

@@ -114,6 +114,11 @@ cudaError_t launch_snap_score_tc05(const SnapPlan &p, const SnapArgs &a, const C
 // (64 columns, G heads, W rows): the 128-byte-swizzled W*G x 64 tile of a KV head.
 int encode_qwin_tensor_map(CUtensorMap *map, const void *base, int B, int W, int Hq, int D, int G);
 
+// ------------------------------------------------------------------ self-test
+// One bounded wait that nothing completes (0: an mbarrier phase, 1: a counter
+// in the workspace); needs 2 * kAlign bytes of workspace.
+cudaError_t launch_selftest_wait(int which, void *ws, cudaStream_t stream);
+
 // ------------------------------------------------------------------ sampling
 struct SpecPlan {
   int B, gamma, V;

@@ -238,12 +238,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Ws
   return false;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
     snap_score_fused(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                      const int32_t *__restrict__ kv_len, unsigned char *__restrict__ ws, T5Params p) {
@@ -475,19 +469,9 @@ __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
       }
       if (jb.nt2 > 0) {
         // wait for every slice of the pair, then merge their partials into -lse
-        if (exch && !*abort_flag) {
-          const unsigned need = static_cast<unsigned>(jb.ns);
-          if (ld_acquire_gpu(&cnt[jb.pair]) < need) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(&cnt[jb.pair]) < need) {
-              __nanosleep(64);  // up to a pair's worth of CTAs poll this counter
-              if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                raise_error(hdr, 0x8u);
-                *abort_flag = 1;
-                break;
-              }
-            }
-          }
+        if (exch && !*abort_flag && !spin_until_geq(&cnt[jb.pair], static_cast<unsigned>(jb.ns))) {
+          raise_error(hdr, 0x8u);
+          *abort_flag = 1;
         }
         named_bar(1, kT5SoftWarps * 32);
         if (grp == 0) {  // merge the partials of every slice of row tl

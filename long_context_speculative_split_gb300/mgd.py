@@ -28,6 +28,7 @@ SIGNATURES = {
     "mgd_last_error": (ctypes.c_char_p, []),
     "mgd_version": (_i32, []),
     "mgd_workspace_errors": (_i32, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "mgd_selftest_bounded_wait": (_i32, [_i32, _vp, _sz, _vp]),
     "mgd_verify_workspace_size": (_sz, [_i32] * 6),
     "mgd_verify_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _f32, _i32,
                                _vp, _i32, _vp, _vp, _sz, _vp]),
@@ -121,6 +122,15 @@ def mgd_workspace_errors(ws, stream=None):
     flags = ctypes.c_uint32(0)
     _check(load().mgd_workspace_errors(_ptr(ws), _stream(stream), ctypes.byref(flags)))
     return flags.value
+
+
+SELFTEST_WS_BYTES = 512
+
+
+def mgd_selftest_bounded_wait(which, ws, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size()
+    _check(load().mgd_selftest_bounded_wait(which, _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def mgd_verify_workspace_size(B, T, Hq, Hkv, D, kv_cap):

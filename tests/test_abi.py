@@ -159,6 +159,21 @@ def test_spec_sample_rejects_bad_arguments_on_host(lib):
     assert call(B=0, draft_logits=None) == 0
 
 
+def test_selftest_rejects_bad_arguments_on_host(lib):
+    from long_context_speculative_split_gb300 import mgd
+
+    def call(which=0, ws=FAKE, ws_bytes=mgd.SELFTEST_WS_BYTES):
+        try:
+            mgd.mgd_selftest_bounded_wait(which, ws, ws_bytes, stream=0)
+            return 0
+        except mgd.MgdError as e:
+            return e.status
+    assert call(which=2) == 1 and call(which=-1) == 1
+    assert call(ws=None) == 1
+    assert call(ws_bytes=mgd.SELFTEST_WS_BYTES - 1) == 3
+    assert "MGD_SELFTEST_WS_BYTES %du" % mgd.SELFTEST_WS_BYTES in open(HEADER).read()
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     from long_context_speculative_split_gb300 import mgd
     monkeypatch.setattr(mgd, "LIB_PATH", str(tmp_path / "missing.so"))
