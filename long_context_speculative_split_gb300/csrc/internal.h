@@ -75,11 +75,15 @@ int encode_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Hkv, int
 // enough that the slices open at once (one per resident CTA) mostly stay in L2
 // until their pass 2 re-reads them, large enough that the per-job exchange
 // stays a small share of the job (measured: 1280 / 1536 / 1792 / 2048 keys).
+// Capacities above kSnapMaxSlices * kSnapSliceKeys keys get longer slices, so
+// that a pair never has more slices than CTAs are resident (the scorer's
+// waits for the other slices of a pair rely on that).
 constexpr int kSnapSliceKeys = 1536;
+constexpr int kSnapMaxSlices = 64;
 
 struct SnapPlan {
   int B, Hq, Hkv, D, kv_cap, W, G, rows, RG;
-  int C;       // keys per scoring unit (multiple of 64; kSnapSliceKeys for the tcgen05 scorer)
+  int C;       // keys per scoring unit (multiple of 64; a multiple of 128 for the tcgen05 scorer)
   int nchunk;  // ceil(kv_cap / C)
   int pairs;   // B * Hkv
   size_t off_cnt;  // unsigned [pairs]: slices published per pair (zeroed with the header on every call)

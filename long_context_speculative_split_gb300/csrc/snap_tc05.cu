@@ -14,7 +14,8 @@
 //           owns one key and sums exp2(s - lse_row) over the rows in registers.
 //
 // One read of K.  The work is cut into jobs = (sequence, KV head, slice of
-// kSnapSliceKeys keys).  A CTA runs pass 1 over its slice, publishes the
+// p.C keys: 1536, longer for capacities above 64 such slices).  A CTA runs
+// pass 1 over its slice, publishes the
 // slice's per-row (max, sum) and counts it in a per-(sequence, head) counter,
 // waits until every slice of that (sequence, head) has done the same (they
 // were claimed at nearly the same moment by other CTAs, since jobs are handed
@@ -64,7 +65,6 @@ constexpr uint32_t kT5TmemCols = 128 * kT5Groups;  // one 128-column accumulator
 static_assert(kT5Groups == 2 || kT5Groups == 4, "tcgen05.alloc takes a power-of-two column count");
 constexpr int kExchThread = 64;             // first softmax thread: job broadcast and exchange
 constexpr float kLog2e = 1.4426950408889634f;
-static_assert(kSnapSliceKeys % kT5Keys == 0, "slices are whole tiles");
 
 // Instruction descriptor of tcgen05.mma kind::f16: D f32, A and B bf16, both
 // K-major, M = 128, N = 128.
@@ -83,7 +83,7 @@ struct T5Layout {
 };
 
 struct T5Params {
-  int W, G, Hkv, nslice, kv_cap, units;
+  int W, G, Hkv, C, nslice, kv_cap, units;  // C: keys per slice
   float sl2;
   size_t off_cnt, off_part, off_scores;
 };
@@ -131,7 +131,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// One job: slice `slice` (kSnapSliceKeys keys from `start`) of (sequence b,
+// One job: slice `slice` (p.C keys from `start`) of (sequence b,
 // KV head hkv).  nt1 / nt2 = 128-key tiles of pass 1 (keys < L) and pass 2
 // (prefix keys < L - W); ns = slices of the pair that hold pass-1 keys.
 struct SliceJob {
@@ -146,12 +146,12 @@ __device__ __forceinline__ SliceJob slice_job(int u, const int32_t *__restrict__
   j.hkv = j.pair - j.b * p.Hkv;
   j.L = kv_len[j.b];
   j.valid = j.L >= p.W && j.L <= p.kv_cap;
-  j.start = j.slice * kSnapSliceKeys;
-  const int end1 = min(j.start + kSnapSliceKeys, j.L);
-  j.end2 = min(j.start + kSnapSliceKeys, j.L - p.W);
+  j.start = j.slice * p.C;
+  const int end1 = min(j.start + p.C, j.L);
+  j.end2 = min(j.start + p.C, j.L - p.W);
   j.nt1 = (j.valid && end1 > j.start) ? (end1 - j.start + kT5Keys - 1) / kT5Keys : 0;
   j.nt2 = (j.valid && j.end2 > j.start) ? (j.end2 - j.start + kT5Keys - 1) / kT5Keys : 0;
-  j.ns = j.valid ? (j.L + kSnapSliceKeys - 1) / kSnapSliceKeys : 0;
+  j.ns = j.valid ? (j.L + p.C - 1) / p.C : 0;
   return j;
 }
 
@@ -518,7 +518,9 @@ __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
 
 }  // namespace
 
-bool snap_tc05_eligible(const SnapPlan &p) { return p.D == 128 && p.rows == 128 && p.RG == 1 && p.C == kSnapSliceKeys; }
+bool snap_tc05_eligible(const SnapPlan &p) {
+  return p.D == 128 && p.rows == 128 && p.RG == 1 && p.C % kT5Keys == 0 && p.nchunk <= kSnapMaxSlices;
+}
 
 cudaError_t launch_snap_score_tc05(const SnapPlan &pl, const SnapArgs &a, const CUtensorMap &kmap,
                                    const CUtensorMap &qmap) {
@@ -526,6 +528,7 @@ cudaError_t launch_snap_score_tc05(const SnapPlan &pl, const SnapArgs &a, const 
   kp.W = pl.W;
   kp.G = pl.G;
   kp.Hkv = pl.Hkv;
+  kp.C = pl.C;
   kp.nslice = pl.nchunk;
   kp.kv_cap = pl.kv_cap;
   kp.units = pl.pairs * pl.nchunk;

@@ -819,7 +819,10 @@ SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W) {
   const int cmin = std::max(256, ((kv_cap + 63) / 64 + 63) / 64 * 64);
   while (C > cmin && static_cast<long long>(p.pairs) * p.RG * ((kv_cap + C - 1) / C) < 8LL * slots) C /= 2;
   if (C < cmin) C = cmin;
-  if (D == 128 && p.rows == 128 && p.RG == 1) C = kSnapSliceKeys;  // the one-read tcgen05 scorer's slices
+  if (D == 128 && p.rows == 128 && p.RG == 1) {  // the one-read tcgen05 scorer's slices
+    const int per_slice = (kv_cap + kSnapMaxSlices - 1) / kSnapMaxSlices;
+    C = std::max(kSnapSliceKeys, (per_slice + 127) / 128 * 128);
+  }
   p.C = C;
   p.nchunk = (kv_cap + C - 1) / C;
   p.off_cnt = kAlign;

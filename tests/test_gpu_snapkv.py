@@ -62,6 +62,10 @@ CASES = [
     # lengths at tile (128) and scoring-slice (1536) edges: a slice holding only window keys,
     # a window that straddles a slice edge, a prefix of one key
     (4, 32, 8, 128, [1537, 1568, 3112, 33], 3200, 32, 7, 256),
+    (2, 64, 8, 128, [3000, 1600], 3000, 16, 5, 300),  # G = 8 x W = 16 window rows on the tensor-core scorer
+    # capacities long enough that the scorer's slices grow past 1536 keys (at most 64 per sequence)
+    (1, 8, 2, 128, [200000], 200000, 32, 7, 1024),
+    (2, 8, 2, 128, [150001, 70000], 160000, 32, 7, 512),
 ]
 
 
