@@ -588,6 +588,11 @@ __global__ void __launch_bounds__(256)
 
 // ---------------------------------------------------------------- select + gather
 constexpr int kSelThreads = 1024;
+constexpr int kPoolTile = 4096;     // scores staged in shared memory per pooling step
+constexpr int kPoolHalo = 64;       // pool radius up to which the staged path is used
+constexpr int kStageLoads = (kPoolTile + 2 * kPoolHalo + kSelThreads - 1) / kSelThreads;
+constexpr int kSweepLoads = 8;      // pooled values in flight per thread in a radix pass
+constexpr int kCompactLoads = 4;    // 32-position rows in flight per warp in the compaction
 
 struct SelParams {
   int Hkv, W, pool, K, kv_cap, draft_cap, row_bytes;
@@ -631,6 +636,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   __shared__ unsigned hist[2048];
   __shared__ unsigned sm_warp[33];
   __shared__ unsigned s_bin, s_above;
+  __shared__ float stage[kPoolTile + 2 * kPoolHalo];  // scores of one pooling tile and its halo
   WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
   const int b = blockIdx.x / sp.Hkv, hkv = blockIdx.x % sp.Hkv;
   const int L = kv_len[b];
@@ -655,14 +661,41 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   // ---- 1. max-pool (and the optional copy out), with the first radix
   //         pass's histogram of the top 11 bits
   for (int i = threadIdx.x; i < 2048; i += kSelThreads) hist[i] = 0u;
-  __syncthreads();
-  for (int j = threadIdx.x; j < n; j += kSelThreads) {
-    float m = s[j];
-    const int lo = max(0, j - r), hi = min(n - 1, j + r);
-    for (int t = lo; t <= hi; ++t) m = fmaxf(m, s[t]);
+  auto emit = [&](int j, float m) {
     pooled[j] = m;
     if (scores_out) scores_out[pr * sp.kv_cap + j] = m;
     if (partial) atomicAdd(&hist[__float_as_uint(m) >> 21], 1u);
+  };
+  if (r <= kPoolHalo) {
+    // tiles of kPoolTile scores staged in shared memory with their halo (every
+    // thread's loads issued together), positions outside the prefix as -inf
+    for (int t0 = 0; t0 < n; t0 += kPoolTile) {
+      const int len = min(kPoolTile, n - t0), cnt = len + 2 * r;
+      __syncthreads();  // the previous tile's readers are done
+      float x[kStageLoads];
+#pragma unroll
+      for (int u = 0; u < kStageLoads; ++u) {
+        const int i = threadIdx.x + u * kSelThreads, t = t0 - r + i;
+        x[u] = (i < cnt && t >= 0 && t < n) ? s[t] : -INFINITY;
+      }
+#pragma unroll
+      for (int u = 0; u < kStageLoads; ++u)
+        if (threadIdx.x + u * kSelThreads < cnt) stage[threadIdx.x + u * kSelThreads] = x[u];
+      __syncthreads();
+      for (int i = threadIdx.x; i < len; i += kSelThreads) {
+        float m = stage[i];
+        for (int o = 1; o <= 2 * r; ++o) m = fmaxf(m, stage[i + o]);
+        emit(t0 + i, m);
+      }
+    }
+  } else {
+    __syncthreads();
+    for (int j = threadIdx.x; j < n; j += kSelThreads) {
+      float m = s[j];
+      const int lo = max(0, j - r), hi = min(n - 1, j + r);
+      for (int t = lo; t <= hi; ++t) m = fmaxf(m, s[t]);
+      emit(j, m);
+    }
   }
   __syncthreads();
 
@@ -676,9 +709,16 @@ __global__ void __launch_bounds__(kSelThreads, 2)
       if (pass > 0) {  // pass 0's histogram came with the pooling
         for (int i = threadIdx.x; i < nb; i += kSelThreads) hist[i] = 0u;
         __syncthreads();
-        for (int j = threadIdx.x; j < n; j += kSelThreads) {
-          const unsigned key = __float_as_uint(pooled[j]);
-          if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+        for (int j0 = threadIdx.x; j0 < n; j0 += kSweepLoads * kSelThreads) {
+          unsigned key[kSweepLoads];  // loads issued together, then counted
+#pragma unroll
+          for (int u = 0; u < kSweepLoads; ++u) {
+            const int j = j0 + u * kSelThreads;
+            key[u] = (j < n) ? __float_as_uint(pooled[j]) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < kSweepLoads; ++u)
+            if (j0 + u * kSelThreads < n && (key[u] & mask) == prefix) atomicAdd(&hist[(key[u] >> shift) & (nb - 1)], 1u);
         }
         __syncthreads();
       }
@@ -713,12 +753,19 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   const unsigned lt_mask = (1u << lane) - 1u;
   const int wseg = ((n + kSelThreads / 32 - 1) / (kSelThreads / 32) + 31) / 32 * 32;
   const int w0 = min(n, warp * wseg), w1 = min(n, w0 + wseg);
-  auto classify = [&](int j, unsigned &gt, unsigned &eq) {
+  // keys of positions jb + 32u + lane (u < kCompactLoads), loaded together
+  auto load_keys = [&](int jb, unsigned (&key)[kCompactLoads]) {
+#pragma unroll
+    for (int u = 0; u < kCompactLoads; ++u) {
+      const int j = jb + 32 * u + lane;
+      key[u] = (partial && j < w1) ? __float_as_uint(pooled[j]) : 0u;
+    }
+  };
+  auto classify = [&](int j, unsigned key, unsigned &gt, unsigned &eq) {
     gt = 0u;
     eq = 0u;
     if (j < w1) {
       if (partial) {
-        const unsigned key = __float_as_uint(pooled[j]);
         gt = key > tau ? 1u : 0u;
         eq = key == tau ? 1u : 0u;
       } else {
@@ -727,11 +774,16 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     }
   };
   unsigned gt_cnt = 0u, eq_cnt = 0u;
-  for (int jb = w0; jb < w1; jb += 32) {
-    unsigned gt, eq;
-    classify(jb + lane, gt, eq);
-    gt_cnt += __popc(__ballot_sync(0xffffffffu, gt));
-    eq_cnt += __popc(__ballot_sync(0xffffffffu, eq));
+  for (int jb = w0; jb < w1; jb += 32 * kCompactLoads) {
+    unsigned key[kCompactLoads];
+    load_keys(jb, key);
+#pragma unroll
+    for (int u = 0; u < kCompactLoads; ++u) {
+      unsigned gt, eq;
+      classify(jb + 32 * u + lane, key[u], gt, eq);
+      gt_cnt += __popc(__ballot_sync(0xffffffffu, gt));
+      eq_cnt += __popc(__ballot_sync(0xffffffffu, eq));
+    }
   }
   if (lane == 0) {
     hist[warp] = gt_cnt;
@@ -754,15 +806,20 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   }
   __syncthreads();
   unsigned g_before = hist[64 + warp], e_before = hist[96 + warp];
-  for (int jb = w0; jb < w1; jb += 32) {
-    const int j = jb + lane;
-    unsigned gt, eq;
-    classify(j, gt, eq);
-    const unsigned gb = __ballot_sync(0xffffffffu, gt), eb = __ballot_sync(0xffffffffu, eq);
-    const unsigned gpos = g_before + __popc(gb & lt_mask), epos = e_before + __popc(eb & lt_mask);
-    if (gt || (eq && epos < krem)) sel[gpos + min(epos, krem)] = j;
-    g_before += __popc(gb);
-    e_before += __popc(eb);
+  for (int jb = w0; jb < w1; jb += 32 * kCompactLoads) {
+    unsigned key[kCompactLoads];
+    load_keys(jb, key);
+#pragma unroll
+    for (int u = 0; u < kCompactLoads; ++u) {
+      const int j = jb + 32 * u + lane;
+      unsigned gt, eq;
+      classify(j, key[u], gt, eq);
+      const unsigned gb = __ballot_sync(0xffffffffu, gt), eb = __ballot_sync(0xffffffffu, eq);
+      const unsigned gpos = g_before + __popc(gb & lt_mask), epos = e_before + __popc(eb & lt_mask);
+      if (gt || (eq && epos < krem)) sel[gpos + min(epos, krem)] = j;
+      g_before += __popc(gb);
+      e_before += __popc(eb);
+    }
   }
   for (int w = threadIdx.x; w < sp.W; w += kSelThreads) sel[ktop + w] = n + w;
   for (int i = Keff + threadIdx.x; i < sp.draft_cap; i += kSelThreads) sel[i] = -1;
