@@ -462,10 +462,12 @@ __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
 #pragma unroll
           for (int g = 1; g < kT5Groups; ++g) l += sm_red[g * 256 + 128 + tl] * exp2f(sm_red[g * 256 + tl] - mu);
           part[(static_cast<size_t>(jb.pair) * p.nslice + jb.slice) * 128 + tl] = make_float2(mn, l);
-          __threadfence();
         }
         named_bar(1, kT5SoftWarps * 32);
-        if (exch) atomicAdd(&cnt[jb.pair], 1u);
+        if (exch) {  // after the barrier, one fence orders the 128 rows written above before the count
+          __threadfence();
+          atomicAdd(&cnt[jb.pair], 1u);
+        }
       }
       if (jb.nt2 > 0) {
         // wait for every slice of the pair, then merge their partials into -lse
