@@ -87,6 +87,8 @@ struct SnapPlan {
   int nchunk;  // ceil(kv_cap / C)
   int pairs;   // B * Hkv
   size_t off_cnt;  // unsigned [pairs]: slices published per pair (zeroed with the header on every call)
+  int lrows;       // windows of <= 8 rows: logit rows stored per key by pass 1 (4 or 8), else 0
+  size_t off_logits;  // float [pairs][kv_cap][lrows] when lrows > 0
   size_t off_part, off_scores, off_pooled, ws_bytes;
 };
 SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W);

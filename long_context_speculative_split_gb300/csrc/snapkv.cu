@@ -37,9 +37,9 @@ constexpr int kRowsPerCta = 128;    // window rows (w, g) scored per CTA
 constexpr int kBoxBytes = 64 * 128;
 
 struct SnapK {
-  int W, G, Hq, Hkv, rows, RG, C, nchunk, kv_cap;
+  int W, G, Hq, Hkv, rows, RG, C, nchunk, kv_cap, lrows;
   float sl2;
-  size_t off_part, off_scores;
+  size_t off_part, off_scores, off_logits;
 };
 
 template <int D>
@@ -461,6 +461,18 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
       phase ^= 1u;
     }
     const int k_lo = key0 + gid, k_hi = key0 + gid + 8;  // accumulator rows gid / gid + 8
+    if (PASS == 1 && NT == 1 && p.lrows > 0 && 2 * tig < p.lrows) {
+      // keep this key's logits (rows 2 tig, 2 tig + 1) for the key sums; every
+      // window row sees every prefix key, so no mask applies below L - W
+      float *lg = reinterpret_cast<float *>(ws + p.off_logits) + static_cast<size_t>(pair) * p.kv_cap * p.lrows;
+      const int nprefix = min(end, L - p.W);
+      if (k_lo < nprefix)
+        *reinterpret_cast<float2 *>(lg + static_cast<size_t>(k_lo) * p.lrows + 2 * tig) =
+            make_float2(s[0][0] * p.sl2, s[0][1] * p.sl2);
+      if (k_hi < nprefix)
+        *reinterpret_cast<float2 *>(lg + static_cast<size_t>(k_hi) * p.lrows + 2 * tig) =
+            make_float2(s[0][2] * p.sl2, s[0][3] * p.sl2);
+    }
     if (PASS == 1) {
 #pragma unroll
       for (int j = 0; j < NT; ++j)
@@ -514,6 +526,68 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         if (x.y > 0.f) S += x.y * exp2f(x.x - mu);
       }
       part[(static_cast<size_t>(pair) * p.nchunk + chunk) * kRowsPerCta + r] = make_float2(M, S);
+    }
+  }
+}
+
+// Key sums from the logits pass 1 kept (windows of <= 8 rows): for each prefix
+// key j of the chunk, sum over the rows of exp2(logit - lse_row), lse from the
+// pass-1 partials.  Streams R floats per key instead of reading K again.
+template <int R>
+__global__ void __launch_bounds__(256)
+    snap_logit_sum(const int32_t *__restrict__ kv_len, unsigned char *__restrict__ ws, SnapK p) {
+  __shared__ float sm_nl[R];
+  const int chunk = blockIdx.x % p.nchunk;
+  const int pair = blockIdx.x / p.nchunk;
+  const int b = pair / p.Hkv;
+  const int L = kv_len[b];
+  if (L < p.W || L > p.kv_cap) return;  // raised by pass 1
+  const int start = chunk * p.C, end = min(start + p.C, L - p.W);
+  if (start >= end) return;
+  if (threadIdx.x < R) {  // minus the log2-sum-exp of every row (padding rows contribute 0)
+    const int r = threadIdx.x;
+    float v = -INFINITY;
+    if (r < p.rows) {
+      const int nch1 = (L + p.C - 1) / p.C;
+      const float2 *pp = reinterpret_cast<const float2 *>(ws + p.off_part) + static_cast<size_t>(pair) * p.nchunk * kRowsPerCta + r;
+      float M = -INFINITY;
+      for (int c = 0; c < nch1; ++c) M = fmaxf(M, pp[c * kRowsPerCta].x);
+      float S = 0.f;
+      for (int c = 0; c < nch1; ++c) {
+        const float2 x = pp[c * kRowsPerCta];
+        if (x.y > 0.f) S += x.y * exp2f(x.x - M);
+      }
+      v = -(M + log2f(S));
+    }
+    sm_nl[r] = v;
+  }
+  __syncthreads();
+  float nl[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) nl[r] = sm_nl[r];
+  const float4 *lg = reinterpret_cast<const float4 *>(ws + p.off_logits) + static_cast<size_t>(pair) * p.kv_cap * (R / 4);
+  float *dst = reinterpret_cast<float *>(ws + p.off_scores) + static_cast<size_t>(pair) * p.kv_cap;
+  constexpr int kU = 4;  // keys in flight per thread
+  for (int j0 = start + threadIdx.x; j0 < end; j0 += kU * 256) {
+    float4 x[kU][R / 4];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+#pragma unroll
+      for (int h = 0; h < R / 4; ++h) {
+        const int j = j0 + u * 256;
+        x[u][h] = (j < end) ? lg[static_cast<size_t>(j) * (R / 4) + h] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int j = j0 + u * 256;
+      if (j < end) {
+        float acc = 0.f;
+#pragma unroll
+        for (int h = 0; h < R / 4; ++h)
+          acc += (ex2(x[u][h].x + nl[4 * h]) + ex2(x[u][h].y + nl[4 * h + 1])) +
+                 (ex2(x[u][h].z + nl[4 * h + 2]) + ex2(x[u][h].w + nl[4 * h + 3]));
+        dst[j] = acc;
+      }
     }
   }
 }
@@ -890,6 +964,12 @@ SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W) {
   off = align_up(off + sizeof(float) * static_cast<size_t>(p.pairs) * kv_cap);
   p.off_pooled = off;
   off = align_up(off + sizeof(float) * static_cast<size_t>(p.pairs) * kv_cap);
+  // Windows of at most 8 rows (the draft query alone, for one): pass 1 keeps
+  // every prefix key's logits (16 or 32 bytes a key) and the key sums are
+  // taken from them, instead of a second read of K (2 * D bytes a key).
+  p.lrows = (p.rows <= 4) ? 4 : (p.rows <= 8) ? 8 : 0;
+  p.off_logits = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(p.pairs) * kv_cap * p.lrows);
   p.ws_bytes = off;
   return p;
 }
@@ -912,6 +992,8 @@ cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, cons
   kp.sl2 = a.sm_scale * kLog2e;
   kp.off_part = p.off_part;
   kp.off_scores = p.off_scores;
+  kp.lrows = p.lrows;
+  kp.off_logits = p.off_logits;
   if (in_f32 || kmap == nullptr) {
     const size_t smem = sizeof(float) * p.rows;
     if (in_f32) {
@@ -956,7 +1038,14 @@ cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, cons
     MGD_KR(DD, NTT, 1);        \
     MGD_KR(DD, NTT, 2);        \
   } while (0)
-    if (p.D == 128) {
+    if (nt == 1 && p.lrows > 0) {  // pass 1 keeps the logits; the key sums stream them
+      if (p.D == 128) MGD_KR(128, 1, 1);
+      else MGD_KR(64, 1, 1);
+      if (p.lrows == 4) snap_logit_sum<4><<<units, 256, 0, a.stream>>>(a.kv_len, ws, kp);
+      else snap_logit_sum<8><<<units, 256, 0, a.stream>>>(a.kv_len, ws, kp);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    } else if (p.D == 128) {
       if (nt == 1) MGD_KR_PASSES(128, 1);
       else if (nt == 2) MGD_KR_PASSES(128, 2);
       else MGD_KR_PASSES(128, 4);
