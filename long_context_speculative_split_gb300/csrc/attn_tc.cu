@@ -290,12 +290,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
           s[j][e] = p0;
           s[j][2 + e] = p1;
         }
+        const float2 a2 = make_float2(alpha[0], alpha[1]);
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          acc[mt][j][0] *= alpha[0];
-          acc[mt][j][1] *= alpha[1];
-          acc[mt][j][2] *= alpha[0];
-          acc[mt][j][3] *= alpha[1];
+        for (int mt = 0; mt < MT; ++mt) {  // paired (f32x2) multiplies: columns 2 tig, 2 tig + 1
+          const float2 x = __fmul2_rn(make_float2(acc[mt][j][0], acc[mt][j][1]), a2);
+          const float2 y = __fmul2_rn(make_float2(acc[mt][j][2], acc[mt][j][3]), a2);
+          acc[mt][j][0] = x.x;
+          acc[mt][j][1] = x.y;
+          acc[mt][j][2] = y.x;
+          acc[mt][j][3] = y.y;
         }
         uint32_t h0, l0, h1, l1;
         split_bf16(s[j][0], s[j][1], h0, l0);  // keys gid,   rows 2tig, 2tig+1
