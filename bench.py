@@ -10,7 +10,7 @@ rejection sampling.  The headline metric is verified tokens per second per
 layer (B * (gamma+1) per step); per-kernel KV-read GB/s and the HBM roofline
 fraction of the verify kernel are reported beside it.
 
-  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--config 2|3|4]
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
 
 With --gpus N > 1 launch under torch.distributed.run: every rank runs the same
 batch on its own GPU (weak scaling, no collective on the data path); the
@@ -47,8 +47,10 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--config", type=int, default=3, choices=[2, 3, 4, 5],
-                   help="3: batch 128 x 32k (default); 5: full 32-layer speculation round")
+    p.add_argument("--workload", default="b128_ctx32k",
+                   choices=["b32_ctx8k", "b128_ctx32k", "ragged_b256_ctx4k_64k", "round_b32_ctx16k_32layers"],
+                   help="b128_ctx32k: batch 128 x 32k (default); round_b32_ctx16k_32layers: full 32-layer "
+                        "speculation round")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=1, help="sequences in the oracle sample")
@@ -148,11 +150,11 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ the GPU workload
 class Workload:
-    def __init__(self, cid, device, seed=0):
+    def __init__(self, name, device, seed=0):
         from long_context_speculative_split_gb300 import mgd, ops
         from long_context_speculative_split_gb300 import workloads as wl
         self.ops, self.mgd, self.wl = ops, mgd, wl
-        c = self.cfg = wl.CONFIGS[cid]
+        c = self.cfg = wl.WORKLOADS[name]
         self.dev = device
         self.B, self.Hq, self.Hkv, self.D = c["B"], c["Hq"], c["Hkv"], c["D"]
         self.gamma, self.K, self.W, self.P, self.V = c["gamma"], c["K"], c["W"], c["pool"], c["V"]
@@ -374,7 +376,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from long_context_speculative_split_gb300 import workloads as wl
-    cfg = wl.CONFIGS[args.config]
+    cfg = wl.WORKLOADS[args.workload]
     T = cfg["gamma"] + 1
     for _ in range(args.warmup):
         oracle_sample_step(cfg, 1)
@@ -415,7 +417,7 @@ def run_ours(args):
     dist_init(world, "nccl")
     import __graft_entry__
     __graft_entry__.build()
-    w = Workload(args.config, dev, seed=rank)
+    w = Workload(args.workload, dev, seed=rank)
     for _ in range(args.warmup):
         w.step()
     torch.cuda.synchronize()
@@ -454,7 +456,7 @@ def run_ours(args):
         e_ms = max_over_ranks(e_ms, world, dev)
         e2e = {"value": world * tokens / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
-    traffic = load_traffic(args.config)
+    traffic = load_traffic(args.workload)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -497,7 +499,7 @@ def run_ours(args):
 
 
 def run_round(args):
-    """Config 5: one full 32-layer speculation round per step, replayed from a CUDA graph."""
+    """The 32-layer round workload: one full speculation round per step, replayed from a CUDA graph."""
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -506,7 +508,7 @@ def run_round(args):
     __graft_entry__.build()
     from long_context_speculative_split_gb300 import workloads as wl
     from long_context_speculative_split_gb300.round import SpeculationRound
-    cfg = wl.CONFIGS[5]
+    cfg = wl.WORKLOADS["round_b32_ctx16k_32layers"]
     r = SpeculationRound(cfg, dev, seed=rank).prepare()
     graph = True
     try:
@@ -578,7 +580,7 @@ def speedup_model(t_decode, t_verify, t_draft, t_select, gamma):
     return out
 
 
-def load_traffic(cid):
+def load_traffic(name):
     """DRAM bytes per verify launch from the committed ncu summary; None once the kernel source changed."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "verify_attention_traffic.json")
@@ -590,7 +592,7 @@ def load_traffic(cid):
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
         if d.get("kernel_source_sha256_16") != sha:
             return None
-        return d.get("config%d" % cid)
+        return d.get(name)
     except Exception:
         return None
 
@@ -599,7 +601,7 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
-    if args.config == 5:
+    if args.workload == "round_b32_ctx16k_32layers":
         return run_round(args)
     return run_ours(args)
 

@@ -23,16 +23,17 @@ import torch
 # the float64 oracle (tests/golden/calibrate_round_sigma.py -> round_sigma.json).
 ROUND_SIGMA_N = 0.25557936727955166
 
-CONFIGS = {
-    1: dict(name="tiny_b2", B=2, Hq=4, Hkv=1, D=64, dtype="f32", lens=[512, 300], gamma=3, W=16, pool=5, K=64,
+# Workloads by name; each entry's "name" repeats its key.
+WORKLOADS = {
+    "tiny_b2": dict(name="tiny_b2", B=2, Hq=4, Hkv=1, D=64, dtype="f32", lens=[512, 300], gamma=3, W=16, pool=5, K=64,
             V=1000, sigma=2.0, sigma_n=None, hh=0.0),
-    2: dict(name="b32_ctx8k", B=32, Hq=32, Hkv=8, D=128, dtype="bf16", lens=8192, gamma=3, W=32, pool=7, K=512,
+    "b32_ctx8k": dict(name="b32_ctx8k", B=32, Hq=32, Hkv=8, D=128, dtype="bf16", lens=8192, gamma=3, W=32, pool=7, K=512,
             V=128256, sigma=3.0, sigma_n=0.5, hh=0.01),
-    3: dict(name="b128_ctx32k", B=128, Hq=32, Hkv=8, D=128, dtype="bf16", lens=32768, gamma=4, W=32, pool=7,
+    "b128_ctx32k": dict(name="b128_ctx32k", B=128, Hq=32, Hkv=8, D=128, dtype="bf16", lens=32768, gamma=4, W=32, pool=7,
             K=1024, V=128256, sigma=3.0, sigma_n=0.5, hh=0.01),
-    4: dict(name="ragged_b256_ctx4k_64k", B=256, Hq=32, Hkv=8, D=128, dtype="bf16", lens=(4096, 65536), gamma=2,
+    "ragged_b256_ctx4k_64k": dict(name="ragged_b256_ctx4k_64k", B=256, Hq=32, Hkv=8, D=128, dtype="bf16", lens=(4096, 65536), gamma=2,
             W=32, pool=7, K=512, V=128256, sigma=3.0, sigma_n=0.5, hh=0.01),
-    5: dict(name="round_b32_ctx16k_32layers", B=32, Hq=32, Hkv=8, D=128, dtype="bf16", lens=16384, gamma=3, W=32,
+    "round_b32_ctx16k_32layers": dict(name="round_b32_ctx16k_32layers", B=32, Hq=32, Hkv=8, D=128, dtype="bf16", lens=16384, gamma=3, W=32,
             pool=7, K=512, V=128256, sigma=3.0, sigma_n=ROUND_SIGMA_N, hh=0.01, layers=32),
 }
 

@@ -34,7 +34,7 @@ def mean_alpha(sigma_n, cfg):
 
 
 def main():
-    cfg = wl.CONFIGS[5]
+    cfg = wl.WORKLOADS["round_b32_ctx16k_32layers"]
     lo, hi = 0.0, 3.0
     for _ in range(40):
         mid = 0.5 * (lo + hi)

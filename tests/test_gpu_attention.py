@@ -83,7 +83,7 @@ def test_verify_bf16_output_dtype():
 
 def test_verify_float32_tiny_config_full():
     dev = gpu_or_skip()
-    c = wl.CONFIGS[1]
+    c = wl.WORKLOADS["tiny_b2"]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len)
     q = wl.queries(c, dev)
@@ -95,7 +95,7 @@ def test_verify_float32_tiny_config_full():
 
 def test_draft_float32_tiny_config_full():
     dev = gpu_or_skip()
-    c = wl.CONFIGS[1]
+    c = wl.WORKLOADS["tiny_b2"]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len)
     qd = wl.draft_queries(c, dev)
@@ -151,11 +151,11 @@ def _sampled_pairs(kv_len, Hkv, n=3, seed=0):
     return [(b, int(rng.integers(Hkv))) for b in sorted(bs)]
 
 
-@pytest.mark.parametrize("cid", [2, 3, 4])
-def test_verify_full_size_sampled(cid):
+@pytest.mark.parametrize("name", ["b32_ctx8k", "b128_ctx32k", "ragged_b256_ctx4k_64k"])
+def test_verify_full_size_sampled(name):
     """Full-size workload in the benchmark's launch configuration; sampled (sequence, KV head) pairs."""
     dev = gpu_or_skip()
-    c = wl.CONFIGS[cid]
+    c = wl.WORKLOADS[name]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len)
     q = wl.queries(c, dev)
@@ -173,10 +173,10 @@ def test_verify_full_size_sampled(cid):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("cid", [2, 3])
-def test_draft_full_size_sampled(cid):
+@pytest.mark.parametrize("name", ["b32_ctx8k", "b128_ctx32k"])
+def test_draft_full_size_sampled(name):
     dev = gpu_or_skip()
-    c = wl.CONFIGS[cid]
+    c = wl.WORKLOADS[name]
     K = c["K"]
     dlen = torch.full((c["B"],), K, dtype=torch.int32)
     kd, vd = wl.kv_cache(c, dev, kv_len=dlen, cap=K, layer=7)
@@ -210,7 +210,7 @@ def test_verify_ragged_every_sequence():
     """Ragged batch 256 x U[4096, 65536] (the benchmark's launch configuration): every
     sequence checked, so no unit of the persistent schedule can go missing unnoticed."""
     dev = gpu_or_skip()
-    c = wl.CONFIGS[4]
+    c = wl.WORKLOADS["ragged_b256_ctx4k_64k"]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len)
     q = wl.queries(c, dev)

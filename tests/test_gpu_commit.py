@@ -51,7 +51,7 @@ def test_commit_after_a_sampled_round():
     """Feed the sampler's num_accepted straight into the commit step."""
     dev = gpu_or_skip()
     from long_context_speculative_split_gb300 import workloads as wl
-    c = dict(wl.CONFIGS[2], B=16, V=2048)
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=16, V=2048)
     t, d = wl.logits(c, dev)
     u = wl.uniforms(c, dev)
     tok = ops.draft_draw(d, u)

@@ -26,7 +26,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module")
 def rnd():
     dev = gpu_or_skip()
-    r = SpeculationRound(wl.CONFIGS[5], dev).prepare()
+    r = SpeculationRound(wl.WORKLOADS["round_b32_ctx16k_32layers"], dev).prepare()
     r.run()
     torch.cuda.synchronize()
     yield r

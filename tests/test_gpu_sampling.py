@@ -58,10 +58,10 @@ def _compare_round(t, d, u, dev, min_frac=0.75):
     return nacc_c
 
 
-@pytest.mark.parametrize("cid", [1, 2, 3])
-def test_round_matches_oracle(cid):
+@pytest.mark.parametrize("name", ["tiny_b2", "b32_ctx8k", "b128_ctx32k"])
+def test_round_matches_oracle(name):
     dev = gpu_or_skip()
-    c = wl.CONFIGS[cid]
+    c = wl.WORKLOADS[name]
     t, d = wl.logits(c, "cpu")
     u = wl.uniforms(c, "cpu")
     _compare_round(t, d, u, dev)
@@ -69,7 +69,7 @@ def test_round_matches_oracle(cid):
 
 def test_odd_vocab_and_many_sequences():
     dev = gpu_or_skip()
-    c = dict(wl.CONFIGS[2], B=300, V=4099, gamma=5, sigma=2.0, sigma_n=1.0)
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=300, V=4099, gamma=5, sigma=2.0, sigma_n=1.0)
     t, d = wl.logits(c, "cpu", seed=4)
     u = wl.uniforms(c, "cpu", seed=4)
     _compare_round(t, d, u, dev)
@@ -77,7 +77,7 @@ def test_odd_vocab_and_many_sequences():
 
 def test_single_row_draft_draw():
     dev = gpu_or_skip()
-    c = wl.CONFIGS[2]
+    c = wl.WORKLOADS["b32_ctx8k"]
     _, d = wl.logits(c, "cpu", seed=1)
     u = wl.uniforms(c, "cpu", seed=1)
     tok = torch.full((c["B"], c["gamma"]), -7, dtype=torch.int32, device=dev)
@@ -139,7 +139,7 @@ def test_omega_closed_form_on_gpu():
 
 def test_equal_distributions_accept_everything():
     dev = gpu_or_skip()
-    c = dict(wl.CONFIGS[2], B=64, V=5000)
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=64, V=5000)
     t, _ = wl.logits(c, "cpu", seed=2)
     d = t[:, :c["gamma"]].contiguous()
     u = wl.uniforms(c, "cpu", seed=2)
@@ -149,7 +149,7 @@ def test_equal_distributions_accept_everything():
 
 def test_invalid_draft_token_raises_device_flag():
     dev = gpu_or_skip()
-    c = dict(wl.CONFIGS[1], B=4, V=100)
+    c = dict(wl.WORKLOADS["tiny_b2"], B=4, V=100)
     t, d = wl.logits(c, dev)
     u = wl.uniforms(c, dev)
     tok = torch.tensor([[0, 1, 2], [5, 100, 1], [-1, 0, 0], [3, 3, 3]], dtype=torch.int32, device=dev)

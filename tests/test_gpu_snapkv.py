@@ -40,7 +40,7 @@ def _check_pair(res, k, v, b, h, L, W, P, K, ref_scores_row, D):
 
 def test_tiny_config_float32_full():
     dev = gpu_or_skip()
-    c = wl.CONFIGS[1]
+    c = wl.WORKLOADS["tiny_b2"]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len)
     qw = wl.window_queries(c, dev)
@@ -89,19 +89,19 @@ def test_bf16_cases_match_oracle(case):
             _check_pair(res, k, v, b, h, lens[b], W, P, K, s[b, h], D)
 
 
-@pytest.mark.parametrize("cid", [2, 3, 4])
-def test_full_size_sampled(cid):
-    """Full-size workloads (config 4: ragged lengths 4k-64k at batch 256) with sampled pairs:
+@pytest.mark.parametrize("name,seed", [("b32_ctx8k", 2), ("b128_ctx32k", 3), ("ragged_b256_ctx4k_64k", 4)])
+def test_full_size_sampled(name, seed):
+    """Full-size workloads (including ragged lengths 4k-64k at batch 256) with sampled pairs:
     the first, the last, the longest sequence's and one random (sequence, KV head)."""
     dev = gpu_or_skip()
-    c = wl.CONFIGS[cid]
+    c = wl.WORKLOADS[name]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len, cap=wl.capacity(c))
     qw = wl.window_queries(c, dev)
     res = ops.snapkv_select(qw, k, v, kv_len.to(dev), c["W"], c["pool"], c["K"], want_scores=True)
     torch.cuda.synchronize()
     G = c["Hq"] // c["Hkv"]
-    rng = np.random.default_rng(cid)
+    rng = np.random.default_rng(seed)
     pairs = [(0, 0), (c["B"] - 1, c["Hkv"] - 1), (int(np.argmax(kv_len.numpy())), 3),
              (int(rng.integers(c["B"])), int(rng.integers(c["Hkv"])))]
     for b, h in pairs:

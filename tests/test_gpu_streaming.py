@@ -37,7 +37,7 @@ def test_streaming_matches_oracle(dtype, sink, K, lens):
 def test_streaming_full_size():
     """Benchmark shape: batch 128, context 32768, budget 1024 with 4 sinks."""
     dev = gpu_or_skip()
-    c = wl.CONFIGS[3]
+    c = wl.WORKLOADS["b128_ctx32k"]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len)
     res = ops.streaming_select(k, v, kv_len.to(dev), 4, c["K"])

@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _inputs(dev, seed):
-    c = dict(wl.CONFIGS[2], B=8, lens=4096, V=32000)
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=8, lens=4096, V=32000)
     kv_len = wl.lengths(c, seed)
     k, v = wl.kv_cache(c, dev, seed, kv_len=kv_len, cap=4096)
     q = wl.queries(c, dev, seed)

@@ -79,7 +79,7 @@ def test_bf16_cases_match_oracle(case):
 
 def test_tiny_config_float32():
     dev = gpu_or_skip()
-    c = wl.CONFIGS[1]
+    c = wl.WORKLOADS["tiny_b2"]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len)
     q = wl.draft_queries(c, dev)[:, 0].contiguous()
@@ -91,7 +91,7 @@ def test_tiny_config_float32():
 def test_full_size_sampled():
     """Batch 32 x context 8192, K = 512, in the launch configuration the benchmark uses."""
     dev = gpu_or_skip()
-    c = wl.CONFIGS[2]
+    c = wl.WORKLOADS["b32_ctx8k"]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len)
     q = wl.draft_queries(c, dev)[:, 0].contiguous()

@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
     dev = gpu_or_skip()
-    c = dict(wl.CONFIGS[2], B=64)
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=64)
     B, g, V = c["B"], c["gamma"], c["V"]
     for seed in (31, 32):  # two calls in a row; the second reuses the array the first left behind
         t, d = wl.logits(c, dev, seed=seed)
