@@ -39,6 +39,7 @@ import torch  # noqa: E402
 METRIC = "verified tokens/s/layer and KV-read GB/s (% of GB300 HBM peak) at batch x ctx"
 UNIT = "tokens/s/layer"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_SUSTAINED_TFLOPS = 1700.0
 
 
 def parse_args(argv=None):
@@ -86,6 +87,15 @@ def max_over_ranks(x, world, device):
 
 
 # ------------------------------------------------------------------ peaks and clocks
+def bf16_peak():
+    """Sustained bf16 tensor throughput (TFLOP/s) from MEASURED_PEAKS.json, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return FALLBACK_BF16_SUSTAINED_TFLOPS
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -193,6 +203,8 @@ class Workload:
         self.bytes_draft = float((2 * Hkv * Keff * D * esz).sum())
         # K read once (both scoring passes of a slice share one HBM read) + the gather (K and V rows read and written)
         self.bytes_snap = float((Hkv * L * D * esz).sum() + 4 * Hkv * Keff.sum() * D * esz)
+        # window scores: two contractions of W*G rows x D per key (pass 1 over all L keys, pass 2 over L - W)
+        self.flops_snap = float((2 * self.W * (Hq // Hkv) * D * Hkv * (2 * L - self.W)).sum())
         self.bytes_spec = float(B * (2 * self.gamma + 1) * self.V * 4)
         # SnapKV (one-read scorer + select), gamma x (draft attention + one-row draw), verify,
         # rejection sample (statistics and finish)
@@ -470,7 +482,9 @@ def run_ours(args):
                                  "verified_tokens_per_s_per_layer": tokens / (verify_ms / 1e3)},
             "draft_attention": {"ms_per_launch_back_to_back": draft_alone_ms, "kv_gbs": draft_gbs,
                                 "frac_of_peak": draft_gbs / peak, "ms_per_step_all_gamma_incl_draw": draft_ms},
-            "snapkv_select": {"ms": snap_ms, "kv_gbs": w.bytes_snap / (snap_ms / 1e3) / 1e9},
+            "snapkv_select": {"ms": snap_ms, "kv_gbs": w.bytes_snap / (snap_ms / 1e3) / 1e9,
+                              "score_tflops": w.flops_snap / (snap_ms / 1e3) / 1e12,
+                              "score_frac_of_bf16_sustained": w.flops_snap / (snap_ms / 1e3) / 1e12 / bf16_peak()},
             "rejection_sample": {"ms": spec_ms, "gbs": w.bytes_spec / (spec_ms / 1e3) / 1e9},
         },
         "speedup_model": speedup_model(decode_ms, verify_ms, draft_alone_ms, snap_ms, w.gamma),
