@@ -168,7 +168,32 @@ __global__ void __launch_bounds__(kStatThreads) spec_draw_row_kernel(const float
     __threadfence();
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {  // the slice holding u * Z (float exponentials, double sums)
+  if (warp == 0 && sp.nsplit <= 32) {
+    // the slice holding u * Z: every slice's (max, sum) loaded at once, one per
+    // lane; float exponentials, double prefix sums across the lanes
+    const float2 v = (lane < sp.nsplit) ? __ldcg(st_b + lane) : make_float2(-INFINITY, 0.f);
+    float M = v.x;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const double ts = (lane < sp.nsplit) ? static_cast<double>(v.y * exp2f((v.x - M) * kLog2e)) : 0.0;
+    double incl = ts;
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const double Z = __shfl_sync(0xffffffffu, incl, 31);
+    const double tgt = static_cast<double>(u[(static_cast<size_t>(b) * (sp.gamma + 1) + row) * 3 + 0]) * Z;
+    const unsigned hit = __ballot_sync(0xffffffffu, ts > 0.0 && incl > tgt);  // run + ts > tgt, run = incl - ts
+    const unsigned mass = __ballot_sync(0xffffffffu, lane < sp.nsplit && v.y > 0.f);
+    const int pick = hit ? (__ffs(hit) - 1) : (mass ? 31 - __clz(mass) : -1);
+    const double run = __shfl_sync(0xffffffffu, incl - ts, pick < 0 ? 0 : pick);
+    if (lane == 0) {
+      s_M = M;
+      s_slice = pick;
+      s_pre = hit ? tgt - run : -1.0;  // rounding pushed u * Z past the total: the last slice with mass, its end
+      s_tidx = 0x7fffffff;
+      s_lastpos = -1;
+    }
+  } else if (threadIdx.x == 0 && sp.nsplit > 32) {  // the same, one slice at a time
     float M = -INFINITY;
     for (int q = 0; q < sp.nsplit; ++q) M = fmaxf(M, __ldcg(&st_b[q].x));
     double Z = 0.0;
