@@ -89,7 +89,8 @@ def test_bf16_cases_match_oracle(case):
             _check_pair(res, k, v, b, h, lens[b], W, P, K, s[b, h], D)
 
 
-@pytest.mark.parametrize("name,seed", [("b32_ctx8k", 2), ("b128_ctx32k", 3), ("ragged_b256_ctx4k_64k", 4)])
+@pytest.mark.parametrize("name,seed", [("b32_ctx8k", 2), ("b128_ctx32k", 3), ("ragged_b256_ctx4k_64k", 4)],
+                         ids=["b32_ctx8k", "b128_ctx32k", "ragged_b256_ctx4k_64k"])
 def test_full_size_sampled(name, seed):
     """Full-size workloads (including ragged lengths 4k-64k at batch 256) with sampled pairs:
     the first, the last, the longest sequence's and one random (sequence, KV head)."""
