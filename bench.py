@@ -549,6 +549,19 @@ def run_round(args):
     ms = max_over_ranks(s.elapsed_time(e), world, dev) / args.steps
     nacc = r.nacc.double()
     committed = float((nacc + 1).mean())
+    # the two phases of a round timed on their own (proposal; verification and correction)
+    phase_ms = [None, None]
+    if graph is True:
+        for i, g in enumerate(r.capture_phases()):
+            for _ in range(2):
+                g.replay()
+            torch.cuda.synchronize()
+            s.record()
+            for _ in range(args.steps):
+                g.replay()
+            e.record()
+            torch.cuda.synchronize()
+            phase_ms[i] = s.elapsed_time(e) / args.steps
     tokens = r.B * r.T
     peak, peak_kind = hbm_peak()
     attn_bytes = r.bytes_verify + r.bytes_draft
@@ -564,6 +577,8 @@ def run_round(args):
                    "parallelism": "weak: one full batch per GPU"},
         "round": {"committed_tokens_per_s": world * r.B * committed / (ms / 1e3),
                   "mean_tokens_per_round": committed, "omega_expected_at_alpha_0.9": 3.439,
+                  "ms_per_committed_token": ms / committed,
+                  "proposal_ms": phase_ms[0], "verify_and_correction_ms": phase_ms[1],
                   "attention_kv_gbs": attn_bytes / (ms / 1e3) / 1e9,
                   "attention_frac_of_peak": attn_bytes / (ms / 1e3) / 1e9 / peak, "peak_kind": peak_kind},
         "gpu_launches": r.launches * args.steps,
@@ -590,7 +605,10 @@ def speedup_model(t_decode, t_verify, t_draft, t_select, gamma):
         out["alpha_%.1f" % alpha] = {
             "omega": om,
             "speedup_selection_amortised": t_decode * om / (gamma * t_draft + t_verify),
-            "speedup_selection_every_round": t_decode * om / (t_select + gamma * t_draft + t_verify)}
+            "speedup_selection_every_round": t_decode * om / (t_select + gamma * t_draft + t_verify),
+            # T_SD per round and per generated token (T_SD / Omega), attention only, selection amortised
+            "round_ms": gamma * t_draft + t_verify,
+            "ms_per_token": (gamma * t_draft + t_verify) / om}
     return out
 
 

@@ -78,18 +78,26 @@ class SpeculationRound:
         """Kernels of this library launched per round."""
         return self.gamma * self.layers + self.gamma + self.layers + 2  # one-row draws: 1 kernel; sampling: 2
 
-    def run(self):
+    def propose(self):
+        """The draft phase: gamma x (draft attention over every layer's compacted cache, one draw)."""
         for s in range(self.gamma):
             for layer in range(self.layers):
                 sel = self.sel[layer]
                 ops.draft_attn(self.qd[layer][s], sel["k_draft"], sel["v_draft"], sel["draft_len"],
                                ws=self.ws_draft, out=self.dout[layer, s], lse=self.dlse)
             ops.draft_draw(self.d, self.u, draft_tokens=self.tok, row=s, ws=self.ws_spec)
+
+    def verify_and_sample(self):
+        """Verify attention over every layer's full cache, then rejection sampling."""
         for layer in range(self.layers):
             ops.verify_attn(self.q[layer], self.k[layer], self.v[layer], self.kv_len_d, ws=self.ws_verify,
                             out=self.vout[layer], lse=self.vlse)
         ops.rejection_sample(self.t, self.d, self.tok, self.u, ws=self.ws_spec, out_tokens=self.out_tok,
                              num_accepted=self.nacc)
+
+    def run(self):
+        self.propose()
+        self.verify_and_sample()
 
     def capture(self):
         """Record one round in a CUDA graph (after an eager warm-up run)."""
@@ -100,6 +108,18 @@ class SpeculationRound:
             self.run()
         self.graph = g
         return g
+
+    def capture_phases(self):
+        """Record the two phases of a round in graphs of their own, for timing each."""
+        graphs = []
+        for fn in (self.propose, self.verify_and_sample):
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            graphs.append(g)
+        return graphs
 
     def replay(self):
         if self.graph is None:
