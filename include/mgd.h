@@ -59,7 +59,7 @@ typedef enum {
 
 /* Bits of the device error word (see mgd_workspace_errors). */
 #define MGD_DEVERR_KV_LEN   0x1u   /* kv_len[b] < T, or > kv_cap; or draft_len[b] < 1 or > k_cap */
-#define MGD_DEVERR_SNAP_LEN 0x2u   /* kv_len[b] < W or > kv_cap in mgd_snapkv_select */
+#define MGD_DEVERR_SNAP_LEN 0x2u   /* kv_len[b] < W or > kv_cap in mgd_snapkv_select; or a budget outside [W, draft_cap] */
 #define MGD_DEVERR_TOKEN    0x4u   /* a draft token id outside [0, V) */
 #define MGD_DEVERR_TIMEOUT  0x8u   /* a bounded wait inside a kernel gave up (never expected) */
 #define MGD_DEVERR_COMMIT   0x10u  /* mgd_commit_round: num_accepted, kv_len or draft_len out of range */
@@ -176,6 +176,24 @@ mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, co
                              int32_t *sel_idx, void *k_draft, void *v_draft, int draft_cap,
                              int32_t *draft_len, float *scores,
                              void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The same selection with a budget per sequence ([MagicDec] section 4.3: in a
+ * batch of mixed lengths each sequence may have its own KV budget): step 3
+ * keeps K_eff = min(budgets[b], kv_len[b]) rows of sequence b.
+ *   budgets  [B] int32 device memory, W <= budgets[b] <= draft_cap; a
+ *            sequence whose budget is outside that range is skipped
+ *            (sel_idx -1, draft_len 0) and raises MGD_DEVERR_SNAP_LEN.
+ * Every other argument, the workspace size and the errors are those of
+ * mgd_snapkv_select; host check: draft_cap >= W, budgets not NULL when B > 0.
+ */
+mgd_status mgd_snapkv_select_budgets(const void *q_win, const void *k, const void *v, const int32_t *kv_len,
+                                     int B, int Hq, int Hkv, int D, int kv_cap,
+                                     int64_t kv_batch_stride, int64_t kv_head_stride,
+                                     int W, int pool, const int32_t *budgets, float sm_scale, mgd_dtype in_dtype,
+                                     int32_t *sel_idx, void *k_draft, void *v_draft, int draft_cap,
+                                     int32_t *draft_len, float *scores,
+                                     void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------ *
  * Speculative sampling.  [SD-Serving] "Eine Verifizierungsrunde verstehen":

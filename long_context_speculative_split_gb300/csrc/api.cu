@@ -232,11 +232,13 @@ size_t mgd_snapkv_workspace_size(int B, int Hq, int Hkv, int D, int kv_cap, int 
   return plan_snapkv(B, Hq, Hkv, D, kv_cap, W).ws_bytes;
 }
 
-mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, const int32_t *kv_len, int B, int Hq,
+// SnapKV selection with one budget K for every sequence (budgets == nullptr)
+// or a per-sequence budget array on the device.
+static mgd_status run_snapkv(const void *q_win, const void *k, const void *v, const int32_t *kv_len, int B, int Hq,
                              int Hkv, int D, int kv_cap, int64_t kv_batch_stride, int64_t kv_head_stride, int W,
-                             int pool, int K, float sm_scale, mgd_dtype in_dtype, int32_t *sel_idx, void *k_draft,
-                             void *v_draft, int draft_cap, int32_t *draft_len, float *scores, void *ws,
-                             size_t ws_bytes, void *stream) {
+                             int pool, int K, const int32_t *budgets, float sm_scale, mgd_dtype in_dtype,
+                             int32_t *sel_idx, void *k_draft, void *v_draft, int draft_cap, int32_t *draft_len,
+                             float *scores, void *ws, size_t ws_bytes, void *stream) {
   if (B < 0) return fail(MGD_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
   if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
     return fail(MGD_ERR_INVALID_ARG, "need Hq >= 1, Hkv >= 1 and Hq %% Hkv == 0 (got %d, %d)", Hq, Hkv);
@@ -244,8 +246,9 @@ mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, co
   if (W < 1 || W > 64) return fail(MGD_ERR_UNSUPPORTED, "window W must be in [1, 64] (got %d)", W);
   if (pool < 1 || pool > 63 || pool % 2 == 0)
     return fail(MGD_ERR_INVALID_ARG, "pool kernel must be odd and in [1, 63] (got %d)", pool);
-  if (K < W) return fail(MGD_ERR_INVALID_ARG, "budget K (%d) must be >= window W (%d)", K, W);
-  if (draft_cap < K) return fail(MGD_ERR_INVALID_ARG, "draft_cap (%d) must be >= K (%d)", draft_cap, K);
+  if (!budgets && K < W) return fail(MGD_ERR_INVALID_ARG, "budget K (%d) must be >= window W (%d)", K, W);
+  if (!budgets && draft_cap < K) return fail(MGD_ERR_INVALID_ARG, "draft_cap (%d) must be >= K (%d)", draft_cap, K);
+  if (budgets && draft_cap < W) return fail(MGD_ERR_INVALID_ARG, "draft_cap (%d) must be >= W (%d)", draft_cap, W);
   if (kv_cap < 1) return fail(MGD_ERR_INVALID_ARG, "kv_cap must be >= 1");
   if (in_dtype != MGD_BF16 && in_dtype != MGD_F32) return fail(MGD_ERR_INVALID_ARG, "bad in_dtype %d", in_dtype);
   if (kv_head_stride < static_cast<int64_t>(kv_cap) * D)
@@ -270,7 +273,8 @@ mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, co
   a.kv_batch_stride = kv_batch_stride;
   a.kv_head_stride = kv_head_stride;
   a.pool = pool;
-  a.K = K;
+  a.K = budgets ? draft_cap : K;
+  a.budgets = budgets;
   a.draft_cap = draft_cap;
   a.sm_scale = sm_scale;
   a.sel_idx = sel_idx;
@@ -292,6 +296,27 @@ mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, co
     e = launch_snapkv(plan, a, 1, nullptr, nullptr);
   }
   return e == cudaSuccess ? ok() : cuda_fail(e, "snapkv launch");
+}
+
+mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, const int32_t *kv_len, int B, int Hq,
+                             int Hkv, int D, int kv_cap, int64_t kv_batch_stride, int64_t kv_head_stride, int W,
+                             int pool, int K, float sm_scale, mgd_dtype in_dtype, int32_t *sel_idx, void *k_draft,
+                             void *v_draft, int draft_cap, int32_t *draft_len, float *scores, void *ws,
+                             size_t ws_bytes, void *stream) {
+  return run_snapkv(q_win, k, v, kv_len, B, Hq, Hkv, D, kv_cap, kv_batch_stride, kv_head_stride, W, pool, K, nullptr,
+                    sm_scale, in_dtype, sel_idx, k_draft, v_draft, draft_cap, draft_len, scores, ws, ws_bytes, stream);
+}
+
+mgd_status mgd_snapkv_select_budgets(const void *q_win, const void *k, const void *v, const int32_t *kv_len, int B,
+                                     int Hq, int Hkv, int D, int kv_cap, int64_t kv_batch_stride,
+                                     int64_t kv_head_stride, int W, int pool, const int32_t *budgets, float sm_scale,
+                                     mgd_dtype in_dtype, int32_t *sel_idx, void *k_draft, void *v_draft,
+                                     int draft_cap, int32_t *draft_len, float *scores, void *ws, size_t ws_bytes,
+                                     void *stream) {
+  if (B > 0 && !budgets) return fail(MGD_ERR_INVALID_ARG, "null budgets");
+  return run_snapkv(q_win, k, v, kv_len, B, Hq, Hkv, D, kv_cap, kv_batch_stride, kv_head_stride, W, pool, W,
+                    B > 0 ? budgets : nullptr, sm_scale, in_dtype, sel_idx, k_draft, v_draft, draft_cap, draft_len,
+                    scores, ws, ws_bytes, stream);
 }
 
 size_t mgd_topk_draft_workspace_size(int B, int Hq, int Hkv, int D, int kv_cap, int draft_cap) {

@@ -100,6 +100,7 @@ struct SnapArgs {
   const int32_t *kv_len;
   int64_t kv_batch_stride, kv_head_stride;
   int pool, K, draft_cap;
+  const int32_t *budgets;  // nullable: per-sequence budgets K_b [B] (device), replacing K
   float sm_scale;
   int32_t *sel_idx;
   void *k_draft;

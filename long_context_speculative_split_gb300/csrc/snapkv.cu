@@ -671,6 +671,7 @@ constexpr int kCompactLoads = 4;    // 32-position rows in flight per warp in th
 struct SelParams {
   int Hkv, W, pool, K, kv_cap, draft_cap, row_bytes;
   int64_t bstride_bytes, hstride_bytes;
+  const int32_t *Kb;  // per-sequence budgets (device), or null for K everywhere
 };
 
 // Exclusive block scan of one unsigned per thread (kSelThreads threads); returns
@@ -714,9 +715,10 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
   const int b = blockIdx.x / sp.Hkv, hkv = blockIdx.x % sp.Hkv;
   const int L = kv_len[b];
+  const int Kb = sp.Kb ? sp.Kb[b] : sp.K;  // this sequence's budget (MagicDec notes, section 4.3)
   const size_t pr = static_cast<size_t>(b) * sp.Hkv + hkv;
   int32_t *sel = sel_idx + pr * sp.draft_cap;
-  if (L < sp.W || L > sp.kv_cap) {
+  if (L < sp.W || L > sp.kv_cap || Kb < sp.W || Kb > sp.draft_cap) {
     for (int i = threadIdx.x; i < sp.draft_cap; i += kSelThreads) sel[i] = -1;
     if (threadIdx.x == 0 && hkv == 0) {
       draft_len[b] = 0;
@@ -727,7 +729,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   const float *s = reinterpret_cast<const float *>(ws + off_scores) + pr * sp.kv_cap;
   float *pooled = reinterpret_cast<float *>(ws + off_pooled) + pr * sp.kv_cap;
   const int n = L - sp.W;
-  const int Keff = min(sp.K, L);
+  const int Keff = min(Kb, L);
   const int ktop = Keff - sp.W;
   const int r = sp.pool / 2;
 
@@ -1089,6 +1091,7 @@ cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, cons
   sp.W = p.W;
   sp.pool = a.pool;
   sp.K = a.K;
+  sp.Kb = a.budgets;
   sp.kv_cap = p.kv_cap;
   sp.draft_cap = a.draft_cap;
   sp.row_bytes = p.D * (in_f32 ? 4 : 2);

@@ -38,6 +38,8 @@ SIGNATURES = {
     "mgd_snapkv_workspace_size": (_sz, [_i32] * 6),
     "mgd_snapkv_select": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _i32, _i32,
                                  _f32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "mgd_snapkv_select_budgets": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _i32,
+                                         _vp, _f32, _i32, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "mgd_topk_draft_workspace_size": (_sz, [_i32] * 6),
     "mgd_topk_draft_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _f32, _i32,
                                    _vp, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp]),
@@ -179,6 +181,15 @@ def mgd_snapkv_select(q_win, k, v, kv_len, B, Hq, Hkv, D, kv_cap, kv_batch_strid
                                     kv_batch_stride, kv_head_stride, W, pool, K, sm_scale, in_dtype,
                                     _ptr(sel_idx), _ptr(k_draft), _ptr(v_draft), draft_cap, _ptr(draft_len),
                                     _ptr(scores), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def mgd_snapkv_select_budgets(q_win, k, v, kv_len, B, Hq, Hkv, D, kv_cap, kv_batch_stride, kv_head_stride, W, pool,
+                              budgets, sm_scale, in_dtype, sel_idx, k_draft, v_draft, draft_cap, draft_len, scores, ws,
+                              ws_bytes, stream=None):
+    _check(load().mgd_snapkv_select_budgets(_ptr(q_win), _ptr(k), _ptr(v), _ptr(kv_len), B, Hq, Hkv, D, kv_cap,
+                                            kv_batch_stride, kv_head_stride, W, pool, _ptr(budgets), sm_scale,
+                                            in_dtype, _ptr(sel_idx), _ptr(k_draft), _ptr(v_draft), draft_cap,
+                                            _ptr(draft_len), _ptr(scores), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def mgd_spec_workspace_size(B, gamma, V):

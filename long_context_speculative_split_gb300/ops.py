@@ -70,11 +70,15 @@ def draft_attn(q, k_draft, v_draft, draft_len, sm_scale=None, out_dtype=torch.fl
 def snapkv_select(q_win, k, v, kv_len, W, pool, K, draft_cap=None, sm_scale=None, ws=None, want_scores=False,
                   out=None, stream=None):
     """Returns dict(sel_idx [B,Hkv,draft_cap] int32, k_draft, v_draft [B,Hkv,draft_cap,D], draft_len [B],
-    scores [B,Hkv,kv_cap] float32 or None)."""
+    scores [B,Hkv,kv_cap] float32 or None).  K is one budget for every sequence, or an int32 device tensor
+    [B] of per-sequence budgets (then draft_cap is required)."""
     B, Wq, Hq, D = q_win.shape
     assert Wq == W
     Hkv, cap = k.shape[1], k.shape[2]
     sb, sh = _kv_strides(k, v, D)
+    per_seq = torch.is_tensor(K)
+    if per_seq and draft_cap is None:
+        raise ValueError("per-sequence budgets need an explicit draft_cap")
     cap_d = K if draft_cap is None else draft_cap
     scale = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
     dev = q_win.device
@@ -87,9 +91,14 @@ def snapkv_select(q_win, k, v, kv_len, W, pool, K, draft_cap=None, sm_scale=None
     need = mgd.mgd_snapkv_workspace_size(B, Hq, Hkv, D, cap, W)
     if ws is None:
         ws = workspace(need, dev)
-    mgd.mgd_snapkv_select(q_win, k, v, kv_len, B, Hq, Hkv, D, cap, sb, sh, W, pool, K, scale, _dtype_code(k),
-                          out["sel_idx"], out["k_draft"], out["v_draft"], cap_d, out["draft_len"], out["scores"],
-                          ws, ws.numel(), stream)
+    if per_seq:
+        mgd.mgd_snapkv_select_budgets(q_win, k, v, kv_len, B, Hq, Hkv, D, cap, sb, sh, W, pool, K, scale,
+                                      _dtype_code(k), out["sel_idx"], out["k_draft"], out["v_draft"], cap_d,
+                                      out["draft_len"], out["scores"], ws, ws.numel(), stream)
+    else:
+        mgd.mgd_snapkv_select(q_win, k, v, kv_len, B, Hq, Hkv, D, cap, sb, sh, W, pool, K, scale, _dtype_code(k),
+                              out["sel_idx"], out["k_draft"], out["v_draft"], cap_d, out["draft_len"], out["scores"],
+                              ws, ws.numel(), stream)
     return out
 
 

@@ -159,6 +159,26 @@ def test_spec_sample_rejects_bad_arguments_on_host(lib):
     assert call(B=0, draft_logits=None) == 0
 
 
+def test_snapkv_budgets_rejects_bad_arguments_on_host(lib):
+    from long_context_speculative_split_gb300 import mgd
+
+    def call(**kw):
+        a = dict(q_win=FAKE, k=FAKE, v=FAKE, kv_len=FAKE, B=2, Hq=8, Hkv=2, D=128, kv_cap=1024,
+                 kv_batch_stride=2 * 1024 * 128, kv_head_stride=1024 * 128, W=32, pool=7, budgets=FAKE, sm_scale=0.1,
+                 in_dtype=0, sel_idx=FAKE, k_draft=FAKE, v_draft=FAKE, draft_cap=256, draft_len=FAKE, scores=None,
+                 ws=FAKE, ws_bytes=8, stream=0)
+        a.update(kw)
+        try:
+            mgd.mgd_snapkv_select_budgets(**a)
+            return 0
+        except mgd.MgdError as e:
+            return e.status
+    assert call(budgets=None) == 1
+    assert call(draft_cap=16) == 1               # below the window
+    assert call(ws_bytes=8) == 3                 # the workspace of mgd_snapkv_select
+    assert call(B=0, budgets=None) == 0
+
+
 def test_selftest_rejects_bad_arguments_on_host(lib):
     from long_context_speculative_split_gb300 import mgd
 

@@ -112,3 +112,29 @@ def test_full_size_sampled(name, seed):
         _check_pair(res, k, v, b, h, L, c["W"], c["pool"], c["K"], s[0, 0], c["D"])
     del k, v
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("W,pool,D", [(32, 7, 128), (2, 3, 128), (16, 5, 64)],
+                         ids=["tc05_window128rows", "logit_sums_8rows", "mma_sync_D64"])
+def test_per_sequence_budgets(W, pool, D):
+    """MagicDec notes, section 4.3: every sequence keeps K_eff = min(K_b, L_b) rows of its own budget K_b;
+    a budget outside [W, draft_cap] skips that sequence (flagged) and leaves the others intact."""
+    dev = gpu_or_skip()
+    lens = [3000, 2000, 500, 40, 1500]
+    B, Hq, Hkv, cap, dcap = len(lens), 32, 8, 3000, 1024
+    budgets = [512, W + 32, 1000, 100, W - 1]   # the third and fourth cover their sequence; the last is invalid
+    cfg = dict(B=B, Hq=Hq, Hkv=Hkv, D=D, dtype="bf16", lens=lens, W=W, hh=0.01, gamma=1)
+    kv_len = torch.tensor(lens, dtype=torch.int32)
+    k, v = wl.kv_cache(cfg, dev, seed=8, kv_len=kv_len, cap=cap)
+    qw = wl.window_queries(cfg, dev, seed=8)
+    kb = torch.tensor(budgets, dtype=torch.int32, device=dev)
+    from long_context_speculative_split_gb300 import mgd
+    ws = ops.workspace(mgd.mgd_snapkv_workspace_size(B, Hq, Hkv, D, cap, W), dev)
+    res = ops.snapkv_select(qw, k, v, kv_len.to(dev), W, pool, kb, draft_cap=dcap, ws=ws, want_scores=True)
+    torch.cuda.synchronize()
+    assert mgd.mgd_workspace_errors(ws) == 0x2                      # MGD_DEVERR_SNAP_LEN from the last budget
+    assert int(res["draft_len"][B - 1]) == 0 and bool((res["sel_idx"][B - 1] == -1).all())
+    s = window_scores(qw[:B - 1], k[:B - 1], kv_len[:B - 1], W, 1.0 / math.sqrt(D))
+    for b in range(B - 1):
+        for h in range(Hkv):
+            _check_pair(res, k, v, b, h, lens[b], W, pool, budgets[b], s[b, h], D)
