@@ -54,10 +54,15 @@ struct KParams {
   size_t off_tickets, off_part_o, off_part_l;
 };
 
-template <int D>
+template <int D, int NT>
 struct Layout {
   static constexpr int kBoxes = D / 64;
-  static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;  // K boxes then V boxes
+  static constexpr int kKVBytes = 2 * kBoxes * kBoxBytes;  // K boxes then V boxes
+  // With one row tile (at most 8 query rows: the draft pass) the producer also copies a
+  // unit's query rows, unpadded, behind the K/V boxes of the stage holding its first tile.
+  static constexpr int kQSlotBytes = (NT == 1) ? 8 * D * 2 : 0;
+  static constexpr int kStageBytes = kKVBytes + kQSlotBytes;
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
   static constexpr int kOStride = 68;                          // epilogue row stride (64 cols + 4)
   static constexpr int kQStride = D + 8;                       // query row stride in bf16 (16 B pad)
   // One buffer serves two phases of a unit: the bf16 query rows while its tiles
@@ -81,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                    const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ kv_len,
                    float *__restrict__ out_f32, __nv_bfloat16 *__restrict__ out_bf16, float *__restrict__ lse_out,
                    unsigned char *__restrict__ ws, KParams p) {
-  using Lay = Layout<D>;
+  using Lay = Layout<D, NT>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float *sm_O = reinterpret_cast<float *>(smem + Lay::off_epi);
@@ -122,8 +127,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    bool first = true;
     while (ok) {
-      const unsigned u = atomicAdd(&hdr->next_unit, 1u);
+      // every CTA's first unit is its own index (no counter round trip before the first
+      // load); later units come from the counter
+      const unsigned u = first ? blockIdx.x : gridDim.x + atomicAdd(&hdr->next_unit, 1u);
+      first = false;
       if (u >= p.total_units) break;
       const int pair = static_cast<int>(u) / p.nchunk;
       const int chunk = static_cast<int>(u) % p.nchunk;
@@ -139,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       if (start >= L) continue;
       const int end = min(start + p.C, L);
       const int ntiles = (end - start + kTileKeys - 1) / kTileKeys;
-      {  // warm L2 with this unit's query rows; the consumers load them at its first tile
+      if (NT > 1) {  // warm L2 with this unit's query rows; the consumers load them at its first tile
         const int rg = pair % p.RG;
         const int r_hi = min(p.rows, rg * 32 + 32);
         for (int qg = rg * 32; qg < r_hi; ++qg) {
@@ -155,8 +164,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
           break;
         }
         meta[stage] = TileMeta{static_cast<int>(u), t, ntiles, L};
-        mbar_arrive_expect_tx(&full[stage], Lay::kStageBytes);
+        const uint32_t qbytes = (Lay::kQSlotBytes > 0 && t == 0) ? static_cast<uint32_t>(p.rows * D * 2) : 0u;
+        mbar_arrive_expect_tx(&full[stage], Lay::kKVBytes + qbytes);
         unsigned char *st = smem + stage * Lay::kStageBytes;
+        if (qbytes) {  // rows ordered (t, g) like the row index qg = t * G + g
+          for (int r = 0; r < p.rows; ++r)
+            bulk_load(st + Lay::kKVBytes + r * D * 2,
+                      q + ((static_cast<size_t>(b) * p.T + r / p.G) * p.Hq + hkv * p.G + r % p.G) * D, D * 2,
+                      &full[stage]);
+        }
         const int row = start + t * kTileKeys;
 #pragma unroll
         for (int h = 0; h < Lay::kBoxes; ++h) tma_load_4d(st + h * kBoxBytes, &kmap, &full[stage], h * 64, row, hkv, b);
@@ -208,18 +224,39 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int start = chunk * p.C;
 
     if (md.tile == 0) {
-      // ---- new unit: stage its 32 query rows (zero padded) in shared memory for
-      //      the B operand of S^T = K Q^T, and reset the running state
-      for (int i = threadIdx.x; i < 32 * (D / 8); i += kConsumerWarps * 32) {
-        const int r = i / (D / 8), c = i % (D / 8);
-        const int qg = rg * 32 + r;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (qg < p.rows) {
-          const int t = qg / p.G, g = qg % p.G;
-          val = *reinterpret_cast<const uint4 *>(q + ((static_cast<size_t>(b) * p.T + t) * p.Hq + hkv * p.G + g) * D +
-                                                 8 * c);
+      // ---- new unit: stage its query rows (zero padded) in shared memory for the
+      //      B operand of S^T = K Q^T, and reset the running state
+      if constexpr (NT == 1) {
+        // rows 0..15 (the ldmatrix.x4 of the QK loop reads two n8 tiles) from the
+        // stage's query slot
+        const unsigned char *qs = smem + stage * Lay::kStageBytes + Lay::kKVBytes;
+        for (int i = threadIdx.x; i < 16 * (D / 8); i += kConsumerWarps * 32) {
+          const int r = i / (D / 8), c = i % (D / 8);
+          uint4 val = make_uint4(0u, 0u, 0u, 0u);
+          if (r < p.rows) val = *reinterpret_cast<const uint4 *>(qs + r * D * 2 + 16 * c);
+          *reinterpret_cast<uint4 *>(sQ + r * Lay::kQStride + 8 * c) = val;
         }
-        *reinterpret_cast<uint4 *>(sQ + r * Lay::kQStride + 8 * c) = val;
+      } else {
+        // 32 rows from global memory: every load of this thread first, then the stores
+        constexpr int kPer = 32 * (D / 8) / (kConsumerWarps * 32);
+        uint4 val[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int i = threadIdx.x + k * kConsumerWarps * 32;
+          const int r = i / (D / 8), c = i % (D / 8);
+          const int qg = rg * 32 + r;
+          val[k] = make_uint4(0u, 0u, 0u, 0u);
+          if (qg < p.rows) {
+            const int t = qg / p.G, g = qg % p.G;
+            val[k] = *reinterpret_cast<const uint4 *>(
+                q + ((static_cast<size_t>(b) * p.T + t) * p.Hq + hkv * p.G + g) * D + 8 * c);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int i = threadIdx.x + k * kConsumerWarps * 32;
+          *reinterpret_cast<uint4 *>(sQ + (i / (D / 8)) * Lay::kQStride + 8 * (i % (D / 8))) = val[k];
+        }
       }
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
@@ -383,27 +420,51 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int nch_b = (L + p.C - 1) / p.C;
     const bool single = (nch_b == 1);
     const size_t part_base = (static_cast<size_t>(pair) * p.nchunk + chunk) * 32;
+    // The 4 warps' scaled accumulators meet in kSlices slices of 8*NT rows (as many as the
+    // 32-row buffer holds): the warps of round 0 store their slice, later rounds add into
+    // it in turn, and the write-out sums the slices -- no shared-memory atomics.
+    constexpr int kSlices = (NT == 1) ? 4 : (NT == 2) ? 2 : 1;
+    constexpr int kRounds = kConsumerWarps / kSlices;
+    float *my_slice = sm_O + (warp % kSlices) * (8 * NT) * Lay::kOStride;
+#pragma unroll
     for (int dh = 0; dh < D / 64; ++dh) {
-      for (int i = threadIdx.x; i < 32 * Lay::kOStride; i += kConsumerWarps * 32) sm_O[i] = 0.f;
-      named_bar(1, kConsumerWarps * 32);
 #pragma unroll
-      for (int mm = 0; mm < 4; ++mm) {
-        const int mt = dh * 4 + mm;
+      for (int rd = 0; rd < kRounds; ++rd) {
+        if (warp / kSlices == rd) {
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
+          for (int mm = 0; mm < 4; ++mm) {
+            const int mt = dh * 4 + mm;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int r = 8 * j + 2 * tig + e;
-            atomicAdd(&sm_O[r * Lay::kOStride + 16 * mm + gid], acc[mt][j][e] * f[j][e]);
-            atomicAdd(&sm_O[r * Lay::kOStride + 16 * mm + gid + 8], acc[mt][j][2 + e] * f[j][e]);
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                float *o0 = my_slice + (8 * j + 2 * tig + e) * Lay::kOStride + 16 * mm + gid;
+                const float v0 = acc[mt][j][e] * f[j][e], v1 = acc[mt][j][2 + e] * f[j][e];
+                if (rd == 0) {
+                  o0[0] = v0;
+                  o0[8] = v1;
+                } else {
+                  o0[0] += v0;
+                  o0[8] += v1;
+                }
+              }
           }
+        }
+        named_bar(1, kConsumerWarps * 32);
       }
-      named_bar(1, kConsumerWarps * 32);
       for (int i = threadIdx.x; i < rows_valid * 16; i += kConsumerWarps * 32) {
         const int r = i >> 4, dq = i & 15;
         const float Lt = sm_rowL[r];
         const float inv = (Lt > 0.f) ? 1.f / Lt : 0.f;
         float4 o = *reinterpret_cast<const float4 *>(&sm_O[r * Lay::kOStride + 4 * dq]);
+#pragma unroll
+        for (int sl = 1; sl < kSlices; ++sl) {
+          const float4 x = *reinterpret_cast<const float4 *>(&sm_O[(sl * 8 * NT + r) * Lay::kOStride + 4 * dq]);
+          o.x += x.x;
+          o.y += x.y;
+          o.z += x.z;
+          o.w += x.w;
+        }
         o.x *= inv;
         o.y *= inv;
         o.z *= inv;
@@ -505,7 +566,7 @@ template <int D, int NT>
 cudaError_t launch_one(const AttnPlan &pl, const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap) {
   constexpr int MINB = (NT <= 3) ? 2 : 1;
   auto kern = attn_tc_kernel<D, NT, MINB>;
-  const int smem = Layout<D>::alloc;
+  const int smem = Layout<D, NT>::alloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -525,7 +586,13 @@ cudaError_t launch_one(const AttnPlan &pl, const AttnArgs &a, const CUtensorMap 
   kp.off_tickets = pl.off_tickets;
   kp.off_part_o = pl.off_part_o;
   kp.off_part_l = pl.off_part_l;
-  int grid = pl.grid;
+  // one persistent CTA per resident slot (MINB per SM unless shared memory allows fewer)
+  static const int resident = [&] {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, smem) != cudaSuccess) nb = MINB;
+    return std::max(1, std::min(nb, MINB));
+  }();
+  int grid = pl.grid / MINB * resident;
   if (static_cast<unsigned>(grid) > kp.total_units) grid = static_cast<int>(kp.total_units);
   kern<<<grid, kThreads, smem, a.stream>>>(kmap, vmap, static_cast<const __nv_bfloat16 *>(a.q), a.kv_len,
                                            a.out_bf16 ? nullptr : static_cast<float *>(a.out),

@@ -124,6 +124,14 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
 }
 // L2 eviction-priority policies for loads that carry a cache hint: evict_last
 // for data the CTA will read again soon, evict_first for a last read.
+// One-dimensional bulk copy global -> shared memory through the TMA unit: both addresses
+// 16-byte aligned, `bytes` a multiple of 16; completes as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
