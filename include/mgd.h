@@ -15,6 +15,14 @@
  *     device.  The library never allocates device memory; scratch space is
  *     the caller's `ws` buffer of at least the size the matching
  *     mgd_*_workspace_size() returns for the same shape.
+ *   - A workspace is ZERO-FILLED once before its first use (e.g. one
+ *     cudaMemsetAsync after allocating it).  The attention calls
+ *     (mgd_verify_attn, mgd_draft_attn) do not clear its header per call:
+ *     their kernels leave the counters at zero for the next call, which saves
+ *     a clearing launch ahead of every attention launch.  The other calls
+ *     clear the part they use themselves.  A buffer that served as scratch for
+ *     anything but attention calls is zero-filled again before an attention
+ *     call uses it.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous on that stream; nothing synchronises.
  *   - Shape / argument errors are detected on the host before anything is
@@ -24,7 +32,8 @@
  *   - Values that live on the device (kv_len, draft_len, token ids) cannot be
  *     checked on the host.  Kernels that meet an out-of-range device value skip
  *     that sequence (its outputs are unspecified) and set a bit in the error
- *     word kept at the start of `ws`; mgd_workspace_errors() reads it back.
+ *     word kept at the start of `ws` (two 32-bit words whose OR is the
+ *     call's bits); mgd_workspace_errors() reads it back.
  *   - Element strides are in elements, layouts are row-major, the innermost
  *     dimension (D or V) is contiguous.  Every device pointer must be 16-byte
  *     aligned and bf16 KV strides must be multiples of 8 elements (the K/V

@@ -184,12 +184,12 @@ int mgd_version(void) { return 100; }
 
 mgd_status mgd_workspace_errors(const void *ws, void *stream, uint32_t *flags) {
   if (!ws || !flags) return fail(MGD_ERR_INVALID_ARG, "null pointer argument");
-  uint32_t v = 0;
+  uint32_t v[2] = {0u, 0u};  // the two error words of the header: the call's bits are their OR
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, st);
+  cudaError_t e = cudaMemcpyAsync(v, ws, sizeof(v), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace error word");
-  *flags = v;
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace error words");
+  *flags = v[0] | v[1];
   return MGD_OK;
 }
 
@@ -342,6 +342,11 @@ mgd_status mgd_topk_draft_attn(const void *q, const void *k, const void *v, cons
                                     sm_scale, in_dtype, sel_idx, k_draft, v_draft, draft_cap, draft_len, nullptr,
                                     ws, ws_sel, stream);
   if (st != MGD_OK || B == 0) return st;
+  // the attention step's header sits at a shape-dependent offset that a call of
+  // another shape may have used as selection scratch: clear it
+  cudaError_t e = cudaMemsetAsync(static_cast<unsigned char *>(ws) + ws_sel, 0, kAlign,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the attention header");
   const int64_t dh = static_cast<int64_t>(draft_cap) * D;
   return mgd_draft_attn(q, k_draft, v_draft, draft_len, B, Hq, Hkv, D, draft_cap, dh * Hkv, dh, sm_scale, in_dtype,
                         out, out_dtype, lse, static_cast<unsigned char *>(ws) + ws_sel, ws_bytes - ws_sel, stream);

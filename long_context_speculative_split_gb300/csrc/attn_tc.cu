@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const int b = bh / p.Hkv;
       const int L = kv_len[b];
       if (L < p.T || L > p.kv_cap) {
-        if (chunk == 0) raise_error(hdr, 0x1u);
+        if (chunk == 0) raise_error_sr(hdr, 0x1u);
         continue;
       }
       const int start = chunk * p.C;
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       }
       for (int t = 0; t < ntiles; ++t) {
         if (!mbar_wait(&empty[stage], phase ^ 1u)) {
-          raise_error(hdr, 0x8u);
+          raise_error_sr(hdr, 0x8u);
           ok = false;
           break;
         }
@@ -189,10 +189,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
       meta[stage].unit = -1;
       mbar_arrive(&full[stage]);
     } else {
-      raise_error(hdr, 0x8u);
+      raise_error_sr(hdr, 0x8u);
       // drain: wait (bounded) for every load still in flight before leaving
       for (int s = 0; s < kStages; ++s) mbar_wait(&full[s], phase);
     }
+    call_check_in(hdr, 2u * gridDim.x);  // this CTA's claims are over
     return;
   }
 
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   uint32_t phase = 0;
   while (true) {
     if (!mbar_wait(&full[stage], phase)) {
-      raise_error(hdr, 0x8u);
+      raise_error_sr(hdr, 0x8u);
       break;
     }
     const TileMeta md = meta[stage];
@@ -498,7 +499,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
     named_bar(1, kConsumerWarps * 32);
     if (threadIdx.x == 0) {
       const unsigned old = atomicAdd(&tickets[pair], 1u);
-      *sm_flag = (old == static_cast<unsigned>(nch_b - 1)) ? 1 : 0;
+      const bool last = (old == static_cast<unsigned>(nch_b - 1));
+      if (last) tickets[pair] = 0u;  // every chunk of the pair has arrived: ready for the next call
+      *sm_flag = last ? 1 : 0;
     }
     named_bar(1, kConsumerWarps * 32);
     if (*sm_flag) {
@@ -560,6 +563,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
       named_bar(1, kConsumerWarps * 32);
     }
   }
+  // every consumer's error bits and merges are done: one check-in for the consumers
+  named_bar(2, kConsumerWarps * 32);
+  if (threadIdx.x == 0) call_check_in(hdr, 2u * gridDim.x);
 }
 
 template <int D, int NT>
@@ -607,9 +613,15 @@ int attn_tc_min_blocks(int NT) { return NT <= 3 ? 2 : 1; }
 
 cudaError_t launch_attention_tc(const AttnPlan &pl, const AttnArgs &a, const CUtensorMap &kmap,
                                 const CUtensorMap &vmap) {
-  const size_t clear = pl.off_part_o;  // header + tickets
-  cudaError_t e = cudaMemsetAsync(a.ws, 0, clear, a.stream);
-  if (e != cudaSuccess) return e;
+  // The header needs no clearing launch: the kernel leaves it ready for the next call
+  // (the workspace is zero-filled before its first use).  The merge tickets of split
+  // sequences are cleared here, since a call of another shape may have written
+  // partial results where this call keeps them.
+  if (pl.nchunk > 1) {
+    cudaError_t e = cudaMemsetAsync(static_cast<unsigned char *>(a.ws) + pl.off_tickets, 0,
+                                    pl.off_part_o - pl.off_tickets, a.stream);
+    if (e != cudaSuccess) return e;
+  }
   if (pl.D == 128) {
     switch (pl.NT) {
       case 1: return launch_one<128, 1>(pl, a, kmap, vmap);

@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "internal.h"
@@ -28,8 +29,35 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // claimed, microseconds apart), so a correct kernel never comes close.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Error bit of a kernel whose launch clears the header first.
 __device__ __forceinline__ void raise_error(WsHeader *hdr, unsigned bit) {
-  atomicOr(&hdr->err, bit);
+  atomicOr(&hdr->err[1], bit);
+}
+
+// Error bit of a self-resetting kernel (no clearing launch before it): the word
+// of this call's parity.  seq changes only after every part of the call checked in.
+__device__ __forceinline__ void raise_error_sr(WsHeader *hdr, unsigned bit) {
+  const unsigned s = *reinterpret_cast<volatile unsigned *>(&hdr->seq);
+  atomicOr(&hdr->err[s & 1u], bit);
+}
+
+// End of one part of a self-resetting call (a thread whose share of the work,
+// its claims from next_unit and its error bits are all done).  The last of
+// `parts` check-ins puts the counters back to zero, clears the error word the
+// next call will use and advances seq, so the workspace is ready for the next
+// call with no clearing launch in between.
+__device__ __forceinline__ void call_check_in(WsHeader *hdr, unsigned parts) {
+  __threadfence();
+  if (atomicAdd(&hdr->done, 1u) == parts - 1u) {
+    __threadfence();
+    volatile unsigned *h = reinterpret_cast<volatile unsigned *>(hdr);
+    const unsigned s = h[offsetof(WsHeader, seq) / 4];
+    h[offsetof(WsHeader, next_unit) / 4] = 0u;
+    h[offsetof(WsHeader, next_unit2) / 4] = 0u;
+    h[offsetof(WsHeader, done) / 4] = 0u;
+    h[(s + 1u) & 1u] = 0u;  // err[(s + 1) & 1]
+    h[offsetof(WsHeader, seq) / 4] = s + 1u;
+  }
 }
 
 // Bounded spin until the counter at p (written by other CTAs) reaches `need`,

@@ -13,10 +13,16 @@ namespace mgd {
 // Every workspace starts with this 256-byte header.  It is cleared at the
 // start of every call (cudaMemsetAsync on the call's stream).
 struct WsHeader {
-  unsigned err;        // OR of MGD_DEVERR_* raised by the call
+  // MGD_DEVERR_* bits.  Kernels that clear the header before they run raise into
+  // err[1].  Kernels that leave the workspace ready for the next call (no clearing
+  // launch) raise into err[seq & 1]; the last CTA to finish clears the other word and
+  // advances seq.  Either way, after a call err[0] | err[1] holds exactly its bits.
+  unsigned err[2];
   unsigned next_unit;  // dynamic work counter of persistent kernels
   unsigned next_unit2;
-  unsigned pad[61];
+  unsigned done;  // end-of-call check-ins of the self-resetting kernels
+  unsigned seq;   // calls completed by the self-resetting kernels on this workspace
+  unsigned pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

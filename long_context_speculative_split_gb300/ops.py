@@ -24,7 +24,8 @@ def _kv_strides(k, v, D):
 
 
 def workspace(nbytes, device):
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    """Zero-filled device scratch (calls that skip clearing it rely on a zero start)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 def verify_attn(q, k, v, kv_len, sm_scale=None, out_dtype=torch.float32, ws=None, out=None, lse=None,

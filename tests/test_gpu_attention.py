@@ -242,3 +242,43 @@ def test_draft_split_units_match_oracle():
     ref, ref_lse = ref_draft(q, k, v, dlen, 1.0 / math.sqrt(D))
     assert_attention_close(out, ref[:, 0])
     assert_lse_close(lse, ref_lse[:, 0])
+
+
+def test_workspace_reused_across_shapes_and_errors():
+    """The attention kernels leave the workspace header ready for the next call (no clearing
+    launch): one zero-filled workspace serves, in turn, a split-sequence verify (merge tickets,
+    claims past the grid), a draft, a verify that raises a device error and the first verify
+    again.  Each result equals the same call on a fresh workspace bit for bit, and each call's
+    error word holds its own bits only."""
+    dev = gpu_or_skip()
+    lens = [int(x) for x in np.random.default_rng(5).integers(1500, 4097, size=40)]
+    qa, ka, va, la = (x.to(dev) for x in _case(40, 4, 32, 8, 128, lens, 4096, seed=21))
+    qd, kd, vd, ld = (x.to(dev) for x in _case(4, 1, 32, 8, 128, [512, 300, 1, 511], 512, seed=22))
+    bad = la.clone()
+    bad[7] = 5000  # past the capacity
+    need = max(mgd.mgd_verify_workspace_size(40, 4, 32, 8, 128, 4096), mgd.mgd_draft_workspace_size(4, 32, 8, 128, 512))
+    ws = ops.workspace(need, dev)
+
+    def verify(kv_len, w):
+        return ops.verify_attn(qa, ka, va, kv_len, ws=w)
+
+    def draft(w):
+        return ops.draft_attn(qd[:, 0], kd, vd, ld, ws=w)
+
+    fresh_v = verify(la, ops.workspace(need, dev))
+    fresh_d = draft(ops.workspace(need, dev))
+    fresh_bad = verify(bad, ops.workspace(need, dev))
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out = verify(la, ws)
+        assert mgd.mgd_workspace_errors(ws) == 0
+        assert torch.equal(out[0], fresh_v[0]) and torch.equal(out[1], fresh_v[1])
+        out = draft(ws)
+        assert mgd.mgd_workspace_errors(ws) == 0
+        assert torch.equal(out[0], fresh_d[0]) and torch.equal(out[1], fresh_d[1])
+        out = verify(bad, ws)
+        assert mgd.mgd_workspace_errors(ws) == mgd.MGD_DEVERR_KV_LEN
+        keep = torch.arange(40, device=dev) != 7
+        assert torch.equal(out[0][keep], fresh_bad[0][keep])
+    ref, _ = ref_attention(qa[:3].cpu(), ka[:3].cpu(), va[:3].cpu(), la[:3].cpu(), 1.0 / math.sqrt(128))
+    assert_attention_close(fresh_v[0][:3], ref)
