@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
       // drain: wait (bounded) for every load still in flight before leaving
       for (int s = 0; s < kStages; ++s) mbar_wait(&full[s], phase);
     }
-    call_check_in(hdr, 2u * gridDim.x);  // this CTA's claims are over
+    // This CTA's claims are over: it checks in (its consumers need not: they claim nothing,
+    // and their only error bits, timeouts, land in one of the two words either way).
+    call_check_in(hdr, gridDim.x);
     return;
   }
 
@@ -563,9 +565,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
       named_bar(1, kConsumerWarps * 32);
     }
   }
-  // every consumer's error bits and merges are done: one check-in for the consumers
-  named_bar(2, kConsumerWarps * 32);
-  if (threadIdx.x == 0) call_check_in(hdr, 2u * gridDim.x);
 }
 
 template <int D, int NT>

@@ -34,18 +34,17 @@ __device__ __forceinline__ void raise_error(WsHeader *hdr, unsigned bit) {
   atomicOr(&hdr->err[1], bit);
 }
 
-// Error bit of a self-resetting kernel (no clearing launch before it): the word
-// of this call's parity.  seq changes only after every part of the call checked in.
+// Error bit of a self-resetting kernel (no clearing launch before it): the word of
+// this call's parity.  seq advances only after every CTA's producer checked in.
 __device__ __forceinline__ void raise_error_sr(WsHeader *hdr, unsigned bit) {
   const unsigned s = *reinterpret_cast<volatile unsigned *>(&hdr->seq);
   atomicOr(&hdr->err[s & 1u], bit);
 }
 
-// End of one part of a self-resetting call (a thread whose share of the work,
-// its claims from next_unit and its error bits are all done).  The last of
-// `parts` check-ins puts the counters back to zero, clears the error word the
-// next call will use and advances seq, so the workspace is ready for the next
-// call with no clearing launch in between.
+// End of one part of a self-resetting call (a thread whose claims from next_unit
+// are all done).  The last of `parts` check-ins puts the counters back to zero,
+// clears the error word the next call will use and advances seq, so the workspace
+// is ready for the next call with no clearing launch in between.
 __device__ __forceinline__ void call_check_in(WsHeader *hdr, unsigned parts) {
   __threadfence();
   if (atomicAdd(&hdr->done, 1u) == parts - 1u) {
