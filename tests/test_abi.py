@@ -200,3 +200,12 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(mgd, "_lib", None)
     with pytest.raises(RuntimeError, match="not found"):
         mgd.load()
+
+
+def test_workspaces_from_the_binding_start_zero_filled():
+    """The attention calls do not clear their workspace per call; they rely on a zero start."""
+    import torch
+    from long_context_speculative_split_gb300 import ops
+    ws = ops.workspace(4096 + 3, "cpu")
+    assert ws.dtype == torch.uint8 and ws.numel() == 4099 and int(ws.count_nonzero()) == 0
+    assert ops.workspace(0, "cpu").numel() == 256
