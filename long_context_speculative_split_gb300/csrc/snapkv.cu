@@ -744,20 +744,26 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   };
   if (r <= kPoolHalo) {
     // tiles of kPoolTile scores staged in shared memory with their halo (every
-    // thread's loads issued together), positions outside the prefix as -inf
-    for (int t0 = 0; t0 < n; t0 += kPoolTile) {
-      const int len = min(kPoolTile, n - t0), cnt = len + 2 * r;
-      __syncthreads();  // the previous tile's readers are done
-      float x[kStageLoads];
+    // thread's loads issued together), positions outside the prefix as -inf; the
+    // next tile's loads are in flight while the current tile is pooled
+    float x[kStageLoads];
+    auto load_tile = [&](int t0) {
+      const int cnt = min(kPoolTile, n - t0) + 2 * r;
 #pragma unroll
       for (int u = 0; u < kStageLoads; ++u) {
         const int i = threadIdx.x + u * kSelThreads, t = t0 - r + i;
         x[u] = (i < cnt && t >= 0 && t < n) ? s[t] : -INFINITY;
       }
+    };
+    if (n > 0) load_tile(0);
+    for (int t0 = 0; t0 < n; t0 += kPoolTile) {
+      const int len = min(kPoolTile, n - t0), cnt = len + 2 * r;
+      __syncthreads();  // the previous tile's readers are done
 #pragma unroll
       for (int u = 0; u < kStageLoads; ++u)
         if (threadIdx.x + u * kSelThreads < cnt) stage[threadIdx.x + u * kSelThreads] = x[u];
       __syncthreads();
+      if (t0 + kPoolTile < n) load_tile(t0 + kPoolTile);
       for (int i = threadIdx.x; i < len; i += kSelThreads) {
         float m = stage[i];
         for (int o = 1; o <= 2 * r; ++o) m = fmaxf(m, stage[i + o]);
