@@ -15,8 +15,9 @@ namespace mgd {
 struct WsHeader {
   // MGD_DEVERR_* bits.  Kernels that clear the header before they run raise into
   // err[1].  Kernels that leave the workspace ready for the next call (no clearing
-  // launch) raise into err[seq & 1]; the last CTA to finish clears the other word and
-  // advances seq.  Either way, after a call err[0] | err[1] holds exactly its bits.
+  // launch) raise into err[seq & 1]; the last CTA to check in clears the other word and
+  // advances seq.  Either way, after a call err[0] | err[1] holds its bits (a consumer's
+  // timeout raised after its CTA checked in shows again after the next call).
   unsigned err[2];
   unsigned next_unit;  // dynamic work counter of persistent kernels
   unsigned next_unit2;
