@@ -275,8 +275,12 @@ mgd_status mgd_streaming_select(const void *k, const void *v, const int32_t *kv_
  *            draft_cap >= K; the draft rows are contiguous)
  *   out      [B, Hq, D] out_dtype;  lse [B, Hq] float32 or NULL (natural log)
  *   ws       mgd_topk_draft_workspace_size(...) bytes
- * Every call reads the whole K cache twice (the probabilities need each
- * query's normaliser over all keys first): that is the selection cost.
+ * Every call reads the whole K cache (the probabilities need each query's
+ * normaliser over all keys first; the first pass keeps the G logits of every
+ * key, which the key sums then read back instead of K): that is the
+ * selection cost.  A sequence with kv_len outside [1, kv_cap] is flagged in
+ * the error word at the start of `ws` (MGD_DEVERR_SNAP_LEN, draft_len 0, no
+ * kept rows); its out and lse rows are unspecified.
  * Supported: D in {64, 128}; in_dtype bf16 or float32; 1 <= K <= draft_cap.
  * ------------------------------------------------------------------------ */
 size_t mgd_topk_draft_workspace_size(int B, int Hq, int Hkv, int D, int kv_cap, int draft_cap);
