@@ -180,7 +180,7 @@ const char *mgd_status_string(mgd_status s) {
 
 const char *mgd_last_error(void) { return g_last_error.c_str(); }
 
-int mgd_version(void) { return 100; }
+int mgd_version(void) { return 200; }  // 0.2.0: per-sequence budgets, self-resetting attention workspaces
 
 mgd_status mgd_workspace_errors(const void *ws, void *stream, uint32_t *flags) {
   if (!ws || !flags) return fail(MGD_ERR_INVALID_ARG, "null pointer argument");
