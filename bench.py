@@ -12,11 +12,13 @@ fraction of the verify kernel are reported beside it.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
 
-With --gpus N > 1 launch under torch.distributed.run: every rank runs the same
-batch on its own GPU (weak scaling, no collective on the data path); the
+With --gpus N > 1 every rank runs one full batch on its own GPU (weak scaling,
+no collective on the data path: the sequences of a batch are independent); the
 timed region is bracketed by barriers and the max over ranks is reported.
---impl reference times the float64 CPU oracle on a bounded sample of the same
-workload (rank 0 only).
+Started without WORLD_SIZE in the environment, `--gpus N` re-launches itself
+under torch.distributed.run with N processes; under a launcher, WORLD_SIZE must
+equal N.  --impl reference times the float64 CPU oracle on a bounded sample of
+the same workload (rank 0 only), spread over the host cores by a process pool.
 """
 import argparse
 import json
@@ -53,8 +55,10 @@ def parse_args(argv=None):
                    help="b128_ctx32k: batch 128 x 32k (default); round_b32_ctx16k_32layers: full 32-layer "
                         "speculation round")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-round", action="store_true",
+                   help="skip the 32-layer round block that the default line carries beside its main workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-sample", type=int, default=1, help="sequences in the oracle sample")
+    p.add_argument("--cpu-sample", type=int, default=8, help="sequences in the oracle sample")
     return p.parse_args(argv)
 
 
@@ -84,6 +88,62 @@ def max_over_ranks(x, world, device):
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def free_port():
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def launch_ranks(n, argv, script=None):
+    """Run `script` (this file by default) with `argv` as n ranks on this node under
+    torch.distributed.run; rank 0 prints the line.  Returns the launcher's exit code."""
+    script = os.path.abspath(__file__) if script is None else script
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), script] + list(argv)
+    return subprocess.call(cmd)
+
+
+def check_world(args, world):
+    if world != args.gpus:
+        raise SystemExit("bench.py: --gpus %d but WORLD_SIZE=%d: launch one rank per GPU" % (args.gpus, world))
+
+
+def run_timed(step, steps, world, device, timer, sync):
+    """The timed region of both GPU arms: a barrier and a device sync on both sides of exactly
+    `steps` calls of step(i), timed by `timer` (start(), stop(), elapsed_ms()) on the launching
+    stream; returns the max over ranks of the per-step time in ms."""
+    barrier(world)
+    sync()
+    timer.start()
+    for i in range(steps):
+        step(i)
+    timer.stop()
+    sync()
+    barrier(world)
+    return max_over_ranks(timer.elapsed_ms(), world, device) / steps
+
+
+class CudaTimer:
+    """CUDA events recorded on the current stream (the stream the library calls launch on)."""
+
+    def __init__(self):
+        self.s = torch.cuda.Event(enable_timing=True)
+        self.e = torch.cuda.Event(enable_timing=True)
+
+    def start(self):
+        self.s.record()
+
+    def stop(self):
+        self.e.record()
+
+    def elapsed_ms(self):
+        self.e.synchronize()
+        return self.s.elapsed_time(self.e)
 
 
 # ------------------------------------------------------------------ peaks and clocks
@@ -346,67 +406,132 @@ def run_e2e(w, steps, warmup):
 
 
 # ------------------------------------------------------------------ the oracle on host cores
-def oracle_sample_step(cfg, n_seq, seed=0):
-    """One pass of the float64 oracle over the first n_seq sequences of the workload; returns seconds."""
+def oracle_inputs(cfg, n_seq, seed=0):
+    """CPU inputs of the first n_seq sequences of the workload, in shared memory (not timed)."""
     import math
 
     from long_context_speculative_split_gb300 import workloads as wl
-    from oracle.attention import attention, draft_attention
-    from oracle.sampling import draft_draw, rejection_sample
-    from oracle.snapkv import snapkv_select
-
     c = dict(cfg)
     lens = wl.lengths(cfg, seed)[:n_seq]
     c["B"] = n_seq
     c["lens"] = [int(x) for x in lens]
     cap = int(lens.max())
     k, v = wl.kv_cache(c, "cpu", seed, kv_len=lens, cap=cap)
-    q, qw = wl.queries(c, "cpu", seed), wl.window_queries(c, "cpu", seed)
     t, d = wl.logits(c, "cpu", seed)
-    u = wl.uniforms(c, "cpu", seed)
-    scale = 1.0 / math.sqrt(c["D"])
-    t0 = time.perf_counter()
-    sel = snapkv_select(qw, k, v, lens, c["W"], c["pool"], c["K"], scale)
-    toks = []
-    for s in range(c["gamma"]):
-        qd = wl.draft_queries(c, "cpu", seed, step=s)
-        draft_attention(qd, sel["k_draft"], sel["v_draft"], sel["draft_len"], scale)
-        x, _ = draft_draw(d[:, s:s + 1], u[:, s:s + 1])
-        toks.append(x[:, 0])
-    attention(q, k, v, lens, scale)
-    rejection_sample(t, d, torch.stack([torch.as_tensor(x) for x in toks], dim=1).numpy(), u)
-    return time.perf_counter() - t0
+    inp = dict(k=k, v=v, q=wl.queries(c, "cpu", seed), qw=wl.window_queries(c, "cpu", seed),
+               qd=torch.stack([wl.draft_queries(c, "cpu", seed, step=s) for s in range(c["gamma"])]),
+               t=t, d=d, u=wl.uniforms(c, "cpu", seed), lens=lens)
+    for x in inp.values():
+        x.share_memory_()
+    inp.update(W=c["W"], pool=c["pool"], K=c["K"], gamma=c["gamma"], G=c["Hq"] // c["Hkv"], Hkv=c["Hkv"],
+               scale=1.0 / math.sqrt(c["D"]))
+    return inp
 
 
-def cpu_cores_used():
-    return 1  # the oracle runs single-threaded (BLAS pinned to one thread above)
+def oracle_pair_job(job):
+    """The attention side of the path for one (sequence, KV head), by the float64 oracle: SnapKV
+    selection, gamma draft attentions over the selected rows, verify attention over the cache."""
+    from oracle.attention import attention, draft_attention
+    from oracle.snapkv import snapkv_select
+    x, b, h = job
+    hs = slice(h * x["G"], (h + 1) * x["G"])
+    L = x["lens"][b:b + 1]
+    n = int(L[0])
+    k, v = x["k"][b:b + 1, h:h + 1, :n], x["v"][b:b + 1, h:h + 1, :n]
+    sel = snapkv_select(x["qw"][b:b + 1, :, hs], k, v, L, x["W"], x["pool"], x["K"], x["scale"])
+    for s in range(x["gamma"]):
+        draft_attention(x["qd"][s, b:b + 1, :, hs], sel["k_draft"], sel["v_draft"], sel["draft_len"], x["scale"])
+    attention(x["q"][b:b + 1, :, hs], k, v, L, x["scale"])
+    return b, h
+
+
+def oracle_seq_job(job):
+    """The sampling side for one sequence, by the float64 oracle: gamma draft draws, then
+    rejection sampling of the round."""
+    import numpy as np
+
+    from oracle.sampling import draft_draw, rejection_sample
+    x, b = job
+    d, u = x["d"][b:b + 1], x["u"][b:b + 1]
+    toks = [draft_draw(d[:, s:s + 1], u[:, s:s + 1])[0][:, 0] for s in range(x["gamma"])]
+    rejection_sample(x["t"][b:b + 1], d, np.stack(toks, axis=1), u)
+    return b
+
+
+def _pool_ready(_):
+    import oracle.attention  # noqa: F401  (imports paid before the timed steps)
+    import oracle.sampling  # noqa: F401
+    import oracle.snapkv  # noqa: F401
+    return os.getpid()
+
+
+class OracleBaseline:
+    """The float64 oracle over a sample of n_seq sequences, as it stands, spread over the host
+    cores this process may use: one task per (sequence, KV head) for the attention side and one
+    per sequence for sampling, in a pool of spawned processes (BLAS one thread each)."""
+
+    def __init__(self, cfg, n_seq, seed=0):
+        import torch.multiprocessing as tmp
+        self.n_seq, self.cores = n_seq, len(os.sched_getaffinity(0))
+        self.inp = oracle_inputs(cfg, n_seq, seed)
+        self.pool = tmp.get_context("spawn").Pool(self.cores)
+        self.pool.map(_pool_ready, range(self.cores))
+        self.pairs = [(self.inp, b, h) for b in range(n_seq) for h in range(self.inp["Hkv"])]
+        self.seqs = [(self.inp, b) for b in range(n_seq)]
+
+    def step(self):
+        """One pass over the sample; returns wall-clock seconds."""
+        t0 = time.perf_counter()
+        r1 = self.pool.map_async(oracle_pair_job, self.pairs, chunksize=1)
+        r2 = self.pool.map_async(oracle_seq_job, self.seqs, chunksize=1)
+        r1.get()
+        r2.get()
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+    def sample_text(self, cfg, sec):
+        return ("%d of %d sequences (all %d KV heads, full context), whole path: %d (sequence, KV head) tasks and "
+                "%d sampling tasks over %d processes, %.1f s" % (self.n_seq, cfg["B"], cfg["Hkv"], len(self.pairs),
+                                                                 len(self.seqs), self.cores, sec))
 
 
 # ------------------------------------------------------------------ arms
 def run_reference(args):
     rank, world, _ = dist_env()
+    check_world(args, world)
     if rank != 0:
         return 0
     from long_context_speculative_split_gb300 import workloads as wl
     cfg = wl.WORKLOADS[args.workload]
     T = cfg["gamma"] + 1
+    ob = OracleBaseline(cfg, min(args.cpu_sample, cfg["B"]))
     for _ in range(args.warmup):
-        oracle_sample_step(cfg, 1)
-    times = [oracle_sample_step(cfg, 1) for _ in range(args.steps)]
+        ob.step()
+    times = [ob.step() for _ in range(args.steps)]
+    ob.close()
     sec = sum(times) / len(times)
-    value = T / sec
-    sample = "1 of %d sequences per step (all %d KV heads, full context), whole path" % (cfg["B"], cfg["Hkv"])
+    value = ob.n_seq * T / sec
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_block(cfg),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": ob.cores, "kind": "oracle",
+                         "sample": ob.sample_text(cfg, sec)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def kv_and_logit_gb(cfg):
+    from long_context_speculative_split_gb300 import workloads as wl
+    kv = 2 * cfg["Hkv"] * cfg["D"] * 2 * float(wl.lengths(cfg).double().sum())
+    logits = cfg["B"] * (2 * cfg["gamma"] + 1) * cfg["V"] * 4
+    return kv / 1e9, logits / 1e9
 
 
 def config_block(cfg):
@@ -417,39 +542,37 @@ def config_block(cfg):
                             cfg["name"], cfg["B"], ctx, cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["gamma"], cfg["K"],
                             cfg["W"], cfg["pool"], cfg["V"]),
             "batch": cfg["B"], "ctx": ctx, "gamma": cfg["gamma"], "K": cfg["K"],
-            "l2": "inputs larger than L2 (KV 17 GB, logits 0.6 GB at batch 128); standalone draft timing cycles through draft-cache copies of >= 256 MB",
+            "l2": "inputs larger than L2 (KV %.1f GB, logits %.2f GB); standalone draft timing cycles through "
+                  "draft-cache copies of >= 256 MB" % kv_and_logit_gb(cfg),
             "parallelism": "weak: one full batch per GPU"}
 
 
-def run_ours(args):
+def setup_rank(args):
+    """This rank's GPU (one per rank, LOCAL_RANK) and, for N > 1, the NCCL process group used
+    only for the barriers and the max over ranks around the timed region."""
     rank, world, local = dist_env()
+    check_world(args, world)
     assert torch.cuda.is_available(), "bench.py needs a CUDA GPU (the oracle arm is --impl reference)"
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
     import __graft_entry__
     __graft_entry__.build()
+    return rank, world, local, dev
+
+
+def run_ours(args):
+    rank, world, local, dev = setup_rank(args)
     w = Workload(args.workload, dev, seed=rank)
     for _ in range(args.warmup):
         w.step()
     torch.cuda.synchronize()
     nev = 5
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    start.record()
-    for i in range(args.steps):
-        w.step(evs[i])
-    end.record()
-    torch.cuda.synchronize()
-    barrier(world)
+    ms_step = run_timed(lambda i: w.step(evs[i]), args.steps, world, dev, CudaTimer(), torch.cuda.synchronize)
     clk = clocks.stop()
-    total_ms = start.elapsed_time(end)
-    total_ms = max_over_ranks(total_ms, world, dev)
-    ms_step = total_ms / args.steps
     phase = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)] for j in range(nev - 1)]
     snap_ms, draft_ms, verify_ms, spec_ms = (statistics.mean(x) for x in phase)
     errs = w.mgd.mgd_workspace_errors(w.ws_verify) | w.mgd.mgd_workspace_errors(w.ws_snap)
@@ -498,12 +621,20 @@ def run_ours(args):
         "clocks": clk,
         "e2e": e2e,
     }
+    if not args.no_round:  # the 32-layer speculation round (propose, verify, sample, commit), same GPU
+        cfg_w, B_w, T_w, Hkv_w = w.cfg, w.B, w.T, w.Hkv
+        del w
+        torch.cuda.empty_cache()
+        line["round"] = round_block(args, dev, world, rank, local)[0]
+    else:
+        cfg_w, B_w, T_w, Hkv_w = w.cfg, w.B, w.T, w.Hkv
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n = args.cpu_sample
-        sec = oracle_sample_step(w.cfg, n)
-        line["cpu_baseline"] = {"value": n * w.T / sec, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
-                                "sample": "%d of %d sequences (all %d KV heads, full context), whole path, %.1f s"
-                                          % (n, w.B, w.Hkv, sec)}
+        ob = OracleBaseline(cfg_w, min(args.cpu_sample, B_w))
+        ob.step()  # warm-up pass
+        sec = ob.step()
+        ob.close()
+        line["cpu_baseline"] = {"value": ob.n_seq * T_w / sec, "unit": UNIT, "cores": ob.cores, "kind": "oracle",
+                                "sample": ob.sample_text(cfg_w, sec)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -512,76 +643,87 @@ def run_ours(args):
     return 0
 
 
-def run_round(args):
-    """The 32-layer round workload: one full speculation round per step, replayed from a CUDA graph."""
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist_init(world, "nccl")
-    import __graft_entry__
-    __graft_entry__.build()
+def round_block(args, dev, world, rank, local):
+    """The 32-layer round workload, one full speculation round per step (propose, verify, sample,
+    commit), replayed from a CUDA graph that first restores the lengths, so every replay does the
+    same work.  Returns (block for the JSON line, ms per round, kernels per round, clocks)."""
+    from long_context_speculative_split_gb300 import mgd
     from long_context_speculative_split_gb300 import workloads as wl
     from long_context_speculative_split_gb300.round import SpeculationRound
     cfg = wl.WORKLOADS["round_b32_ctx16k_32layers"]
     r = SpeculationRound(cfg, dev, seed=rank).prepare()
     graph = True
     try:
-        r.capture()
+        r.capture(restore=True)
     except Exception as e:  # eager launches if capture is refused
         graph = "failed: %s" % str(e).splitlines()[0][:120]
         r.graph = None
         torch.cuda.synchronize()
-    for _ in range(args.warmup):
+
+    def one(_i=0):
+        if r.graph is None:
+            r.restore()
         r.replay()
+
+    for _ in range(args.warmup):
+        one()
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    s.record()
-    for _ in range(args.steps):
-        r.replay()
-    e.record()
-    torch.cuda.synchronize()
-    barrier(world)
+    ms = run_timed(one, args.steps, world, dev, CudaTimer(), torch.cuda.synchronize)
     clk = clocks.stop()
-    ms = max_over_ranks(s.elapsed_time(e), world, dev) / args.steps
     nacc = r.nacc.double()
     committed = float((nacc + 1).mean())
-    # the two phases of a round timed on their own (proposal; verification and correction)
-    phase_ms = [None, None]
+    errs = mgd.mgd_workspace_errors(r.ws_commit) | mgd.mgd_workspace_errors(r.ws_verify)
+    # the phases of a round timed on their own (proposal; verification and correction; commit)
+    phase_ms = [None, None, None]
     if graph is True:
         for i, g in enumerate(r.capture_phases()):
             for _ in range(2):
                 g.replay()
+            t = CudaTimer()
             torch.cuda.synchronize()
-            s.record()
+            t.start()
             for _ in range(args.steps):
                 g.replay()
-            e.record()
-            torch.cuda.synchronize()
-            phase_ms[i] = s.elapsed_time(e) / args.steps
-    tokens = r.B * r.T
+            t.stop()
+            phase_ms[i] = t.elapsed_ms() / args.steps
     peak, peak_kind = hbm_peak()
     attn_bytes = r.bytes_verify + r.bytes_draft
+    block = {
+        "workload": "%s: batch %d, context %d, %d layers of %dq/%dkv head_dim %d, gamma %d, draft K=%d, vocab %d, "
+                    "draft noise sigma_n=%.4f (mean acceptance 0.9)" % (
+                        cfg["name"], r.B, r.cap, r.layers, r.Hq, r.Hkv, r.D, r.gamma, r.K, r.V, cfg["sigma_n"]),
+        "cuda_graph": graph,
+        "ms_per_round": ms,
+        "verified_tokens_per_s_per_layer": world * r.B * r.T / (ms / 1e3) * r.layers,
+        "committed_tokens_per_s": world * r.B * committed / (ms / 1e3),
+        "mean_tokens_per_round": committed, "omega_expected_at_alpha_0.9": 3.439,
+        "ms_per_committed_token": ms / committed,
+        "proposal_ms": phase_ms[0], "verify_and_correction_ms": phase_ms[1], "commit_ms": phase_ms[2],
+        "attention_kv_gbs": attn_bytes / (ms / 1e3) / 1e9,
+        "attention_frac_of_peak": attn_bytes / (ms / 1e3) / 1e9 / peak, "peak_kind": peak_kind,
+        "gpu_launches_per_round": r.launches,
+        "device_error_flags": errs,
+        "clocks": clk,
+    }
+    del r
+    torch.cuda.empty_cache()
+    return block, ms, block["gpu_launches_per_round"], clk
+
+
+def run_round(args):
+    """The 32-layer round workload as the bench line's main measurement."""
+    rank, world, local, dev = setup_rank(args)
+    block, ms, launches, clk = round_block(args, dev, world, rank, local)
     line = {
-        "metric": METRIC, "value": world * tokens * r.layers / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": block["verified_tokens_per_s_per_layer"], "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "%s: batch %d, context %d, %d layers of %dq/%dkv head_dim %d, gamma %d, draft K=%d, "
-                               "vocab %d, draft noise sigma_n=%.4f (mean acceptance 0.9)" % (
-                                   cfg["name"], r.B, r.cap, r.layers, r.Hq, r.Hkv, r.D, r.gamma, r.K, r.V,
-                                   cfg["sigma_n"]),
-                   "l2": "inputs larger than L2 (68.7 GB KV)", "cuda_graph": graph,
-                   "parallelism": "weak: one full batch per GPU"},
-        "round": {"committed_tokens_per_s": world * r.B * committed / (ms / 1e3),
-                  "mean_tokens_per_round": committed, "omega_expected_at_alpha_0.9": 3.439,
-                  "ms_per_committed_token": ms / committed,
-                  "proposal_ms": phase_ms[0], "verify_and_correction_ms": phase_ms[1],
-                  "attention_kv_gbs": attn_bytes / (ms / 1e3) / 1e9,
-                  "attention_frac_of_peak": attn_bytes / (ms / 1e3) / 1e9 / peak, "peak_kind": peak_kind},
-        "gpu_launches": r.launches * args.steps,
+        "config": {"workload": block["workload"], "l2": "inputs larger than L2 (68.7 GB KV)",
+                   "cuda_graph": block["cuda_graph"], "parallelism": "weak: one full batch per GPU"},
+        "round": block,
+        "gpu_launches": launches * args.steps,
         "clocks": clk,
     }
     if rank == 0:
@@ -630,7 +772,10 @@ def load_traffic(name):
 
 
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     args = parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return launch_ranks(args.gpus, argv)  # one rank per GPU, each runs the rest of main()
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "round_b32_ctx16k_32layers":

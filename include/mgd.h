@@ -17,12 +17,16 @@
  *     mgd_*_workspace_size() returns for the same shape.
  *   - A workspace is ZERO-FILLED once before its first use (e.g. one
  *     cudaMemsetAsync after allocating it).  The attention calls
- *     (mgd_verify_attn, mgd_draft_attn) do not clear its header per call:
+ *     (mgd_verify_attn, mgd_draft_attn) and mgd_commit_round do not clear
+ *     its header per call:
  *     their kernels leave the counters at zero for the next call, which saves
  *     a clearing launch ahead of every attention launch.  The other calls
  *     clear the part they use themselves.  A buffer that served as scratch for
  *     anything but attention calls is zero-filled again before an attention
- *     call uses it.
+ *     call uses it.  An attention call that starts from a header in any other
+ *     state (its work counters not at zero) detects it at its end and raises
+ *     MGD_DEVERR_STALE_WS: its outputs are then unspecified, and the workspace
+ *     is zero-filled again before the next call.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous on that stream; nothing synchronises.
  *   - Shape / argument errors are detected on the host before anything is
@@ -72,6 +76,8 @@ typedef enum {
 #define MGD_DEVERR_TOKEN    0x4u   /* a draft token id outside [0, V) */
 #define MGD_DEVERR_TIMEOUT  0x8u   /* a bounded wait inside a kernel gave up (never expected) */
 #define MGD_DEVERR_COMMIT   0x10u  /* mgd_commit_round: num_accepted, kv_len or draft_len out of range */
+#define MGD_DEVERR_STALE_WS 0x20u  /* an attention call found its workspace header not ready (not zero-filled,
+                                      or last used by another call); its outputs are unspecified */
 
 const char *mgd_status_string(mgd_status s);
 /* Detail text of the last non-OK status returned on the calling thread ("" if none). */
@@ -103,6 +109,19 @@ mgd_status mgd_workspace_errors(const void *ws, void *stream, uint32_t *flags);
  */
 #define MGD_SELFTEST_WS_BYTES 512u
 mgd_status mgd_selftest_bounded_wait(int which, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Diagnostic: holds SMs for a while, so that a test can run another call on a
+ * second stream while few SMs are free (the SnapKV scorer's CTAs wait for one
+ * another; this shows that they make progress whatever number of them is
+ * resident).  Launches `ctas` CTAs of one warp on `stream`; each holds
+ * `smem_bytes` of dynamic shared memory (which keeps other CTAs off its SM when
+ * large) and returns after `usec` microseconds of the GPU's global timer.  It
+ * waits on nothing else and touches no memory.  Errors: MGD_ERR_INVALID_ARG
+ * (ctas outside [1, 65535], smem_bytes outside [1, 232448], usec outside
+ * [0, 2000000]), MGD_ERR_CUDA.
+ */
+mgd_status mgd_selftest_occupy(int ctas, int smem_bytes, int usec, void *stream);
 
 /* ------------------------------------------------------------------------ *
  * Verify attention.  [MagicDec] section 3.2: verifying gamma draft tokens
@@ -307,7 +326,10 @@ mgd_status mgd_topk_draft_attn(const void *q, const void *k, const void *v, cons
  *   `dtype`, strides in elements as for mgd_verify_attn (rows contiguous).
  * A sequence with n outside [0, gamma], kv_len outside [T, kv_cap] or
  * draft_len + n + 1 > draft_cap is left unchanged and flagged
- * (MGD_DEVERR_COMMIT).  Byte copies and integer updates only.
+ * (MGD_DEVERR_COMMIT).  Byte copies and integer updates only, in one launch.
+ * Like the attention calls, this call does not clear its workspace header:
+ * the kernel leaves it ready for the next call, so `ws` is zero-filled once
+ * before its first use (and again after serving as any other call's scratch).
  * ------------------------------------------------------------------------ */
 size_t mgd_commit_workspace_size(int B);
 mgd_status mgd_commit_round(const int32_t *num_accepted, int B, int gamma, int Hkv, int D, mgd_dtype dtype,
@@ -334,9 +356,11 @@ mgd_status mgd_commit_round(const int32_t *num_accepted, int B, int gamma, int H
  *     fit in MGD_NOALLOC_SCRATCH_BYTES (about B * ((2*gamma+1) * ceil(V/16384) * 8
  *     + 4) + 512 bytes; e.g. B <= 1807 at gamma = 4, V = 128256); larger requests
  *     return MGD_ERR_UNSUPPORTED with an explanation in mgd_last_error().
- *   - The first call on a device (with that device current) looks up the
- *     array's device address with cudaGetSymbolAddress; make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     with cudaGetSymbolAddress (a host-side lookup, so the address is never
+ *     stale, e.g. after a device reset).  The first call on a device may also
+ *     load the library's device code there; make that first call before any
+ *     stream capture.
  *   - Every call shares the one array, which keeps the last call's contents
  *     (the error word at its start is cleared by each call).  Calls that
  *     overlap on the GPU (different streams or host threads) race on it and

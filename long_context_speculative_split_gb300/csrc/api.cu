@@ -202,6 +202,15 @@ mgd_status mgd_selftest_bounded_wait(int which, void *ws, size_t ws_bytes, void 
   return e == cudaSuccess ? ok() : cuda_fail(e, "self-test launch");
 }
 
+mgd_status mgd_selftest_occupy(int ctas, int smem_bytes, int usec, void *stream) {
+  if (ctas < 1 || ctas > 65535) return fail(MGD_ERR_INVALID_ARG, "ctas must be in [1, 65535] (got %d)", ctas);
+  if (smem_bytes < 1 || smem_bytes > 227 * 1024)
+    return fail(MGD_ERR_INVALID_ARG, "smem_bytes must be in [1, 232448] (got %d)", smem_bytes);
+  if (usec < 0 || usec > 2000000) return fail(MGD_ERR_INVALID_ARG, "usec must be in [0, 2000000] (got %d)", usec);
+  cudaError_t e = launch_selftest_occupy(ctas, smem_bytes, usec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "occupy launch");
+}
+
 size_t mgd_verify_workspace_size(int B, int T, int Hq, int Hkv, int D, int kv_cap) {
   if (B <= 0 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || kv_cap < 1) return kAlign;
   return plan_attention(B, T, Hq, Hkv, D, kv_cap, current_sm_count()).ws_bytes;

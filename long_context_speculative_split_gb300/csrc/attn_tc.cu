@@ -128,12 +128,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint32_t phase = 0;
     bool ok = true;
     bool first = true;
+    unsigned claims = 0;  // successful claims from the counter
     while (ok) {
       // every CTA's first unit is its own index (no counter round trip before the first
       // load); later units come from the counter
       const unsigned u = first ? blockIdx.x : gridDim.x + atomicAdd(&hdr->next_unit, 1u);
-      first = false;
       if (u >= p.total_units) break;
+      claims += first ? 0u : 1u;
+      first = false;
       const int pair = static_cast<int>(u) / p.nchunk;
       const int chunk = static_cast<int>(u) % p.nchunk;
       const int bh = pair / p.RG;
@@ -195,7 +197,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     // This CTA's claims are over: it checks in (its consumers need not: they claim nothing,
     // and their only error bits, timeouts, land in one of the two words either way).
-    call_check_in(hdr, gridDim.x);
+    // From a ready header the counter hands out exactly the units past the first wave.
+    call_check_in(hdr, gridDim.x, blockIdx.x, claims, p.total_units - gridDim.x);
     return;
   }
 

@@ -10,9 +10,11 @@
 // with n accepted, rows 0..n are kept (kv_len -= gamma - n) and copied to the
 // draft cache at draft_len .. draft_len + n (draft_len += n + 1).
 //
-// Two launches: commit_copy (one CTA per (sequence, KV head), 16-byte vector
-// copies of the kept K and V rows) reads the old lengths; commit_lengths then
-// rewrites them, so no CTA ever reads a length another CTA is updating.
+// One launch, one CTA per sequence: the CTA reads its sequence's lengths,
+// copies the kept K and V rows of every KV head (16-byte vectors), and only
+// then rewrites those two lengths, so no CTA reads a length another CTA is
+// updating.  The workspace header resets itself at the end of the call (no
+// clearing launch): the last CTA to check in leaves it ready for the next call.
 #include "common.cuh"
 
 namespace mgd {
@@ -27,38 +29,37 @@ __device__ __forceinline__ bool commit_valid(int n, int L, int dl, const CommitP
   return n >= 0 && n <= p.gamma && L >= p.gamma + 1 && L <= p.kv_cap && dl >= 0 && dl + n + 1 <= p.draft_cap;
 }
 
-__global__ void __launch_bounds__(128)
-    commit_copy(const int32_t *__restrict__ num_accepted, const int32_t *__restrict__ kv_len,
-                const int32_t *__restrict__ draft_len, const unsigned char *__restrict__ k,
-                const unsigned char *__restrict__ v, unsigned char *__restrict__ kd, unsigned char *__restrict__ vd,
-                CommitParams p, WsHeader *hdr) {
-  const int b = blockIdx.x / p.Hkv, h = blockIdx.x % p.Hkv;
+__global__ void __launch_bounds__(256)
+    commit_kernel(const int32_t *__restrict__ num_accepted, int32_t *__restrict__ kv_len,
+                  int32_t *__restrict__ draft_len, const unsigned char *__restrict__ k,
+                  const unsigned char *__restrict__ v, unsigned char *__restrict__ kd, unsigned char *__restrict__ vd,
+                  CommitParams p, WsHeader *hdr) {
+  const int b = blockIdx.x;
   const int n = num_accepted[b], L = kv_len[b], dl = draft_len[b];
-  if (!commit_valid(n, L, dl, p)) {
-    if (threadIdx.x == 0 && h == 0) raise_error(hdr, 0x10u);
-    return;
+  const bool ok = commit_valid(n, L, dl, p);
+  if (ok) {
+    const int first = L - p.gamma - 1;
+    const int vecs = p.row_bytes / 16;
+    const int per_head = (n + 1) * vecs;
+    for (int i = threadIdx.x; i < p.Hkv * per_head; i += blockDim.x) {
+      const int h = i / per_head, r = i - h * per_head;
+      const int64_t off = static_cast<int64_t>(r / vecs) * p.row_bytes + (r % vecs) * 16;
+      const int64_t src = b * p.kv_bstride + h * p.kv_hstride + static_cast<int64_t>(first) * p.row_bytes + off;
+      const int64_t dst = b * p.d_bstride + h * p.d_hstride + static_cast<int64_t>(dl) * p.row_bytes + off;
+      *reinterpret_cast<uint4 *>(kd + dst) = *reinterpret_cast<const uint4 *>(k + src);
+      *reinterpret_cast<uint4 *>(vd + dst) = *reinterpret_cast<const uint4 *>(v + src);
+    }
   }
-  const int first = L - p.gamma - 1;
-  const int vecs = p.row_bytes / 16;
-  const unsigned char *ks = k + b * p.kv_bstride + h * p.kv_hstride + static_cast<int64_t>(first) * p.row_bytes;
-  const unsigned char *vs = v + b * p.kv_bstride + h * p.kv_hstride + static_cast<int64_t>(first) * p.row_bytes;
-  unsigned char *kt = kd + b * p.d_bstride + h * p.d_hstride + static_cast<int64_t>(dl) * p.row_bytes;
-  unsigned char *vt = vd + b * p.d_bstride + h * p.d_hstride + static_cast<int64_t>(dl) * p.row_bytes;
-  for (int i = threadIdx.x; i < (n + 1) * vecs; i += blockDim.x) {
-    const int64_t off = static_cast<int64_t>(i / vecs) * p.row_bytes + (i % vecs) * 16;
-    *reinterpret_cast<uint4 *>(kt + off) = *reinterpret_cast<const uint4 *>(ks + off);
-    *reinterpret_cast<uint4 *>(vt + off) = *reinterpret_cast<const uint4 *>(vs + off);
+  __syncthreads();  // every thread has read the lengths above before they change
+  if (threadIdx.x == 0) {
+    if (ok) {
+      kv_len[b] = L - (p.gamma - n);
+      draft_len[b] = dl + n + 1;
+    } else {
+      raise_error_sr(hdr, 0x10u);
+    }
+    call_check_in(hdr, gridDim.x, blockIdx.x, 0u, 0u);
   }
-}
-
-__global__ void commit_lengths(const int32_t *__restrict__ num_accepted, int32_t *__restrict__ kv_len,
-                               int32_t *__restrict__ draft_len, CommitParams p) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= p.B) return;
-  const int n = num_accepted[b], L = kv_len[b], dl = draft_len[b];
-  if (!commit_valid(n, L, dl, p)) return;
-  kv_len[b] = L - (p.gamma - n);
-  draft_len[b] = dl + n + 1;
 }
 
 }  // namespace
@@ -67,8 +68,6 @@ cudaError_t launch_commit(const int32_t *num_accepted, int B, int gamma, int Hkv
                           const void *k, const void *v, int kv_cap, int64_t kv_bstride, int64_t kv_hstride,
                           void *k_draft, void *v_draft, int draft_cap, int64_t d_bstride, int64_t d_hstride,
                           int32_t *draft_len, void *ws, cudaStream_t stream) {
-  cudaError_t e = cudaMemsetAsync(ws, 0, kAlign, stream);
-  if (e != cudaSuccess) return e;
   CommitParams p;
   p.B = B;
   p.gamma = gamma;
@@ -80,13 +79,9 @@ cudaError_t launch_commit(const int32_t *num_accepted, int B, int gamma, int Hkv
   p.kv_hstride = kv_hstride * esz;
   p.d_bstride = d_bstride * esz;
   p.d_hstride = d_hstride * esz;
-  commit_copy<<<B * Hkv, 128, 0, stream>>>(num_accepted, kv_len, draft_len, static_cast<const unsigned char *>(k),
-                                           static_cast<const unsigned char *>(v),
-                                           static_cast<unsigned char *>(k_draft), static_cast<unsigned char *>(v_draft),
-                                           p, static_cast<WsHeader *>(ws));
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  commit_lengths<<<(B + 255) / 256, 256, 0, stream>>>(num_accepted, kv_len, draft_len, p);
+  commit_kernel<<<B, 256, 0, stream>>>(num_accepted, kv_len, draft_len, static_cast<const unsigned char *>(k),
+                                       static_cast<const unsigned char *>(v), static_cast<unsigned char *>(k_draft),
+                                       static_cast<unsigned char *>(v_draft), p, static_cast<WsHeader *>(ws));
   return cudaGetLastError();
 }
 

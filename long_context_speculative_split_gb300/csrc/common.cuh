@@ -41,18 +41,33 @@ __device__ __forceinline__ void raise_error_sr(WsHeader *hdr, unsigned bit) {
   atomicOr(&hdr->err[s & 1u], bit);
 }
 
-// End of one part of a self-resetting call (a thread whose claims from next_unit
-// are all done).  The last of `parts` check-ins puts the counters back to zero,
-// clears the error word the next call will use and advances seq, so the workspace
-// is ready for the next call with no clearing launch in between.
-__device__ __forceinline__ void call_check_in(WsHeader *hdr, unsigned parts) {
+// End of one part of a self-resetting call: block `id` (one check-in per block,
+// after its claims from next_unit are all done; `claims` of them succeeded).
+// The last of `parts` check-ins puts the counters back to zero, clears the
+// error word the next call will use and advances seq, so the workspace is ready
+// for the next call with no clearing launch in between.  It also checks two
+// sums against the values a call started from a ready header produces: the
+// successful claims (`expect`) and the block ids of the check-ins.  A header
+// left dirty by other use (a stale next_unit skips units; a stale done ends the
+// call early; stale sums) breaks one of them, and the call raises
+// MGD_DEVERR_STALE_WS unless one of its waits timed out (which stops claiming).
+__device__ __forceinline__ void call_check_in(WsHeader *hdr, unsigned parts, unsigned id, unsigned claims,
+                                              unsigned expect) {
+  if (claims) atomicAdd(&hdr->claimed, claims);
+  atomicAdd(&hdr->ids, id + 1u);
   __threadfence();
   if (atomicAdd(&hdr->done, 1u) == parts - 1u) {
     __threadfence();
     volatile unsigned *h = reinterpret_cast<volatile unsigned *>(hdr);
     const unsigned s = h[offsetof(WsHeader, seq) / 4];
+    const unsigned got = h[offsetof(WsHeader, claimed) / 4];
+    const unsigned ids = h[offsetof(WsHeader, ids) / 4];
+    const unsigned all_ids = static_cast<unsigned>((static_cast<unsigned long long>(parts) * (parts + 1ull)) / 2ull);
+    if ((got != expect || ids != all_ids) && !(h[s & 1u] & 0x8u)) atomicOr(&hdr->err[s & 1u], 0x20u);
     h[offsetof(WsHeader, next_unit) / 4] = 0u;
     h[offsetof(WsHeader, next_unit2) / 4] = 0u;
+    h[offsetof(WsHeader, claimed) / 4] = 0u;
+    h[offsetof(WsHeader, ids) / 4] = 0u;
     h[offsetof(WsHeader, done) / 4] = 0u;
     h[(s + 1u) & 1u] = 0u;  // err[(s + 1) & 1]
     h[offsetof(WsHeader, seq) / 4] = s + 1u;

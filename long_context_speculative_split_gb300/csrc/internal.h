@@ -10,8 +10,9 @@
 
 namespace mgd {
 
-// Every workspace starts with this 256-byte header.  It is cleared at the
-// start of every call (cudaMemsetAsync on the call's stream).
+// Every workspace starts with this 256-byte header.  Kernels either clear it
+// ahead of the call (cudaMemsetAsync on the call's stream) or leave it ready
+// for the next call themselves (the self-resetting kernels, see call_check_in).
 struct WsHeader {
   // MGD_DEVERR_* bits.  Kernels that clear the header before they run raise into
   // err[1].  Kernels that leave the workspace ready for the next call (no clearing
@@ -23,7 +24,15 @@ struct WsHeader {
   unsigned next_unit2;
   unsigned done;  // end-of-call check-ins of the self-resetting kernels
   unsigned seq;   // calls completed by the self-resetting kernels on this workspace
-  unsigned pad[58];
+  // Successful claims from next_unit, summed at check-in.  From a zero start a
+  // self-resetting call's claims add up to a known count; any other sum means
+  // the call started from a header that was not left ready (MGD_DEVERR_STALE_WS).
+  unsigned claimed;
+  // Sum of (block index + 1) over the check-ins so far: at the last check-in of a call
+  // started from a ready header it is parts * (parts + 1) / 2 (a stale `done` makes a
+  // check-in look like the last one while other CTAs have not checked in yet).
+  unsigned ids;
+  unsigned pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -93,7 +102,7 @@ struct SnapPlan {
   int C;       // keys per scoring unit (multiple of 64; a multiple of 128 for the tcgen05 scorer)
   int nchunk;  // ceil(kv_cap / C)
   int pairs;   // B * Hkv
-  size_t off_cnt;  // unsigned [pairs]: slices published per pair (zeroed with the header on every call)
+  size_t off_cnt;  // unsigned [2][pairs]: slices published and slices claimed per pair (zeroed with the header)
   int lrows;       // windows of <= 8 rows: logit rows stored per key by pass 1 (4 or 8), else 0
   size_t off_logits;  // float [pairs][kv_cap][lrows] when lrows > 0
   size_t off_part, off_scores, off_pooled, ws_bytes;
@@ -132,6 +141,8 @@ int encode_qwin_tensor_map(CUtensorMap *map, const void *base, int B, int W, int
 // One bounded wait that nothing completes (0: an mbarrier phase, 1: a counter
 // in the workspace); needs 2 * kAlign bytes of workspace.
 cudaError_t launch_selftest_wait(int which, void *ws, cudaStream_t stream);
+// `ctas` CTAs, each holding `smem_bytes` of shared memory for `usec` microseconds.
+cudaError_t launch_selftest_occupy(int ctas, int smem_bytes, int usec, cudaStream_t stream);
 
 // ------------------------------------------------------------------ sampling
 struct SpecPlan {

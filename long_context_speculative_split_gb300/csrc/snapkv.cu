@@ -964,8 +964,8 @@ SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W) {
   }
   p.C = C;
   p.nchunk = (kv_cap + C - 1) / C;
-  p.off_cnt = kAlign;
-  size_t off = align_up(p.off_cnt + sizeof(unsigned) * static_cast<size_t>(p.pairs));
+  p.off_cnt = kAlign;  // [pairs] slices published, then [pairs] slices claimed (one-read tcgen05 scorer)
+  size_t off = align_up(p.off_cnt + 2 * sizeof(unsigned) * static_cast<size_t>(p.pairs));
   p.off_part = off;
   off = align_up(off + sizeof(float2) * static_cast<size_t>(p.pairs) * p.RG * p.nchunk * kRowsPerCta);
   p.off_scores = off;

@@ -11,12 +11,12 @@
 //
 // The array (kNoAllocScratchBytes) exists on every GPU that loads the library
 // until the process exits.  In host code its name is only a host-side stand-in,
-// not a device address, so the device address is looked up once per device,
-// with that device current, through cudaGetSymbolAddress.
+// not a device address, so every call looks the device address up, with the
+// call's device current, through cudaGetSymbolAddress: a cheap host-side
+// lookup, and never stale (after a device reset the array may live elsewhere).
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "../../include/mgd.h"
 #include "internal.h"
@@ -31,25 +31,12 @@ static_assert(kNoAllocScratchBytes % kAlign == 0, "scratch size is a multiple of
 
 static __device__ __align__(256) unsigned char g_spec_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_spec_scratch on the current device; the first call on a
-// device performs the lookup and caches it.
+// Device address of g_spec_scratch on the current device.
 cudaError_t scratch_on_current_device(void **out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_spec_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_spec_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

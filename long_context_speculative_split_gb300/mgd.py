@@ -19,6 +19,7 @@ MGD_BF16, MGD_F32 = 0, 1
 MGD_VERIFY, MGD_DRAW_DRAFT = 0, 1
 MGD_DEVERR_KV_LEN, MGD_DEVERR_SNAP_LEN, MGD_DEVERR_TOKEN, MGD_DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 MGD_DEVERR_COMMIT = 0x10
+MGD_DEVERR_STALE_WS = 0x20
 
 _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 
@@ -29,6 +30,7 @@ SIGNATURES = {
     "mgd_version": (_i32, []),
     "mgd_workspace_errors": (_i32, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]),
     "mgd_selftest_bounded_wait": (_i32, [_i32, _vp, _sz, _vp]),
+    "mgd_selftest_occupy": (_i32, [_i32, _i32, _i32, _vp]),
     "mgd_verify_workspace_size": (_sz, [_i32] * 6),
     "mgd_verify_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _f32, _i32,
                                _vp, _i32, _vp, _vp, _sz, _vp]),
@@ -133,6 +135,10 @@ def mgd_selftest_bounded_wait(which, ws, ws_bytes=None, stream=None):
     if ws_bytes is None:
         ws_bytes = ws.numel() * ws.element_size()
     _check(load().mgd_selftest_bounded_wait(which, _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def mgd_selftest_occupy(ctas, smem_bytes, usec, stream=None):
+    _check(load().mgd_selftest_occupy(ctas, smem_bytes, usec, _stream(stream)))
 
 
 def mgd_verify_workspace_size(B, T, Hq, Hkv, D, kv_cap):

@@ -61,3 +61,55 @@ def assert_index_sets_match(gpu_idx, ref_idx, pooled_ref, kth):
         assert abs(pooled_ref[j] - kth) <= SNAP_REL * abs(kth), \
             "position %d (score %.9g) differs outside the band around %.9g" % (j, pooled_ref[j], kth)
     return len(diff)
+
+
+# ---------------------------------------------------------------- canaries
+# Out-of-bounds writes by a kernel would only be caught by a compared value they happen to
+# corrupt; instead every output of the parity tests can sit between two guard regions of one
+# allocation, filled with a poison bit pattern (a NaN for float types, the same bits for
+# integers), and padded rows that a call must leave alone can be poisoned too.  After the
+# call the poison must be intact, bit for bit.
+_BITS = {torch.float32: torch.int32, torch.int32: torch.int32, torch.bfloat16: torch.int16,
+         torch.int16: torch.int16}
+_POISON = {torch.int32: 0x7FBADBAD, torch.int16: 0x7FBA}   # NaN payloads as f32 / bf16
+
+
+def poison_value(dtype):
+    return _POISON[_BITS[dtype]]
+
+
+def poison_(t):
+    """Fill t (any tensor of a guarded dtype) with the poison pattern; returns t."""
+    t.view(_BITS[t.dtype]).fill_(poison_value(t.dtype))
+    return t
+
+
+def is_poison(t):
+    """Elementwise: does t still hold the poison pattern?"""
+    return t.view(_BITS[t.dtype]) == poison_value(t.dtype)
+
+
+class Guarded:
+    """An output tensor `t` between two 4 KB poisoned guard regions of one allocation (the
+    offset keeps t 256-byte aligned).  `init` fills t (default: poison, so elements a call
+    must write and does not stay visibly unwritten)."""
+    GUARD_BYTES = 4096
+
+    def __init__(self, shape, dtype, device, init=None):
+        esz = torch.empty((), dtype=dtype).element_size()
+        self.g = self.GUARD_BYTES // esz
+        n = int(np.prod(shape)) if len(shape) else 1
+        self.buf = poison_(torch.empty(2 * self.g + n, dtype=dtype, device=device))
+        self.t = self.buf[self.g:self.g + n].view(*shape)
+        if init is not None:
+            self.t.copy_(init)
+
+    def check(self, what="output"):
+        head, tail = self.buf[:self.g], self.buf[self.buf.numel() - self.g:]
+        assert bool(is_poison(head).all()), "%s: the guard region before it was written" % what
+        assert bool(is_poison(tail).all()), "%s: the guard region after it was written" % what
+
+
+def check_guards(**guards):
+    for name, g in guards.items():
+        g.check(name)

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from _parity import assert_attention_close, assert_lse_close, gpu_or_skip, to64
+from _parity import Guarded, assert_attention_close, assert_lse_close, check_guards, gpu_or_skip, poison_, to64
 from long_context_speculative_split_gb300 import mgd, ops
 from long_context_speculative_split_gb300 import workloads as wl
 from oracle.attention import attention as ref_attention
@@ -14,7 +14,7 @@ from oracle.attention import draft_attention as ref_draft
 pytestmark = pytest.mark.gpu
 
 
-def _case(B, T, Hq, Hkv, D, lens, cap, seed, dtype=torch.bfloat16, hh=True):
+def _case(B, T, Hq, Hkv, D, lens, cap, seed, dtype=torch.bfloat16, hh=True, poison_pad=False):
     g = torch.Generator().manual_seed(seed)
     q = torch.randn((B, T, Hq, D), generator=g).to(dtype)
     k = torch.randn((B, Hkv, cap, D), generator=g)
@@ -23,7 +23,24 @@ def _case(B, T, Hq, Hkv, D, lens, cap, seed, dtype=torch.bfloat16, hh=True):
         for b in range(B):
             idx = torch.randperm(lens[b], generator=g)[: max(1, lens[b] // 100)]
             k[b, :, idx] *= 8
-    return q, k.to(dtype), v.to(dtype), torch.tensor(lens, dtype=torch.int32)
+    k, v = k.to(dtype), v.to(dtype)
+    if poison_pad:  # rows past each sequence's length hold NaN: no result may ever see them
+        for b in range(B):
+            poison_(k[b, :, lens[b]:])
+            poison_(v[b, :, lens[b]:])
+    return q, k, v, torch.tensor(lens, dtype=torch.int32)
+
+
+def _guarded_attention(fn, q, B, T, Hq, D, dev, **kw):
+    """Run an attention call with its out and lse between poisoned guard regions; checks the
+    guards and that every element was written."""
+    o = Guarded((B, T, Hq, D) if T else (B, Hq, D), torch.float32, dev)
+    l = Guarded((B, T, Hq) if T else (B, Hq), torch.float32, dev)
+    out, lse = fn(out=o.t, lse=l.t, **kw)
+    torch.cuda.synchronize()
+    check_guards(out=o, lse=l)
+    assert bool(torch.isfinite(o.t).all()) and bool(torch.isfinite(l.t).all()), "an output element was not written"
+    return out, lse
 
 
 CASES = [
@@ -45,9 +62,9 @@ CASES = [
 def test_verify_bf16_matches_oracle(case):
     dev = gpu_or_skip()
     B, T, Hq, Hkv, D, lens, cap = case
-    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=sum(lens) + T)
-    out, lse = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev))
-    torch.cuda.synchronize()
+    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=sum(lens) + T, poison_pad=True)
+    out, lse = _guarded_attention(lambda **kw: ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev), **kw),
+                                  q, B, T, Hq, D, dev)
     ref, ref_lse = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(D))
     assert_attention_close(out, ref)
     assert_lse_close(lse, ref_lse)
@@ -63,8 +80,9 @@ def test_verify_split_units_and_merges_match_oracle(B, T, Hq, Hkv):
     g = torch.Generator().manual_seed(B)
     lens = torch.randint(T, cap + 1, (B,), generator=g).tolist()
     lens[0] = cap
-    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=B + T)
-    out, lse = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev))
+    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=B + T, poison_pad=True)
+    out, lse = _guarded_attention(lambda **kw: ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev), **kw),
+                                  q, B, T, Hq, D, dev)
     ref, ref_lse = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(D))
     assert_attention_close(out, ref)
     assert_lse_close(lse, ref_lse)
@@ -111,8 +129,9 @@ def test_draft_float32_tiny_config_full():
 def test_draft_bf16_matches_oracle(lens, cap):
     dev = gpu_or_skip()
     B = len(lens)
-    q, k, v, dlen = _case(B, 1, 32, 8, 128, lens, cap, seed=cap)
-    out, lse = ops.draft_attn(q.to(dev), k.to(dev), v.to(dev), dlen.to(dev))
+    q, k, v, dlen = _case(B, 1, 32, 8, 128, lens, cap, seed=cap, poison_pad=True)
+    out, lse = _guarded_attention(lambda **kw: ops.draft_attn(q.to(dev), k.to(dev), v.to(dev), dlen.to(dev), **kw),
+                                  q, B, 0, 32, 128, dev)
     ref, ref_lse = ref_draft(q, k, v, dlen, 1.0 / math.sqrt(128))
     assert_attention_close(out, ref[:, 0])
     assert_lse_close(lse, ref_lse[:, 0])
@@ -208,22 +227,32 @@ def _torch_attention(q, k, v, L, scale):
 
 def test_verify_ragged_every_sequence():
     """Ragged batch 256 x U[4096, 65536] (the benchmark's launch configuration): every
-    sequence checked, so no unit of the persistent schedule can go missing unnoticed."""
+    sequence is compared with the float64 oracle on one of its KV heads (head b % Hkv, so all
+    heads are covered across the batch), so no unit of the persistent schedule can go missing
+    unnoticed.  As an extra, every head of every sequence is checked against float32 torch
+    math on the GPU."""
     dev = gpu_or_skip()
     c = wl.WORKLOADS["ragged_b256_ctx4k_64k"]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len)
     q = wl.queries(c, dev)
-    out, _ = ops.verify_attn(q, k, v, kv_len.to(dev))
+    out, lse = ops.verify_attn(q, k, v, kv_len.to(dev))
     torch.cuda.synchronize()
     scale = 1.0 / math.sqrt(c["D"])
+    G, Hkv = c["Hq"] // c["Hkv"], c["Hkv"]
     worst_abs, num, den = 0.0, 0.0, 0.0
     for b in range(c["B"]):
-        ref = _torch_attention(q[b], k[b], v[b], int(kv_len[b]), scale)
-        d = (out[b] - ref).double()
+        L, h = int(kv_len[b]), b % Hkv
+        hs = slice(h * G, (h + 1) * G)
+        ref, ref_lse = ref_attention(q[b:b + 1, :, hs], k[b:b + 1, h:h + 1, :L], v[b:b + 1, h:h + 1, :L],
+                                     kv_len[b:b + 1], scale)
+        assert_attention_close(out[b:b + 1, :, hs], ref, "out[b=%d,h=%d]" % (b, h))
+        assert_lse_close(lse[b:b + 1, :, hs], ref_lse)
+        t = _torch_attention(q[b], k[b], v[b], L, scale)
+        d = (out[b] - t).double()
         worst_abs = max(worst_abs, float(d.abs().max()))
         num += float((d ** 2).sum())
-        den += float((ref.double() ** 2).sum())
+        den += float((t.double() ** 2).sum())
     assert worst_abs <= 2e-2 and (num / den) ** 0.5 <= 1e-3, (worst_abs, (num / den) ** 0.5)
     del k, v
     torch.cuda.empty_cache()
@@ -237,8 +266,9 @@ def test_draft_split_units_match_oracle():
     B, Hq, Hkv, D, cap = 64, 32, 8, 128, 2048
     g = torch.Generator().manual_seed(77)
     lens = torch.randint(1200, cap + 1, (B,), generator=g).tolist()
-    q, k, v, dlen = _case(B, 1, Hq, Hkv, D, lens, cap, seed=78)
-    out, lse = ops.draft_attn(q.to(dev), k.to(dev), v.to(dev), dlen.to(dev))
+    q, k, v, dlen = _case(B, 1, Hq, Hkv, D, lens, cap, seed=78, poison_pad=True)
+    out, lse = _guarded_attention(lambda **kw: ops.draft_attn(q.to(dev), k.to(dev), v.to(dev), dlen.to(dev), **kw),
+                                  q, B, 0, Hq, D, dev)
     ref, ref_lse = ref_draft(q, k, v, dlen, 1.0 / math.sqrt(D))
     assert_attention_close(out, ref[:, 0])
     assert_lse_close(lse, ref_lse[:, 0])
@@ -282,3 +312,44 @@ def test_workspace_reused_across_shapes_and_errors():
         assert torch.equal(out[0][keep], fresh_bad[0][keep])
     ref, _ = ref_attention(qa[:3].cpu(), ka[:3].cpu(), va[:3].cpu(), la[:3].cpu(), 1.0 / math.sqrt(128))
     assert_attention_close(fresh_v[0][:3], ref)
+
+
+def test_stale_workspace_is_detected():
+    """The attention calls do not clear their workspace header; a header that is not ready
+    (not zero-filled, or last used as SnapKV scratch) is detected at the end of the call and
+    raises MGD_DEVERR_STALE_WS.  The shape has more (sequence, KV head) pairs than CTA slots,
+    so units past the first wave come from the header's work counter."""
+    dev = gpu_or_skip()
+    lens = [int(x) for x in np.random.default_rng(6).integers(500, 1001, size=40)]
+    q, k, v, kv_len = (x.to(dev) for x in _case(40, 4, 32, 8, 128, lens, 1000, seed=31))
+    qw = torch.randn((40, 32, 32, 128), generator=torch.Generator().manual_seed(32)).to(torch.bfloat16).to(dev)
+    need = max(mgd.mgd_verify_workspace_size(40, 4, 32, 8, 128, 1000),
+               mgd.mgd_snapkv_workspace_size(40, 32, 8, 128, 1000, 32))
+    fresh = ops.verify_attn(q, k, v, kv_len, ws=ops.workspace(need, dev))
+    ws = ops.workspace(need, dev)
+    hdr = ws[:256].view(torch.int32)   # err[0], err[1], next_unit, next_unit2, done, seq, claimed, ids, ...
+    # a stale work counter (small, past every unit); a stale check-in count; stale sums
+    for field, value in ((2, 5), (2, 100000), (4, 3), (4, 1), (6, 2), (7, 9)):
+        ws.zero_()
+        hdr[field] = value
+        ops.verify_attn(q, k, v, kv_len, ws=ws)
+        assert mgd.mgd_workspace_errors(ws) & mgd.MGD_DEVERR_STALE_WS, (field, value)
+    # zero-filled again, the same buffer gives the fresh result with no error bits
+    ws.zero_()
+    out = ops.verify_attn(q, k, v, kv_len, ws=ws)
+    assert mgd.mgd_workspace_errors(ws) == 0
+    assert torch.equal(out[0], fresh[0]) and torch.equal(out[1], fresh[1])
+    # a buffer last used by a SnapKV call: detected if its counters were left nonzero,
+    # otherwise the call is clean
+    ops.snapkv_select(qw, k, v, kv_len, 32, 7, 128, ws=ws)
+    torch.cuda.synchronize()
+    dirty = bool(hdr[2:5].any()) or bool(hdr[6:8].any())
+    out = ops.verify_attn(q, k, v, kv_len, ws=ws)
+    flags = mgd.mgd_workspace_errors(ws)
+    if dirty:
+        assert flags & mgd.MGD_DEVERR_STALE_WS
+    else:
+        assert flags == 0
+        assert torch.equal(out[0], fresh[0]) and torch.equal(out[1], fresh[1])
+    ref, _ = ref_attention(q[:2].cpu(), k[:2].cpu(), v[:2].cpu(), kv_len[:2].cpu(), 1.0 / math.sqrt(128))
+    assert_attention_close(fresh[0][:2], ref)

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from _parity import gpu_or_skip
+from _parity import Guarded, check_guards, gpu_or_skip
 from long_context_speculative_split_gb300 import mgd, ops
 from oracle.commit import commit_round as ref_commit
 
@@ -35,11 +35,14 @@ def test_commit_matches_oracle(dtype, gamma):
                                                       kd.view(torch.int16) if dtype == torch.bfloat16 else kd,
                                                       vd.view(torch.int16) if dtype == torch.bfloat16 else vd, draft_len)
     assert bad[3] and bad[5] and bad[7]
-    kl_d, dl_d = kv_len.to(dev), draft_len.to(dev)
-    kd_d, vd_d = kd.to(dev), vd.to(dev)
+    # the updated arrays between poisoned guard regions
+    g = dict(kv_len=Guarded((B,), torch.int32, dev, init=kv_len), draft_len=Guarded((B,), torch.int32, dev, init=draft_len),
+             k_draft=Guarded(tuple(kd.shape), dtype, dev, init=kd), v_draft=Guarded(tuple(vd.shape), dtype, dev, init=vd))
+    kl_d, dl_d, kd_d, vd_d = g["kv_len"].t, g["draft_len"].t, g["k_draft"].t, g["v_draft"].t
     ws = ops.workspace(mgd.mgd_commit_workspace_size(B), dev)
     ops.commit_round(nacc.to(dev), gamma, kl_d, k.to(dev), v.to(dev), kd_d, vd_d, dl_d, ws=ws)
     assert mgd.mgd_workspace_errors(ws) & mgd.MGD_DEVERR_COMMIT
+    check_guards(**g)
     np.testing.assert_array_equal(kl_d.cpu().numpy(), ref_len)
     np.testing.assert_array_equal(dl_d.cpu().numpy(), ref_dl)
     view = (lambda t: t.cpu().view(torch.int16).numpy()) if dtype == torch.bfloat16 else (lambda t: t.cpu().numpy())

@@ -9,9 +9,11 @@ import numpy as np
 import pytest
 import torch
 
-from _parity import assert_index_sets_match, gpu_or_skip
+from _parity import (Guarded, assert_attention_close, assert_index_sets_match, assert_lse_close, check_guards,
+                     gpu_or_skip, is_poison)
 from long_context_speculative_split_gb300 import ops
 from long_context_speculative_split_gb300 import workloads as wl
+from oracle.attention import draft_attention as ref_draft
 from oracle.snapkv import max_pool, select_indices, snapkv_select as ref_select, window_scores
 
 pytestmark = pytest.mark.gpu
@@ -35,7 +37,7 @@ def _check_pair(res, k, v, b, h, L, W, P, K, ref_scores_row, D):
     if res["scores"] is not None and n > 0:
         gs = res["scores"][b, h, :n].double().cpu().numpy()
         np.testing.assert_allclose(gs, pooled[:n], rtol=1e-4, atol=1e-9)
-    return ndiff
+    return ndiff, ref_idx
 
 
 def test_tiny_config_float32_full():
@@ -81,8 +83,19 @@ def test_bf16_cases_match_oracle(case):
     kv_len = torch.tensor(lens, dtype=torch.int32)
     k, v = wl.kv_cache(cfg, dev, seed=3, kv_len=kv_len, cap=cap)
     qw = wl.window_queries(cfg, dev, seed=3)
-    res = ops.snapkv_select(qw, k, v, kv_len.to(dev), W, P, K, want_scores=True)
+    # every output between poisoned guard regions; the draft cache has 64 spare rows per
+    # (sequence, KV head) that the call must leave as they are (poisoned here)
+    dcap = K + 64
+    g = dict(sel_idx=Guarded((B, Hkv, dcap), torch.int32, dev), k_draft=Guarded((B, Hkv, dcap, D), k.dtype, dev),
+             v_draft=Guarded((B, Hkv, dcap, D), k.dtype, dev), draft_len=Guarded((B,), torch.int32, dev),
+             scores=Guarded((B, Hkv, cap), torch.float32, dev, init=torch.zeros(())))
+    res = ops.snapkv_select(qw, k, v, kv_len.to(dev), W, P, K, draft_cap=dcap, want_scores=True,
+                            out={n: x.t for n, x in g.items()})
     torch.cuda.synchronize()
+    check_guards(**g)
+    for b in range(B):
+        keff = min(K, lens[b])
+        assert bool(is_poison(res["k_draft"][b, :, keff:]).all()) and bool(is_poison(res["v_draft"][b, :, keff:]).all())
     s = window_scores(qw, k, kv_len, W, 1.0 / math.sqrt(D))
     for b in range(B):
         for h in range(Hkv):
@@ -93,23 +106,42 @@ def test_bf16_cases_match_oracle(case):
                          ids=["b32_ctx8k", "b128_ctx32k", "ragged_b256_ctx4k_64k"])
 def test_full_size_sampled(name, seed):
     """Full-size workloads (including ragged lengths 4k-64k at batch 256) with sampled pairs:
-    the first, the last, the longest sequence's and one random (sequence, KV head)."""
+    the first, the last, the longest sequence's and one random (sequence, KV head).  Then the
+    draft step over the selected caches: draft attention over each sampled pair's compacted
+    cache is compared with the oracle's draft attention over the oracle's own selection,
+    gathered from the input cache (where the two index sets differ inside the tie band the
+    outputs legitimately differ and only the selection check above applies)."""
     dev = gpu_or_skip()
     c = wl.WORKLOADS[name]
     kv_len = wl.lengths(c)
     k, v = wl.kv_cache(c, dev, kv_len=kv_len, cap=wl.capacity(c))
     qw = wl.window_queries(c, dev)
     res = ops.snapkv_select(qw, k, v, kv_len.to(dev), c["W"], c["pool"], c["K"], want_scores=True)
+    qd = wl.draft_queries(c, dev)
+    dout, dlse = ops.draft_attn(qd, res["k_draft"], res["v_draft"], res["draft_len"])
     torch.cuda.synchronize()
-    G = c["Hq"] // c["Hkv"]
+    assert bool(torch.isfinite(dout).all()) and bool(torch.isfinite(dlse).all())
+    G, D = c["Hq"] // c["Hkv"], c["D"]
+    scale = 1.0 / math.sqrt(D)
     rng = np.random.default_rng(seed)
     pairs = [(0, 0), (c["B"] - 1, c["Hkv"] - 1), (int(np.argmax(kv_len.numpy())), 3),
              (int(rng.integers(c["B"])), int(rng.integers(c["Hkv"])))]
+    drafts_compared = 0
     for b, h in pairs:
         L = int(kv_len[b])
-        s = window_scores(qw[b:b + 1, :, h * G:(h + 1) * G], k[b:b + 1, h:h + 1, :L], kv_len[b:b + 1], c["W"],
-                          1.0 / math.sqrt(c["D"]))
-        _check_pair(res, k, v, b, h, L, c["W"], c["pool"], c["K"], s[0, 0], c["D"])
+        hs = slice(h * G, (h + 1) * G)
+        s = window_scores(qw[b:b + 1, :, hs], k[b:b + 1, h:h + 1, :L], kv_len[b:b + 1], c["W"], scale)
+        ndiff, ref_idx = _check_pair(res, k, v, b, h, L, c["W"], c["pool"], c["K"], s[0, 0], c["D"])
+        if ndiff:
+            continue
+        sel = torch.from_numpy(np.asarray(ref_idx, dtype=np.int64))
+        kd = k[b, h, :L].cpu()[sel][None, None]
+        vd = v[b, h, :L].cpu()[sel][None, None]
+        ref, ref_lse = ref_draft(qd[b:b + 1, :, hs], kd, vd, torch.tensor([len(ref_idx)]), scale)
+        assert_attention_close(dout[b:b + 1, hs], ref[:, 0], "draft[b=%d,h=%d]" % (b, h))
+        assert_lse_close(dlse[b:b + 1, hs], ref_lse[:, 0])
+        drafts_compared += 1
+    assert drafts_compared >= len(pairs) - 1
     del k, v
     torch.cuda.empty_cache()
 
