@@ -47,28 +47,29 @@ __device__ __forceinline__ void raise_error_sr(WsHeader *hdr, unsigned bit) {
 // error word the next call will use and advances seq, so the workspace is ready
 // for the next call with no clearing launch in between.  It also checks two
 // sums against the values a call started from a ready header produces: the
-// successful claims (`expect`) and the block ids of the check-ins.  A header
-// left dirty by other use (a stale next_unit skips units; a stale done ends the
-// call early; stale sums) breaks one of them, and the call raises
-// MGD_DEVERR_STALE_WS unless one of its waits timed out (which stops claiming).
+// successful claims (`expect`) and the block ids of the check-ins, which come
+// with the check-in count in one atomic word.  A header left dirty by other use
+// (a stale next_unit skips units; a stale count ends the call early; stale
+// sums) breaks one of them, and the call raises MGD_DEVERR_STALE_WS unless one
+// of its waits timed out (which stops claiming).
 __device__ __forceinline__ void call_check_in(WsHeader *hdr, unsigned parts, unsigned id, unsigned claims,
                                               unsigned expect) {
   if (claims) atomicAdd(&hdr->claimed, claims);
-  atomicAdd(&hdr->ids, id + 1u);
   __threadfence();
-  if (atomicAdd(&hdr->done, 1u) == parts - 1u) {
+  const unsigned long long mine = (1ull << 40) + id + 1ull;
+  const unsigned long long now = atomicAdd(&hdr->done_ids, mine) + mine;
+  if ((now >> 40) == parts) {
     __threadfence();
     volatile unsigned *h = reinterpret_cast<volatile unsigned *>(hdr);
     const unsigned s = h[offsetof(WsHeader, seq) / 4];
     const unsigned got = h[offsetof(WsHeader, claimed) / 4];
-    const unsigned ids = h[offsetof(WsHeader, ids) / 4];
-    const unsigned all_ids = static_cast<unsigned>((static_cast<unsigned long long>(parts) * (parts + 1ull)) / 2ull);
-    if ((got != expect || ids != all_ids) && !(h[s & 1u] & 0x8u)) atomicOr(&hdr->err[s & 1u], 0x20u);
+    const unsigned long long all_ids = (static_cast<unsigned long long>(parts) * (parts + 1ull)) / 2ull;
+    if ((got != expect || (now & ((1ull << 40) - 1ull)) != all_ids) && !(h[s & 1u] & 0x8u))
+      atomicOr(&hdr->err[s & 1u], 0x20u);
     h[offsetof(WsHeader, next_unit) / 4] = 0u;
     h[offsetof(WsHeader, next_unit2) / 4] = 0u;
     h[offsetof(WsHeader, claimed) / 4] = 0u;
-    h[offsetof(WsHeader, ids) / 4] = 0u;
-    h[offsetof(WsHeader, done) / 4] = 0u;
+    *reinterpret_cast<volatile unsigned long long *>(&hdr->done_ids) = 0ull;
     h[(s + 1u) & 1u] = 0u;  // err[(s + 1) & 1]
     h[offsetof(WsHeader, seq) / 4] = s + 1u;
   }
@@ -137,15 +138,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete may
+// be parked by the hardware until it completes or `hint_ns` pass, instead of
+// polling; parked warps leave their issue slots to the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_parked(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kParkNs = 1000000;  // 1 ms per parked try; the overall limit is kWaitLimitNs
+
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // (and the caller must unwind) when kWaitLimitNs elapsed first.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_parked(bar, parity, kParkNs)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }

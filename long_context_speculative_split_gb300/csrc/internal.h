@@ -22,16 +22,17 @@ struct WsHeader {
   unsigned err[2];
   unsigned next_unit;  // dynamic work counter of persistent kernels
   unsigned next_unit2;
-  unsigned done;  // end-of-call check-ins of the self-resetting kernels
-  unsigned seq;   // calls completed by the self-resetting kernels on this workspace
+  unsigned seq;  // calls completed by the self-resetting kernels on this workspace
   // Successful claims from next_unit, summed at check-in.  From a zero start a
   // self-resetting call's claims add up to a known count; any other sum means
   // the call started from a header that was not left ready (MGD_DEVERR_STALE_WS).
   unsigned claimed;
-  // Sum of (block index + 1) over the check-ins so far: at the last check-in of a call
-  // started from a ready header it is parts * (parts + 1) / 2 (a stale `done` makes a
-  // check-in look like the last one while other CTAs have not checked in yet).
-  unsigned ids;
+  // End-of-call check-ins of the self-resetting kernels, one 64-bit word updated
+  // by one atomic per check-in: bits 40..63 count the check-ins, bits 0..39 sum
+  // (block index + 1) over them.  The value a check-in gets back therefore says
+  // exactly which blocks had checked in: at the last check-in of a call started
+  // from a ready header the sum is parts * (parts + 1) / 2.
+  unsigned long long done_ids;
   unsigned pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");

@@ -327,9 +327,11 @@ def test_stale_workspace_is_detected():
                mgd.mgd_snapkv_workspace_size(40, 32, 8, 128, 1000, 32))
     fresh = ops.verify_attn(q, k, v, kv_len, ws=ops.workspace(need, dev))
     ws = ops.workspace(need, dev)
-    hdr = ws[:256].view(torch.int32)   # err[0], err[1], next_unit, next_unit2, done, seq, claimed, ids, ...
+    # err[0], err[1], next_unit, next_unit2, seq, claimed, then the 64-bit check-in word (low: id sum,
+    # high: id-sum bits 32..39 and the check-in count << 8)
+    hdr = ws[:256].view(torch.int32)
     # a stale work counter (small, past every unit); a stale check-in count; stale sums
-    for field, value in ((2, 5), (2, 100000), (4, 3), (4, 1), (6, 2), (7, 9)):
+    for field, value in ((2, 5), (2, 100000), (7, 3 << 8), (7, 1 << 8), (5, 2), (6, 9)):
         ws.zero_()
         hdr[field] = value
         ops.verify_attn(q, k, v, kv_len, ws=ws)
@@ -343,7 +345,7 @@ def test_stale_workspace_is_detected():
     # otherwise the call is clean
     ops.snapkv_select(qw, k, v, kv_len, 32, 7, 128, ws=ws)
     torch.cuda.synchronize()
-    dirty = bool(hdr[2:5].any()) or bool(hdr[6:8].any())
+    dirty = bool(hdr[2:4].any()) or bool(hdr[5:8].any())
     out = ops.verify_attn(q, k, v, kv_len, ws=ws)
     flags = mgd.mgd_workspace_errors(ws)
     if dirty:
