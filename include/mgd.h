@@ -16,15 +16,15 @@
  *     the caller's `ws` buffer of at least the size the matching
  *     mgd_*_workspace_size() returns for the same shape.
  *   - A workspace is ZERO-FILLED once before its first use (e.g. one
- *     cudaMemsetAsync after allocating it).  The attention calls
- *     (mgd_verify_attn, mgd_draft_attn) and mgd_commit_round do not clear
- *     its header per call:
- *     their kernels leave the counters at zero for the next call, which saves
- *     a clearing launch ahead of every attention launch.  The other calls
- *     clear the part they use themselves.  A buffer that served as scratch for
- *     anything but attention calls is zero-filled again before an attention
- *     call uses it.  An attention call that starts from a header in any other
- *     state (its work counters not at zero) detects it at its end and raises
+ *     cudaMemsetAsync after allocating it).  The attention, sampling and
+ *     commit calls (mgd_verify_attn, mgd_draft_attn, mgd_spec_sample,
+ *     mgd_commit_round) do not clear it per call: their kernels leave its
+ *     counters at zero for the next call, which saves a clearing launch ahead
+ *     of every launch.  mgd_snapkv_select and mgd_topk_draft_attn clear the
+ *     part they use themselves.  A buffer that served as scratch for another
+ *     kind of call is zero-filled again before it serves one of the former.
+ *     An attention or commit call that starts from a header in any other state
+ *     (its counters not at zero) detects it at its end and raises
  *     MGD_DEVERR_STALE_WS: its outputs are then unspecified, and the workspace
  *     is zero-filled again before the next call.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
@@ -109,6 +109,17 @@ mgd_status mgd_workspace_errors(const void *ws, void *stream, uint32_t *flags);
  */
 #define MGD_SELFTEST_WS_BYTES 512u
 mgd_status mgd_selftest_bounded_wait(int which, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Launch mode of every later call in the process.  By default (enable != 0)
+ * the kernels of consecutive calls on one stream are launched with
+ * programmatic stream serialization: a kernel may be scheduled, and do set-up
+ * that touches no memory, while the previous kernel in the stream finishes; it
+ * waits for that kernel's completion (and memory) before any access.  With
+ * enable == 0 every kernel is launched plainly, after the previous one ends.
+ * Results are the same either way; this switch exists for comparisons.
+ */
+void mgd_set_programmatic_launch(int enable);
 
 /*
  * Diagnostic: holds SMs for a while, so that a test can run another call on a
@@ -354,15 +365,17 @@ mgd_status mgd_commit_round(const int32_t *num_accepted, int B, int gamma, int H
  * memory.  The call allocates nothing.
  *   - Limit: the scratch it needs, mgd_spec_workspace_size(B, gamma, V), must
  *     fit in MGD_NOALLOC_SCRATCH_BYTES (about B * ((2*gamma+1) * ceil(V/16384) * 8
- *     + 4) + 512 bytes; e.g. B <= 1807 at gamma = 4, V = 128256); larger requests
- *     return MGD_ERR_UNSUPPORTED with an explanation in mgd_last_error().
+ *     + ceil(V/2048) * 8 + 4) + 512 bytes; e.g. B <= 966 at gamma = 4,
+ *     V = 128256); larger requests return MGD_ERR_UNSUPPORTED with an
+ *     explanation in mgd_last_error().
  *   - Every call looks up the array's device address on the current device
  *     with cudaGetSymbolAddress (a host-side lookup, so the address is never
  *     stale, e.g. after a device reset).  The first call on a device may also
  *     load the library's device code there; make that first call before any
  *     stream capture.
- *   - Every call shares the one array, which keeps the last call's contents
- *     (the error word at its start is cleared by each call).  Calls that
+ *   - Every call shares the one array, which keeps the last call's contents;
+ *     each call leaves its counters at zero for the next one (the array is
+ *     zero when the library is loaded).  Calls that
  *     overlap on the GPU (different streams or host threads) race on it and
  *     must be serialised by the caller.  The device error word of this
  *     variant is not readable through mgd_workspace_errors.

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -116,6 +117,11 @@ mgd_status run_attention(const void *q, const void *k, const void *v, const int3
 
 }  // namespace
 
+namespace {
+std::atomic<int> g_pdl{1};
+}  // namespace
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+
 // Sets the calling thread's mgd_last_error() text (for entry points defined in
 // other translation units).
 void record_error(const char *msg) { g_last_error = msg; }
@@ -201,6 +207,8 @@ mgd_status mgd_selftest_bounded_wait(int which, void *ws, size_t ws_bytes, void 
   cudaError_t e = launch_selftest_wait(which, ws, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e, "self-test launch");
 }
+
+void mgd_set_programmatic_launch(int enable) { g_pdl.store(enable ? 1 : 0, std::memory_order_relaxed); }
 
 mgd_status mgd_selftest_occupy(int ctas, int smem_bytes, int usec, void *stream) {
   if (ctas < 1 || ctas > 65535) return fail(MGD_ERR_INVALID_ARG, "ctas must be in [1, 65535] (got %d)", ctas);

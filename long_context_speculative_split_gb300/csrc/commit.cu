@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(256)
                   int32_t *__restrict__ draft_len, const unsigned char *__restrict__ k,
                   const unsigned char *__restrict__ v, unsigned char *__restrict__ kd, unsigned char *__restrict__ vd,
                   CommitParams p, WsHeader *hdr) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.x;
   const int n = num_accepted[b], L = kv_len[b], dl = draft_len[b];
   const bool ok = commit_valid(n, L, dl, p);
@@ -79,10 +81,10 @@ cudaError_t launch_commit(const int32_t *num_accepted, int B, int gamma, int Hkv
   p.kv_hstride = kv_hstride * esz;
   p.d_bstride = d_bstride * esz;
   p.d_hstride = d_hstride * esz;
-  commit_kernel<<<B, 256, 0, stream>>>(num_accepted, kv_len, draft_len, static_cast<const unsigned char *>(k),
-                                       static_cast<const unsigned char *>(v), static_cast<unsigned char *>(k_draft),
-                                       static_cast<unsigned char *>(v_draft), p, static_cast<WsHeader *>(ws));
-  return cudaGetLastError();
+  return launch_pdl(commit_kernel, dim3(B), dim3(256), 0, stream, num_accepted, kv_len, draft_len,
+                    static_cast<const unsigned char *>(k), static_cast<const unsigned char *>(v),
+                    static_cast<unsigned char *>(k_draft), static_cast<unsigned char *>(v_draft), p,
+                    static_cast<WsHeader *>(ws));
 }
 
 }  // namespace mgd

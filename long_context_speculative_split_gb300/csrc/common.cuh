@@ -12,9 +12,37 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "internal.h"
 
 namespace mgd {
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// The timed kernels are launched with programmatic stream serialization
+// (launch_pdl), so the next kernel in the stream can be scheduled and run its
+// set-up while this one finishes.  Each of them lets its dependents launch at
+// entry and calls pdl_wait() before it touches global memory: the wait returns
+// once the preceding kernel has completed and its writes are visible, and since
+// every kernel launched this way waits, completion stays ordered along a chain.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- time / errors
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -207,6 +235,15 @@ __device__ __forceinline__ void tma_load_4d_hint(void *dst, const void *tmap, ui
       " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
       : "memory");
+}
+// 4-D tiled prefetch of a box into L2: no shared memory, nothing to wait for,
+// and no memory changed (L2 is the point of coherence, so a prefetch issued
+// while another kernel writes the same lines cannot leave a stale copy).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void *tmap, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
 }
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses of the same bytes.

@@ -38,6 +38,10 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 constexpr size_t kAlign = 256;
+
+// Whether kernels are launched with programmatic stream serialization
+// (mgd_set_programmatic_launch; on by default).
+bool pdl_enabled();
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
 // Number of SMs of the current device (152 on GB300 when no device is visible,
@@ -148,10 +152,11 @@ cudaError_t launch_selftest_occupy(int ctas, int smem_bytes, int usec, cudaStrea
 // ------------------------------------------------------------------ sampling
 struct SpecPlan {
   int B, gamma, V;
-  int split;     // elements per statistics block
+  int split;     // elements per statistics block (and per CTA of the draw kernels)
   int nsplit;    // ceil(V / split)
+  int nsub;      // ceil(V / 2048): sub-ranges of a row (one warp each)
   int nrows;     // 2*gamma + 1 rows per sequence (gamma+1 target, gamma draft)
-  size_t off_tickets, off_stats, ws_bytes;
+  size_t off_tickets, off_stats, off_sub, ws_bytes;
 };
 SpecPlan plan_spec(int B, int gamma, int V);
 

@@ -262,6 +262,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Ws
 __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
     snap_score_fused(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                      const int32_t *__restrict__ kv_len, unsigned char *__restrict__ ws, T5Params p) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T5Layout::off_bar);
@@ -623,8 +625,8 @@ cudaError_t launch_snap_score_tc05(const SnapPlan &pl, const SnapArgs &a, const 
   // persistent grid: two CTAs per SM (what the kernel's registers and shared
   // memory allow); a CTA that only starts after others finished finds no job
   const int grid = std::min(kp.units, kT5CtasPerSm * current_sm_count());
-  kern<<<grid, kT5Threads, T5Layout::alloc, a.stream>>>(kmap, qmap, a.kv_len, static_cast<unsigned char *>(a.ws), kp);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kT5Threads), T5Layout::alloc, a.stream, kmap, qmap, a.kv_len,
+                    static_cast<unsigned char *>(a.ws), kp);
 }
 
 }  // namespace mgd

@@ -708,6 +708,8 @@ __global__ void __launch_bounds__(kSelThreads, 2)
                 unsigned char *__restrict__ k_draft, unsigned char *__restrict__ v_draft,
                 int32_t *__restrict__ draft_len, float *__restrict__ scores_out, unsigned char *__restrict__ ws,
                 size_t off_scores, size_t off_pooled) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ unsigned hist[2048];
   __shared__ unsigned sm_warp[33];
   __shared__ unsigned s_bin, s_above;
@@ -1103,11 +1105,10 @@ cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, cons
   sp.row_bytes = p.D * (in_f32 ? 4 : 2);
   sp.bstride_bytes = a.kv_batch_stride * (in_f32 ? 4 : 2);
   sp.hstride_bytes = a.kv_head_stride * (in_f32 ? 4 : 2);
-  snap_select<<<p.pairs, kSelThreads, 0, a.stream>>>(
-      static_cast<const unsigned char *>(a.k), static_cast<const unsigned char *>(a.v), a.kv_len, sp, a.sel_idx,
-      static_cast<unsigned char *>(a.k_draft), static_cast<unsigned char *>(a.v_draft), a.draft_len, a.scores_out,
-      ws, p.off_scores, p.off_pooled);
-  return cudaGetLastError();
+  return launch_pdl(snap_select, dim3(p.pairs), dim3(kSelThreads), 0, a.stream, static_cast<const unsigned char *>(a.k),
+                    static_cast<const unsigned char *>(a.v), a.kv_len, sp, a.sel_idx,
+                    static_cast<unsigned char *>(a.k_draft), static_cast<unsigned char *>(a.v_draft), a.draft_len,
+                    a.scores_out, ws, p.off_scores, p.off_pooled);
 }
 
 }  // namespace mgd

@@ -8,33 +8,42 @@
 // accepted one more target token is drawn.  The paragraph after it: this
 // preserves the target distribution.
 //
-// A draft step's draw of one draft row is one kernel (spec_draw_row: the
-// statistics of every slice, then the CTA completing a sequence draws its
-// token from the slice holding u * Z).  Otherwise two kernels per call:
-//   1. spec_stats: (max, sum of exp) of every logit row the mode needs, each
-//      row split over several small CTAs (HBM stream, float4 loads, full
-//      occupancy);
-//   2. spec_finish: one CTA of 1024 threads per sequence merges the row
-//      statistics, tests all candidates at once (u1 * q(x) < p(x)) and keeps
-//      the prefix before the first rejection, then draws the correction /
-//      bonus (or, in draft mode, the draft token) by inverse CDF in two
-//      levels: 32 warps each sum a contiguous slice of the weights, a
-//      double-precision prefix over the 32 slice totals finds the slice
-//      holding u * Z, and the whole block scans that slice to find the first
-//      index whose running sum exceeds u * Z.  Softmax draws start from the
-//      statistics slice that holds u * Z, so only that slice is read.
+// Every draw is an inverse-CDF draw in three levels over a vocab row: the row
+// is cut into sub-ranges of 2048 entries (one warp each), whose weight sums
+// locate the sub-range holding u * Z; the CTA that completes a sequence scans
+// only that sub-range, 8 entries per thread held in registers, with a block
+// scan ordering the threads.  Sums of sub-range weights are float; their
+// running prefix is double.
+//
+//   spec_draw_row: a draft step's draw of one draft row per sequence.  Every
+//     warp streams one sub-range and records its (max, sum of exp); the CTA
+//     completing a sequence (atomic ticket) merges the sub-range records and
+//     draws.  One launch.
+//   spec_stats + spec_decide: rejection sampling.  spec_stats computes
+//     (max, sum of exp) of each 16384-entry slice of every logit row;
+//     spec_decide runs over (sequence, 16384-entry chunk): every CTA of a
+//     sequence merges the row statistics and takes the same acceptance
+//     decisions (u * q(x) < p(x) for each candidate, the chain keeps the prefix
+//     before the first rejection), then sums the weights of the final draw --
+//     the residual max(0, p - q) at the first rejection (and p itself, in case
+//     the residual vanishes through rounding), or p of the bonus row -- over its
+//     chunk, one warp per sub-range; the CTA completing the sequence draws.
+//
+// No clearing launch: the tickets go back to zero when a sequence completes,
+// and the workspace header resets itself at the last completing CTA's check-in.
 #include "common.cuh"
 
 namespace mgd {
 namespace {
 
 constexpr int kStatThreads = 256;
-constexpr int kThreads = 1024;  // finish kernel
-constexpr int kWarps = kThreads / 32;
+constexpr int kWarps = kStatThreads / 32;
+constexpr int kSub = 2048;                 // entries per sub-range (one warp)
+constexpr int kChunk = kWarps * kSub;      // entries per CTA of the draw kernels (= the statistics split)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct StatParams {
-  int B, gamma, V, split, nsplit, nrows;
+  int B, gamma, V, split, nsplit, nrows, nsub;
   int r_begin, nr;  // rows [r_begin, r_begin + nr) of every sequence (unified row index)
 };
 
@@ -93,7 +102,7 @@ __device__ float2 slice_stats(const float *__restrict__ x, int lo, int hi) {
     }
   }
   // block reduce of (m, l)
-  __shared__ float sm[2][kStatThreads / 32];
+  __shared__ float sm[2][kWarps];
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
     const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
@@ -111,10 +120,10 @@ __device__ float2 slice_stats(const float *__restrict__ x, int lo, int hi) {
   float2 r = make_float2(-INFINITY, 0.f);
   if (threadIdx.x == 0) {
     float M = -INFINITY;
-    for (int i = 0; i < kStatThreads / 32; ++i) M = fmaxf(M, sm[0][i]);
+    for (int i = 0; i < kWarps; ++i) M = fmaxf(M, sm[0][i]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
     float Lt = 0.f;
-    for (int i = 0; i < kStatThreads / 32; ++i) Lt += sm[1][i] * exp2f((sm[0][i] - Mu) * kLog2e);
+    for (int i = 0; i < kWarps; ++i) Lt += sm[1][i] * exp2f((sm[0][i] - Mu) * kLog2e);
     r = make_float2(M, Lt);
   }
   return r;
@@ -124,6 +133,8 @@ template <bool VEC4>
 __global__ void __launch_bounds__(kStatThreads) spec_stats_kernel(const float *__restrict__ target,
                                                                    const float *__restrict__ draft, StatParams sp,
                                                                    float2 *__restrict__ stats) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.x / sp.nr;
   const int r = sp.r_begin + blockIdx.x % sp.nr;
   const int s = blockIdx.y;
@@ -132,34 +143,248 @@ __global__ void __launch_bounds__(kStatThreads) spec_stats_kernel(const float *_
   if (threadIdx.x == 0) stats[(static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit + s] = st;
 }
 
-// One draft-token draw of a single draft row per sequence (a draft step):
-// every CTA computes one slice's statistics; the CTA that completes a
-// sequence's statistics (atomic ticket) draws its token.  The slice totals
-// locate the slice holding u * Z; the block scans that slice: each thread sums
-// a contiguous segment, warp scans order the threads, one warp turns the
-// running double sum into a float target per warp, and the first thread whose
-// range [excl, incl) holds the target walks its segment.
+// Weights of a draw, as a function of the entry index: kind 0 -> exp(a - Ma) *
+// ia (a softmax); kind 1 -> max(0, exp(a - Ma) * ia - exp(c - Mc) * ic) (the
+// residual p - q).  ia, ic are the reciprocal normalisers.
+struct Weights {
+  const float *a;
+  const float *c;
+  float Ma, ia, Mc, ic;
+  int kind;
+  __device__ __forceinline__ float operator()(float av, float cv) const {
+    const float pa = exp2f((av - Ma) * kLog2e) * ia;
+    if (kind == 0) return pa;
+    return fmaxf(0.f, pa - exp2f((cv - Mc) * kLog2e) * ic);
+  }
+};
+
+// The 8 entries [i, i + 8) of a weight row (zero at or past `hi`).  With VEC4,
+// i is a multiple of 8 and the rows are 16-byte aligned.
+template <bool VEC4>
+__device__ __forceinline__ void weights8(const Weights &w, int i, int hi, float (&out)[8]) {
+  float a[8], c[8];
+  if (VEC4 && i + 7 < hi) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float4 fa = __ldg(reinterpret_cast<const float4 *>(w.a + i + 4 * h));
+      a[4 * h] = fa.x, a[4 * h + 1] = fa.y, a[4 * h + 2] = fa.z, a[4 * h + 3] = fa.w;
+      if (w.kind == 1) {
+        const float4 fc = __ldg(reinterpret_cast<const float4 *>(w.c + i + 4 * h));
+        c[4 * h] = fc.x, c[4 * h + 1] = fc.y, c[4 * h + 2] = fc.z, c[4 * h + 3] = fc.w;
+      } else {
+        c[4 * h] = c[4 * h + 1] = c[4 * h + 2] = c[4 * h + 3] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) out[e] = w(a[e], c[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (i + e < hi) {
+        a[e] = __ldg(w.a + i + e);
+        c[e] = (w.kind == 1) ? __ldg(w.c + i + e) : 0.f;
+        out[e] = w(a[e], c[e]);
+      } else {
+        out[e] = 0.f;
+      }
+    }
+  }
+}
+
+struct DrawShared {
+  double pre;      // weight before the chosen sub-range, subtracted from the target
+  int sub;         // chosen sub-range, -1 if every weight is zero
+  int tidx;        // first thread whose range holds the target
+  int tok;
+  float wsum[kWarps];
+  float trel[kWarps];
+};
+
+// Warp 0: pick the sub-range holding u * Z among n sub-ranges of weight
+// wsum(q) (a function evaluated the same way on every call).  Lane L sums a
+// contiguous block of sub-ranges, a double scan over the lanes locates the
+// block holding the target, and that lane walks its block.  Sets sh.sub (-1
+// when Z == 0) and sh.pre (the target measured from the sub-range start); a
+// target past the total (rounding) picks the last sub-range with weight with
+// sh.pre = -1, so that its last entry with weight is drawn.
+template <typename F>
+__device__ __forceinline__ void pick_sub(F wsum, int n, float u, DrawShared &sh) {
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) / 32;
+  const int q0 = min(n, lane * per), q1 = min(n, q0 + per);
+  double ls = 0.0;
+  for (int q = q0; q < q1; ++q) ls += static_cast<double>(wsum(q));
+  double incl = ls;
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const double Z = __shfl_sync(0xffffffffu, incl, 31);
+  const double tgt = static_cast<double>(u) * Z;
+  const unsigned hit = __ballot_sync(0xffffffffu, ls > 0.0 && incl > tgt);
+  const unsigned mass = __ballot_sync(0xffffffffu, ls > 0.0);
+  if (lane == 0) sh.sub = -1;
+  __syncwarp();
+  if (hit) {
+    if (lane == __ffs(hit) - 1) {
+      double run = incl - ls;
+      int pick = -1, last = -1;
+      for (int q = q0; q < q1 && pick < 0; ++q) {
+        const double w = static_cast<double>(wsum(q));
+        if (w > 0.0) {
+          last = q;
+          if (run + w > tgt) pick = q;
+          else run += w;
+        }
+      }
+      sh.sub = pick >= 0 ? pick : last;
+      sh.pre = pick >= 0 ? tgt - run : -1.0;
+    }
+  } else if (mass) {  // rounding pushed u * Z past the total: the last sub-range with weight
+    if (lane == 31 - __clz(mass)) {
+      int last = -1;
+      for (int q = q0; q < q1; ++q)
+        if (wsum(q) > 0.f) last = q;
+      sh.sub = last;
+      sh.pre = -1.0;  // take its last entry with weight
+    }
+  }
+}
+
+// The whole block: draw inside sub-range sub ([sub * kSub, ...) of the row),
+// target sh.pre measured from the sub-range start.  Thread t covers 8 entries;
+// the block scan gives each warp a float target relative to its start, and the
+// first thread whose range [excl, incl) holds it walks its 8 weights.  A target
+// past the scanned total (rounding), or sh.pre < 0, takes the last entry with
+// weight.  Returns the token (every thread).
+template <bool VEC4>
+__device__ int draw_in_sub(const Weights &w, int V, DrawShared &sh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lo = sh.sub * kSub;
+  const int hi = min(V, lo + kSub);
+  const int i0 = lo + 8 * static_cast<int>(threadIdx.x);
+  float v[8];
+  weights8<VEC4>(w, i0, hi, v);
+  float ts = 0.f;
+  int lastpos = -1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ts += v[e];
+    if (v[e] > 0.f) lastpos = i0 + e;
+  }
+  float incl = ts;
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.f;
+  if (lane == 31) sh.wsum[warp] = incl;
+  if (threadIdx.x == 0) {
+    sh.tidx = 0x7fffffff;
+    sh.tok = -1;
+  }
+  __syncthreads();
+  if (warp == 0) {  // per-warp float targets from a double scan of the warp totals
+    const double x0 = (lane < kWarps) ? static_cast<double>(sh.wsum[lane]) : 0.0;
+    double ix = x0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, ix, o);
+      if (lane >= o) ix += y;
+    }
+    if (lane < kWarps) sh.trel[lane] = fmaxf(0.f, static_cast<float>(sh.pre - (ix - x0)));
+  }
+  // the last entry with weight in the whole sub-range (rounding fallback)
+  int lp = lastpos;
+  for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+  if (lane == 0 && lp >= 0) atomicMax(&sh.tok, lp);
+  __syncthreads();
+  const float trel = sh.trel[warp];
+  if (sh.pre >= 0.0 && ts > 0.f && excl <= trel && incl > trel) atomicMin(&sh.tidx, static_cast<int>(threadIdx.x));
+  __syncthreads();
+  if (static_cast<int>(threadIdx.x) == sh.tidx) {
+    float c = excl;
+    int p = -1;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      c += v[e];
+      if (p < 0 && v[e] > 0.f && c > trel) p = i0 + e;
+    }
+    sh.tok = (p >= 0) ? p : lastpos;  // the crossing is here; rounding: this thread's last entry with weight
+  }
+  __syncthreads();
+  return sh.tok;
+}
+
+// One draft-token draw of a single draft row per sequence (a draft step).
+// CTA (b, s) streams entries [s * kChunk, ...) of the row; warp w keeps the
+// (max, sum of exp) of its sub-range s * kWarps + w.  The CTA completing the
+// sequence merges the sub-range records into weights relative to the row max
+// and draws.
 template <bool VEC4>
 __global__ void __launch_bounds__(kStatThreads) spec_draw_row_kernel(const float *__restrict__ draft,
                                                                       int32_t *__restrict__ draft_tokens,
                                                                       const float *__restrict__ u, StatParams sp,
-                                                                      float2 *__restrict__ stats,
-                                                                      unsigned *__restrict__ tickets) {
-  constexpr int kW = kStatThreads / 32;
-  __shared__ int s_last, s_slice, s_tidx, s_lastpos;
-  __shared__ float s_M, s_trel[kW], s_wsum[kW];
-  __shared__ double s_pre;
+                                                                      float2 *__restrict__ sub,
+                                                                      unsigned *__restrict__ tickets, WsHeader *hdr) {
+  pdl_launch_dependents();
+  {  // warm L2 with this CTA's 64 KB of the row while the previous kernel finishes (prefetch only)
+    const float *x0 = draft + (static_cast<size_t>(blockIdx.x) * sp.gamma + (sp.r_begin - sp.gamma - 1)) * sp.V;
+    const int lo = blockIdx.y * kChunk, hi = min(sp.V, lo + kChunk);
+    for (int e = lo + 32 * static_cast<int>(threadIdx.x); e < hi; e += 32 * kStatThreads)  // one 128-byte line each
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(x0 + e));
+  }
+  pdl_wait();
+  __shared__ int s_last;
+  __shared__ float s_M;
+  __shared__ DrawShared sh;
   const int b = blockIdx.x, s = blockIdx.y;
-  const int r = sp.r_begin;                // unified row index of the draft row
-  const int row = r - sp.gamma - 1;        // its draft position
+  const int row = sp.r_begin - sp.gamma - 1;  // draft position
   const int V = sp.V;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float *x = draft + (static_cast<size_t>(b) * sp.gamma + row) * V;
-  const float2 *st_b = stats + (static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit;
+  float2 *sub_b = sub + static_cast<size_t>(b) * sp.nsub;
   {
-    const int lo = s * sp.split;
-    const float2 st = slice_stats<VEC4>(x, lo, min(lo + sp.split, V));
+    // this warp's sub-range: 64 entries per lane in two rounds of 32 (8 float4 loads in flight)
+    const int g = s * kWarps + warp;
+    const int lo = g * kSub, hi = min(V, lo + kSub);
+    float m = -INFINITY, l = 0.f;
+    if (lo < hi) {
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+        if (VEC4) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = lo + 4 * lane + 128 * (8 * h + k);
+            const float4 f = (i < hi) ? __ldcs(reinterpret_cast<const float4 *>(x + i))
+                                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            v[4 * k] = f.x, v[4 * k + 1] = f.y, v[4 * k + 2] = f.z, v[4 * k + 3] = f.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int i = lo + lane + 32 * (32 * h + k);
+            v[k] = (i < hi) ? __ldcs(x + i) : -INFINITY;
+          }
+        }
+        float mx = v[0];
+#pragma unroll
+        for (int k = 1; k < 32; ++k) mx = fmaxf(mx, v[k]);
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float mn = fmaxf(m, mx);
+        const float ml = (mn == -INFINITY) ? 0.f : mn * kLog2e;  // -inf logits (masked entries) weigh 0
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) t += ex2(fmaf(v[k], kLog2e, -ml));
+        l = (m == -INFINITY) ? t : l * ex2((m - mn) * kLog2e) + t;
+        m = mn;
+      }
+      l = warp_sum_xor(l, 1, 16);
+    }
+    if (lane == 0 && g < sp.nsub) sub_b[g] = make_float2(m, l);
+    __syncthreads();
     if (threadIdx.x == 0) {
-      stats[(static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit + s] = st;
       __threadfence();
       s_last = (atomicAdd(&tickets[b], 1u) == static_cast<unsigned>(sp.nsplit - 1)) ? 1 : 0;
     }
@@ -167,473 +392,152 @@ __global__ void __launch_bounds__(kStatThreads) spec_draw_row_kernel(const float
     if (!s_last) return;
     __threadfence();
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 0 && sp.nsplit <= 32) {
-    // the slice holding u * Z: every slice's (max, sum) loaded at once, one per
-    // lane; float exponentials, double prefix sums across the lanes
-    const float2 v = (lane < sp.nsplit) ? __ldcg(st_b + lane) : make_float2(-INFINITY, 0.f);
-    float M = v.x;
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const double ts = (lane < sp.nsplit) ? static_cast<double>(v.y * exp2f((v.x - M) * kLog2e)) : 0.0;
-    double incl = ts;
-    for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const double Z = __shfl_sync(0xffffffffu, incl, 31);
-    const double tgt = static_cast<double>(u[(static_cast<size_t>(b) * (sp.gamma + 1) + row) * 3 + 0]) * Z;
-    const unsigned hit = __ballot_sync(0xffffffffu, ts > 0.0 && incl > tgt);  // run + ts > tgt, run = incl - ts
-    const unsigned mass = __ballot_sync(0xffffffffu, lane < sp.nsplit && v.y > 0.f);
-    const int pick = hit ? (__ffs(hit) - 1) : (mass ? 31 - __clz(mass) : -1);
-    const double run = __shfl_sync(0xffffffffu, incl - ts, pick < 0 ? 0 : pick);
-    if (lane == 0) {
-      s_M = M;
-      s_slice = pick;
-      s_pre = hit ? tgt - run : -1.0;  // rounding pushed u * Z past the total: the last slice with mass, its end
-      s_tidx = 0x7fffffff;
-      s_lastpos = -1;
-    }
-  } else if (threadIdx.x == 0 && sp.nsplit > 32) {  // the same, one slice at a time
+  // this CTA completed the sequence: sub-range weights relative to the row max, then the draw
+  if (warp == 0) {
     float M = -INFINITY;
-    for (int q = 0; q < sp.nsplit; ++q) M = fmaxf(M, __ldcg(&st_b[q].x));
-    double Z = 0.0;
-    for (int q = 0; q < sp.nsplit; ++q) {
-      const float2 v = __ldcg(st_b + q);
-      Z += static_cast<double>(v.y * exp2f((v.x - M) * kLog2e));
-    }
-    const double tgt = static_cast<double>(u[(static_cast<size_t>(b) * (sp.gamma + 1) + row) * 3 + 0]) * Z;
-    double run = 0.0;
-    int pick = -1;
-    for (int q = 0; q < sp.nsplit; ++q) {
-      const float2 v = __ldcg(st_b + q);
-      const double ts = static_cast<double>(v.y * exp2f((v.x - M) * kLog2e));
-      if (ts > 0.0 && run + ts > tgt) {
-        pick = q;
-        break;
-      }
-      run += ts;
-    }
-    if (pick < 0) {  // rounding pushed u * Z past the total: the last slice with mass, its end
-      for (int q = sp.nsplit - 1; q >= 0 && pick < 0; --q)
-        if (__ldcg(&st_b[q].y) > 0.f) pick = q;
-      run = tgt + 1.0;
-    }
-    s_M = M;
-    s_slice = pick;
-    s_pre = tgt - run;  // target measured from the slice start (negative: take its last entry)
-    s_tidx = 0x7fffffff;
-    s_lastpos = -1;
+    for (int q = lane; q < sp.nsub; q += 32) M = fmaxf(M, __ldcg(&sub_b[q].x));
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0) s_M = M;
+    auto wsum = [&](int q) {
+      const float2 r = __ldcg(sub_b + q);
+      return r.y * exp2f((r.x - M) * kLog2e);
+    };
+    pick_sub(wsum, sp.nsub, u[(static_cast<size_t>(b) * (sp.gamma + 1) + row) * 3 + 0], sh);
   }
   __syncthreads();
-  const int pick_slice = s_slice;
   int tok = -1;
-  if (pick_slice >= 0) {
-    const float M = s_M;
-    const int lo = pick_slice * sp.split, hi = min(lo + sp.split, V);
-    const int seg = ((hi - lo + kStatThreads - 1) / kStatThreads + 3) / 4 * 4;  // contiguous entries per thread
-    const int j0 = min(hi, lo + static_cast<int>(threadIdx.x) * seg), j1 = min(hi, j0 + seg);
-    // 16 entries per batch, all loads in flight (segments start on a multiple of 4)
-    auto load16 = [&](int jb, float (&v)[16]) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int jj = jb + 4 * q;
-        if (VEC4 && jj + 3 < j1) {
-          const float4 f = __ldg(reinterpret_cast<const float4 *>(x + jj));
-          v[4 * q] = f.x;
-          v[4 * q + 1] = f.y;
-          v[4 * q + 2] = f.z;
-          v[4 * q + 3] = f.w;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[4 * q + e] = (jj + e < j1) ? __ldg(x + jj + e) : -INFINITY;
-        }
-      }
-    };
-    float tsum = 0.f;
-    int lastpos = -1;
-#pragma unroll 1
-    for (int jb = j0; jb < j1; jb += 16) {
-      float v[16];
-      load16(jb, v);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float w = exp2f((v[k] - M) * kLog2e);
-        tsum += w;
-        if (w > 0.f) lastpos = jb + k;
-      }
-    }
-    float incl = tsum;
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.f;
-    if (lane == 31) s_wsum[warp] = incl;
-    if (lastpos >= 0) atomicMax(&s_lastpos, lastpos);
-    __syncthreads();
-    if (warp == 0) {  // per-warp float targets from a double scan of the warp totals
-      const double x0 = (lane < kW) ? static_cast<double>(s_wsum[lane]) : 0.0;
-      double ix = x0;
-      for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, ix, o);
-        if (lane >= o) ix += y;
-      }
-      if (lane < kW) s_trel[lane] = fmaxf(0.f, static_cast<float>(s_pre - (ix - x0)));
-    }
-    __syncthreads();
-    const float trel = s_trel[warp];
-    if (tsum > 0.f && excl <= trel && incl > trel && s_pre >= 0.0) atomicMin(&s_tidx, static_cast<int>(threadIdx.x));
-    __syncthreads();
-    if (static_cast<int>(threadIdx.x) == s_tidx) {
-      float c = excl;
-      int p = -1;
-#pragma unroll 1
-      for (int jb = j0; jb < j1 && p < 0; jb += 16) {
-        float v[16];
-        load16(jb, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float w = exp2f((v[k] - M) * kLog2e);
-          c += w;
-          if (p < 0 && w > 0.f && c > trel) p = jb + k;
-        }
-      }
-      s_lastpos = (p >= 0) ? p : lastpos;  // the crossing is here; rounding: this segment's last positive weight
-    }
-    __syncthreads();
-    tok = s_lastpos;  // no claim: the target lies past the slice's scanned total (rounding): its last entry
+  if (sh.sub >= 0) {
+    const Weights w{x, nullptr, s_M, 1.f, 0.f, 0.f, 0};
+    tok = draw_in_sub<VEC4>(w, V, sh);
   }
   if (threadIdx.x == 0) {
     draft_tokens[static_cast<size_t>(b) * sp.gamma + row] = tok;
-    tickets[b] = 0u;  // left clean for the next call on this workspace (the call also clears it first)
+    tickets[b] = 0u;  // left clean for the next call on this workspace
+    call_check_in(hdr, sp.B, b, 0u, 0u);
   }
 }
 
-// Weights of a draw: MODE 0 -> exp(a - Ma) (an unnormalised softmax);
-// MODE 1 -> max(0, exp(a - Ma) * ia - exp(c - Mc) * ic) (residual p - q).
-struct DrawSrc {
-  const float *a;
-  const float *c;
-  float Ma, ia, Mc, ic;
-  int mode;
-};
-
-__device__ __forceinline__ float weight_of(const DrawSrc &s, float a, float c) {
-  const float pa = exp2f((a - s.Ma) * kLog2e);
-  if (s.mode == 0) return pa;
-  const float pc = exp2f((c - s.Mc) * kLog2e);
-  return fmaxf(0.f, pa * s.ia - pc * s.ic);
-}
-
-// Weights of entries i..i+3 (zero at or past `hi`).  With VEC4, i is a
-// multiple of 4 and the rows are 16-byte aligned.
-template <bool VEC4>
-__device__ __forceinline__ void weights4(const DrawSrc &s, int i, int hi, float (&w)[4]) {
-  float a[4], c[4] = {0.f, 0.f, 0.f, 0.f};
-  if (VEC4 && i + 3 < hi) {
-    const float4 fa = __ldg(reinterpret_cast<const float4 *>(s.a + i));
-    a[0] = fa.x;
-    a[1] = fa.y;
-    a[2] = fa.z;
-    a[3] = fa.w;
-    if (s.mode == 1) {
-      const float4 fc = __ldg(reinterpret_cast<const float4 *>(s.c + i));
-      c[0] = fc.x;
-      c[1] = fc.y;
-      c[2] = fc.z;
-      c[3] = fc.w;
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) w[e] = weight_of(s, a[e], c[e]);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (i + e < hi) {
-        a[e] = __ldg(s.a + i + e);
-        if (s.mode == 1) c[e] = __ldg(s.c + i + e);
-        w[e] = weight_of(s, a[e], c[e]);
-      } else {
-        w[e] = 0.f;
-      }
-    }
-  }
-}
-
-struct DrawShared {
-  float tot[kWarps];
-  int last[kWarps];
-  float wsum[kWarps];
-  float trel[kWarps];
-  double base;
-  double target;
-  double chunk;
-  int wstar;
-  int tidx;  // first thread of the block-wide scan holding the crossing
-  int idx;
-  int status;  // 0 ok, 1 total weight is zero
-};
-
-// Block-wide inverse-CDF draw over the index range [r0, r1).  The target is
-// u * (sum of the weights in the range) when `target_in` < 0, else
-// `target_in` (a running-sum value measured from r0).  Returns the index, or
-// -1 when the weights of the range sum to zero.
-template <bool VEC4>
-__device__ int block_draw(const DrawSrc &src, int r0, int r1, float u, double target_in, DrawShared &sh) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = r1 - r0;
-  const int per = ((n + kWarps * 128 - 1) / (kWarps * 128)) * 128;  // slice per warp, multiple of 128
-  {
-    const int lo = r0 + warp * per, hi = min(lo + per, r1);
-    float sum = 0.f;
-    int last = -1;
-#pragma unroll 4
-    for (int i = lo + 4 * lane; i < hi; i += 128) {
-      float w[4];
-      weights4<VEC4>(src, i, hi, w);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sum += w[e];
-        if (w[e] > 0.f) last = i + e;
-      }
-    }
-    sum = warp_sum_xor(sum, 1, 16);
-    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-    if (lane == 0) {
-      sh.tot[warp] = sum;
-      sh.last[warp] = last;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double Z = 0.0;
-    for (int w = 0; w < kWarps; ++w) Z += static_cast<double>(sh.tot[w]);
-    sh.status = (Z > 0.0) ? 0 : 1;
-    const double target = (target_in < 0.0) ? static_cast<double>(u) * Z : target_in;
-    double run = 0.0;
-    int ws = -1;
-    double base = 0.0;
-    for (int w = 0; w < kWarps; ++w) {
-      if (sh.tot[w] > 0.f && run + static_cast<double>(sh.tot[w]) > target) {
-        ws = w;
-        base = run;
-        break;
-      }
-      run += static_cast<double>(sh.tot[w]);
-    }
-    if (ws < 0) {  // rounding pushed u*Z past the total: last slice with mass, its last entry
-      for (int w = kWarps - 1; w >= 0; --w)
-        if (sh.tot[w] > 0.f) {
-          ws = w;
-          break;
-        }
-      base = target + 1.0;
-    }
-    sh.wstar = ws;
-    sh.base = base;
-    sh.target = target;
-    sh.idx = 0x7fffffff;
-  }
-  __syncthreads();
-  if (sh.status != 0) return -1;
-  // Second level: the whole block scans slice wstar, 4 * kThreads entries at a
-  // time.  Double precision is rare on this GPU, so one warp turns the running
-  // sum into a float target relative to each warp's start (clamped at 0);
-  // within a warp, thread t covers [excl_t, incl_t) and neighbours share their
-  // endpoints exactly, so a target inside the chunk is claimed by at least one
-  // thread, and the first claiming thread holds the crossing.
-  const int ws = sh.wstar;
-  const int lo = r0 + ws * per, hi = min(lo + per, r1);
-  if (sh.base <= sh.target) {
-    for (int c0 = lo; c0 < hi; c0 += 4 * kThreads) {
-      const int i = c0 + 4 * threadIdx.x;
-      float w[4];
-      weights4<VEC4>(src, i, hi, w);
-      const float ls = (w[0] + w[1]) + (w[2] + w[3]);
-      float incl = ls;
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-      if (lane == 0) excl = 0.f;
-      if (lane == 31) sh.wsum[warp] = incl;
-      __syncthreads();
-      if (warp == 0) {
-        const double x = static_cast<double>(sh.wsum[lane]);
-        double ix = x;  // inclusive prefix of the warp totals
-        for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xffffffffu, ix, o);
-          if (lane >= o) ix += y;
-        }
-        double ex = __shfl_up_sync(0xffffffffu, ix, 1);
-        if (lane == 0) ex = 0.0;
-        sh.trel[lane] = fmaxf(0.f, static_cast<float>(sh.target - (sh.base + ex)));
-        if (lane == 31) sh.chunk = ix;
-        if (lane == 0) sh.tidx = 0x7fffffff;
-      }
-      __syncthreads();
-      const float trel = sh.trel[warp];
-      if (ls > 0.f && excl <= trel && incl > trel) atomicMin(&sh.tidx, static_cast<int>(threadIdx.x));
-      __syncthreads();
-      const int tsel = sh.tidx;
-      if (static_cast<int>(threadIdx.x) == tsel) {
-        float cacc = excl;
-        int pick = -1;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          cacc += w[e];
-          if (pick < 0 && w[e] > 0.f && cacc > trel) pick = i + e;
-        }
-        if (pick < 0)  // the crossing is here but rounding moved it: last positive weight
-          for (int e = 3; e >= 0; --e)
-            if (w[e] > 0.f) {
-              pick = i + e;
-              break;
-            }
-        sh.idx = pick;
-      }
-      if (threadIdx.x == 0 && tsel == 0x7fffffff) sh.base += sh.chunk;  // next chunk
-      __syncthreads();
-      if (tsel != 0x7fffffff) break;
-    }
-  }
-  if (threadIdx.x == 0 && sh.idx == 0x7fffffff) sh.idx = sh.last[ws];
-  __syncthreads();
-  return sh.idx;
-}
-
-// Draw from softmax(row) knowing the per-slice statistics of the row (slices of
-// `split` entries): the slice totals locate the slice holding u * Z, and only
-// that slice is scanned.
-template <bool VEC4>
-__device__ int draw_softmax_row(const float *row, const float2 *st, int nsplit, int split, int V, float M, float u,
-                                DrawShared &sh, double *s_pre, int *s_slice) {
-  if (threadIdx.x == 0) {
-    double Z = 0.0;
-    for (int s = 0; s < nsplit; ++s) Z += static_cast<double>(st[s].y * exp2f((st[s].x - M) * kLog2e));
-    const double target = static_cast<double>(u) * Z;
-    double run = 0.0;
-    int pick = nsplit - 1;
-    for (int s = 0; s < nsplit; ++s) {
-      const double ts = static_cast<double>(st[s].y * exp2f((st[s].x - M) * kLog2e));
-      if (ts > 0.0 && run + ts > target) {
-        pick = s;
-        break;
-      }
-      run += ts;
-    }
-    if (run > target) run = target;  // only when every later slice is empty
-    *s_pre = target - run;
-    *s_slice = pick;
-  }
-  __syncthreads();
-  const int s = *s_slice;
-  const double t = *s_pre;
-  DrawSrc src{row, nullptr, M, 1.f, 0.f, 0.f, 0};
-  const int r0 = s * split, r1 = min(V, r0 + split);
-  int tok = block_draw<VEC4>(src, r0, r1, u, t, sh);
-  if (tok < 0) tok = block_draw<VEC4>(src, 0, V, u, -1.0, sh);  // the slice held no mass: full scan
-  return tok;
-}
-
-__device__ __forceinline__ void merge_stats(const float2 *st, int nsplit, float &M, float &Z) {
+// Merge the slice statistics of unified row r into (max, 1 / sum).
+__device__ __forceinline__ void merge_row(const float2 *st, int nsplit, float &M, float &iZ) {
   M = -INFINITY;
   for (int s = 0; s < nsplit; ++s) M = fmaxf(M, st[s].x);
-  Z = 0.f;
+  float Z = 0.f;
   for (int s = 0; s < nsplit; ++s) Z += st[s].y * exp2f((st[s].x - M) * kLog2e);
+  iZ = 1.f / Z;
 }
 
+// Rejection sampling, CTA (b, s): the acceptance decisions of sequence b (the
+// same in every CTA of b), then the weight sums of the final draw over the
+// sub-ranges of chunk s; the CTA completing the sequence draws and writes the
+// round's tokens.
 template <bool VEC4>
-__global__ void __launch_bounds__(kThreads, 1) spec_finish_kernel(const float *__restrict__ target,
-                                                               const float *__restrict__ draft,
-                                                               int32_t *__restrict__ draft_tokens,
-                                                               const float *__restrict__ u, StatParams sp, int mode,
-                                                               int32_t *__restrict__ out_tokens,
-                                                               int32_t *__restrict__ num_accepted,
-                                                               const float2 *__restrict__ stats, WsHeader *hdr) {
-  __shared__ float sM[33], sZ[33];
-  __shared__ int s_last, s_slice;
+__global__ void __launch_bounds__(kStatThreads) spec_decide_kernel(const float *__restrict__ target,
+                                                                    const float *__restrict__ draft,
+                                                                    const int32_t *__restrict__ draft_tokens,
+                                                                    const float *__restrict__ u, StatParams sp,
+                                                                    const float2 *__restrict__ stats,
+                                                                    float2 *__restrict__ sub,
+                                                                    unsigned *__restrict__ tickets,
+                                                                    int32_t *__restrict__ out_tokens,
+                                                                    int32_t *__restrict__ num_accepted,
+                                                                    WsHeader *hdr) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float sM[33], siZ[33];
   __shared__ int s_tok[16];
   __shared__ unsigned char s_ok[16], s_bad[16];
-  __shared__ double s_pre;
+  __shared__ int s_j, s_last;
   __shared__ DrawShared sh;
-  const int b = blockIdx.x;
+  const int b = blockIdx.x, s = blockIdx.y;
   const int g = sp.gamma, V = sp.V;
-
-  for (int r = sp.r_begin + threadIdx.x; r < sp.r_begin + sp.nr; r += kThreads)
-    merge_stats(stats + (static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit, sp.nsplit, sM[r], sZ[r]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = threadIdx.x; r < sp.nrows; r += kStatThreads)
+    merge_row(stats + (static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit, sp.nsplit, sM[r], siZ[r]);
   __syncthreads();
-
-  if (mode == 1) {  // draft draw: row s uses draft row s, uniform slot 0
-    for (int r = sp.r_begin; r < sp.r_begin + sp.nr; ++r) {
-      const int s = r - g - 1;
-      const float uu = u[(static_cast<size_t>(b) * (g + 1) + s) * 3 + 0];
-      const int tok = draw_softmax_row<VEC4>(row_ptr(target, draft, b, r, g, V),
-                                             stats + (static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit, sp.nsplit,
-                                             sp.split, V, sM[r], uu, sh, &s_pre, &s_slice);
-      if (threadIdx.x == 0) draft_tokens[static_cast<size_t>(b) * g + s] = tok;
-      __syncthreads();
-    }
-    return;
-  }
-
   // every candidate's test at once; the chain keeps the prefix before the first rejection
   if (threadIdx.x < g) {
     const int i = threadIdx.x;
-    const int x = draft_tokens[static_cast<size_t>(b) * g + i];
-    const bool bad = (x < 0 || x >= V);
+    const int xi = draft_tokens[static_cast<size_t>(b) * g + i];
+    const bool bad = (xi < 0 || xi >= V);
     bool acc = false;
     if (!bad) {
-      const float *t = row_ptr(target, draft, b, i, g, V);
-      const float *d = row_ptr(target, draft, b, g + 1 + i, g, V);
-      const float px = exp2f((t[x] - sM[i]) * kLog2e) / sZ[i];
-      const float qx = exp2f((d[x] - sM[g + 1 + i]) * kLog2e) / sZ[g + 1 + i];
-      const float u1 = u[(static_cast<size_t>(b) * (g + 1) + i) * 3 + 1];
-      acc = (u1 * qx < px);
+      const float px = exp2f((row_ptr(target, draft, b, i, g, V)[xi] - sM[i]) * kLog2e) * siZ[i];
+      const float qx = exp2f((row_ptr(target, draft, b, g + 1 + i, g, V)[xi] - sM[g + 1 + i]) * kLog2e) * siZ[g + 1 + i];
+      acc = u[(static_cast<size_t>(b) * (g + 1) + i) * 3 + 1] * qx < px;
     }
-    s_tok[i] = x;
+    s_tok[i] = xi;
     s_ok[i] = acc ? 1 : 0;
     s_bad[i] = bad ? 1 : 0;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int j = g;
-    for (int i = 0; i < g; ++i) {
-      if (s_bad[i]) {
-        raise_error(hdr, 0x4u);
+    for (int i = 0; i < g; ++i)
+      if (s_bad[i] || !s_ok[i]) {
         j = i;
         break;
       }
-      if (!s_ok[i]) {
-        j = i;
-        break;
-      }
-      out_tokens[static_cast<size_t>(b) * (g + 1) + i] = s_tok[i];
-    }
-    s_last = j;
-    num_accepted[b] = j;
+    s_j = j;
   }
   __syncthreads();
-  const int j = s_last;
-  const float uu = u[(static_cast<size_t>(b) * (g + 1) + j) * 3 + 2];
-  int tok;
-  if (j < g) {
-    DrawSrc src{row_ptr(target, draft, b, j, g, V), row_ptr(target, draft, b, g + 1 + j, g, V), sM[j],
-                1.f / sZ[j], sM[g + 1 + j], 1.f / sZ[g + 1 + j], 1};
-    tok = block_draw<VEC4>(src, 0, V, uu, -1.0, sh);
-    if (tok < 0) {  // the residual vanished through rounding: draw from p_j
-      DrawSrc sp2{row_ptr(target, draft, b, j, g, V), nullptr, sM[j], 1.f, 0.f, 0.f, 0};
-      tok = block_draw<VEC4>(sp2, 0, V, uu, -1.0, sh);
+  const int j = s_j;
+  // the draw's weights: the residual at a rejection (kind 1) and p_j for the rare
+  // case where the residual sums to zero; p of the bonus row otherwise
+  const Weights wr{row_ptr(target, draft, b, j, g, V), row_ptr(target, draft, b, g + 1 + min(j, g - 1), g, V),
+                   sM[j], siZ[j], sM[g + 1 + min(j, g - 1)], siZ[g + 1 + min(j, g - 1)], j < g ? 1 : 0};
+  const Weights wp{wr.a, nullptr, sM[j], siZ[j], 0.f, 0.f, 0};
+  float2 *sub_b = sub + static_cast<size_t>(b) * sp.nsub;
+  {
+    const int sg = s * kWarps + warp;
+    const int lo = sg * kSub, hi = min(V, lo + kSub);
+    float r = 0.f, pp = 0.f;
+    for (int i = lo + 8 * lane; i < hi; i += 8 * 32) {
+      float vr[8];
+      weights8<VEC4>(wr, i, hi, vr);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r += vr[e];
+      if (j < g) {
+        float vp[8];
+        weights8<VEC4>(wp, i, hi, vp);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pp += vp[e];
+      }
     }
-  } else {  // bonus from p_gamma
-    tok = draw_softmax_row<VEC4>(row_ptr(target, draft, b, g, g, V),
-                                 stats + (static_cast<size_t>(b) * sp.nrows + g) * sp.nsplit, sp.nsplit, sp.split, V,
-                                 sM[g], uu, sh, &s_pre, &s_slice);
+    r = warp_sum_xor(r, 1, 16);
+    pp = warp_sum_xor(pp, 1, 16);
+    if (lane == 0 && sg < sp.nsub) sub_b[sg] = make_float2(r, pp);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last = (atomicAdd(&tickets[b], 1u) == static_cast<unsigned>(sp.nsplit - 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
   }
+  // this CTA completed the sequence: draw the correction (or bonus) token
+  __shared__ int s_use_p;
+  if (warp == 0) {
+    float zr = 0.f;
+    for (int q = lane; q < sp.nsub; q += 32) zr += __ldcg(&sub_b[q].x);
+    zr = warp_sum_xor(zr, 1, 16);
+    const int use_p = (j < g && !(zr > 0.f)) ? 1 : 0;  // the residual vanished through rounding: draw from p_j
+    if (lane == 0) s_use_p = use_p;
+    auto wsum = [&](int q) { return use_p ? __ldcg(&sub_b[q].y) : __ldcg(&sub_b[q].x); };
+    pick_sub(wsum, sp.nsub, u[(static_cast<size_t>(b) * (g + 1) + j) * 3 + 2], sh);
+  }
+  __syncthreads();
+  int tok = -1;
+  if (sh.sub >= 0) tok = draw_in_sub<VEC4>(s_use_p ? wp : wr, V, sh);
   if (threadIdx.x == 0) {
-    out_tokens[static_cast<size_t>(b) * (g + 1) + j] = tok;
-    for (int i = j + 1; i <= g; ++i) out_tokens[static_cast<size_t>(b) * (g + 1) + i] = -1;
+    int32_t *o = out_tokens + static_cast<size_t>(b) * (g + 1);
+    for (int i = 0; i < j; ++i) o[i] = s_tok[i];
+    o[j] = tok;
+    for (int i = j + 1; i <= g; ++i) o[i] = -1;
+    num_accepted[b] = j;
+    if (j < g && s_bad[j]) raise_error_sr(hdr, 0x4u);
+    tickets[b] = 0u;
+    call_check_in(hdr, sp.B, b, 0u, 0u);
   }
 }
 
@@ -644,18 +548,18 @@ SpecPlan plan_spec(int B, int gamma, int V) {
   p.B = B;
   p.gamma = gamma;
   p.V = V;
-  p.split = 16384;
+  p.split = kChunk;
   p.nsplit = (V + p.split - 1) / p.split;
+  p.nsub = (V + kSub - 1) / kSub;
   p.nrows = 2 * gamma + 1;
   p.off_tickets = kAlign;
   p.off_stats = align_up(p.off_tickets + sizeof(unsigned) * static_cast<size_t>(B));
-  p.ws_bytes = align_up(p.off_stats + sizeof(float2) * static_cast<size_t>(B) * p.nrows * p.nsplit);
+  p.off_sub = align_up(p.off_stats + sizeof(float2) * static_cast<size_t>(B) * p.nrows * p.nsplit);
+  p.ws_bytes = align_up(p.off_sub + sizeof(float2) * static_cast<size_t>(B) * p.nsub);
   return p;
 }
 
 cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
-  cudaError_t e = cudaMemsetAsync(a.ws, 0, p.off_stats, a.stream);  // header and tickets
-  if (e != cudaSuccess) return e;
   StatParams sp;
   sp.B = p.B;
   sp.gamma = p.gamma;
@@ -663,44 +567,36 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   sp.split = p.split;
   sp.nsplit = p.nsplit;
   sp.nrows = p.nrows;
-  if (a.mode == 0) {
-    sp.r_begin = 0;
-    sp.nr = p.nrows;
-  } else if (a.row < 0) {
-    sp.r_begin = p.gamma + 1;
-    sp.nr = p.gamma;
-  } else {
-    sp.r_begin = p.gamma + 1 + a.row;
-    sp.nr = 1;
-  }
-  float2 *stats = reinterpret_cast<float2 *>(static_cast<unsigned char *>(a.ws) + p.off_stats);
+  sp.nsub = p.nsub;
+  unsigned char *ws = static_cast<unsigned char *>(a.ws);
+  unsigned *tickets = reinterpret_cast<unsigned *>(ws + p.off_tickets);
+  float2 *stats = reinterpret_cast<float2 *>(ws + p.off_stats);
+  float2 *sub = reinterpret_cast<float2 *>(ws + p.off_sub);
   WsHeader *hdr = static_cast<WsHeader *>(a.ws);
   const bool vec4 = (p.V % 4) == 0 && (reinterpret_cast<uintptr_t>(a.draft) % 16) == 0 &&
                     (a.target == nullptr || (reinterpret_cast<uintptr_t>(a.target) % 16) == 0);
-  if (a.mode == 1 && a.row >= 0) {  // one draft row: statistics and draw in one launch
-    unsigned *tickets = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(a.ws) + p.off_tickets);
-    const dim3 g(p.B, p.nsplit);
-    if (vec4)
-      spec_draw_row_kernel<true><<<g, kStatThreads, 0, a.stream>>>(a.draft, a.draft_tokens, a.u, sp, stats, tickets);
-    else
-      spec_draw_row_kernel<false><<<g, kStatThreads, 0, a.stream>>>(a.draft, a.draft_tokens, a.u, sp, stats,
-                                                                     tickets);
-    return cudaGetLastError();
+  const dim3 grid(p.B, p.nsplit);
+  if (a.mode == 1) {  // draft draws: one launch per drawn row
+    const int r0 = a.row < 0 ? 0 : a.row, r1 = a.row < 0 ? p.gamma : a.row + 1;
+    for (int r = r0; r < r1; ++r) {
+      sp.r_begin = p.gamma + 1 + r;
+      sp.nr = 1;
+      const cudaError_t e =
+          launch_pdl(vec4 ? spec_draw_row_kernel<true> : spec_draw_row_kernel<false>, grid, dim3(kStatThreads), 0,
+                     a.stream, a.draft, a.draft_tokens, a.u, sp, sub, tickets, hdr);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
   }
-  dim3 g1(p.B * sp.nr, p.nsplit);
-  if (vec4)
-    spec_stats_kernel<true><<<g1, kStatThreads, 0, a.stream>>>(a.target, a.draft, sp, stats);
-  else
-    spec_stats_kernel<false><<<g1, kStatThreads, 0, a.stream>>>(a.target, a.draft, sp, stats);
-  e = cudaGetLastError();
+  sp.r_begin = 0;
+  sp.nr = p.nrows;
+  const dim3 g1(p.B * sp.nr, p.nsplit);
+  cudaError_t e = launch_pdl(vec4 ? spec_stats_kernel<true> : spec_stats_kernel<false>, g1, dim3(kStatThreads), 0,
+                             a.stream, a.target, a.draft, sp, stats);
   if (e != cudaSuccess) return e;
-  if (vec4)
-    spec_finish_kernel<true><<<p.B, kThreads, 0, a.stream>>>(a.target, a.draft, a.draft_tokens, a.u, sp, a.mode,
-                                                             a.out_tokens, a.num_accepted, stats, hdr);
-  else
-    spec_finish_kernel<false><<<p.B, kThreads, 0, a.stream>>>(a.target, a.draft, a.draft_tokens, a.u, sp, a.mode,
-                                                              a.out_tokens, a.num_accepted, stats, hdr);
-  return cudaGetLastError();
+  return launch_pdl(vec4 ? spec_decide_kernel<true> : spec_decide_kernel<false>, grid, dim3(kStatThreads), 0, a.stream,
+                    a.target, a.draft, a.draft_tokens, a.u, sp, stats, sub, tickets, a.out_tokens, a.num_accepted,
+                    hdr);
 }
 
 }  // namespace mgd

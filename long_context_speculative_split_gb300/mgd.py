@@ -31,6 +31,7 @@ SIGNATURES = {
     "mgd_workspace_errors": (_i32, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]),
     "mgd_selftest_bounded_wait": (_i32, [_i32, _vp, _sz, _vp]),
     "mgd_selftest_occupy": (_i32, [_i32, _i32, _i32, _vp]),
+    "mgd_set_programmatic_launch": (None, [_i32]),
     "mgd_verify_workspace_size": (_sz, [_i32] * 6),
     "mgd_verify_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _f32, _i32,
                                _vp, _i32, _vp, _vp, _sz, _vp]),
@@ -135,6 +136,11 @@ def mgd_selftest_bounded_wait(which, ws, ws_bytes=None, stream=None):
     if ws_bytes is None:
         ws_bytes = ws.numel() * ws.element_size()
     _check(load().mgd_selftest_bounded_wait(which, _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def mgd_set_programmatic_launch(enable):
+    """Launch later calls' kernels with programmatic stream serialization (True, the default) or plainly."""
+    load().mgd_set_programmatic_launch(1 if enable else 0)
 
 
 def mgd_selftest_occupy(ctas, smem_bytes, usec, stream=None):

@@ -213,3 +213,28 @@ def test_round_graph_replay_is_identical(rnd):
     r.replay()
     torch.cuda.synchronize()
     assert torch.equal(r.out_tok, ref["out_tok"]) and torch.equal(r.lengths, r.pre[1]["lengths"])
+
+
+def test_programmatic_launch_round_equals_plain_launch_round(rnd):
+    """The same round (from the same restored state) with kernels launched with programmatic
+    stream serialization (the default) and plainly gives the same tokens, lengths and committed
+    draft rows, and attention outputs equal up to the arrival-order rounding of a CTA's merge."""
+    from long_context_speculative_split_gb300 import mgd
+    r = rnd
+    r.u.copy_(r.post[0]["u"])
+    outs = []
+    for pdl in (True, False):
+        mgd.mgd_set_programmatic_launch(pdl)
+        try:
+            r.restore()
+            r.run()
+            torch.cuda.synchronize()
+        finally:
+            mgd.mgd_set_programmatic_launch(True)
+        outs.append(_snap(r))
+    a, b = outs
+    for name in ("tok", "out_tok", "nacc", "lengths", "kd", "vd"):
+        assert torch.equal(a[name], b[name]), name
+    assert torch.equal(a["out_tok"], r.post[0]["out_tok"])
+    torch.testing.assert_close(a["vout"], b["vout"], rtol=1e-5, atol=1e-6)
+    torch.testing.assert_close(a["dout"], b["dout"], rtol=1e-5, atol=1e-6)
