@@ -16,14 +16,12 @@
  *     the caller's `ws` buffer of at least the size the matching
  *     mgd_*_workspace_size() returns for the same shape.
  *   - A workspace is ZERO-FILLED once before its first use (e.g. one
- *     cudaMemsetAsync after allocating it).  The attention, sampling and
- *     commit calls (mgd_verify_attn, mgd_draft_attn, mgd_spec_sample,
- *     mgd_commit_round) do not clear it per call: their kernels leave its
- *     counters at zero for the next call, which saves a clearing launch ahead
- *     of every launch.  mgd_snapkv_select and mgd_topk_draft_attn clear the
- *     part they use themselves.  A buffer that served as scratch for another
- *     kind of call is zero-filled again before it serves one of the former.
- *     An attention or commit call that starts from a header in any other state
+ *     cudaMemsetAsync after allocating it).  The calls do not clear it per
+ *     call: their kernels leave its counters at zero for the next call, which
+ *     saves a clearing launch ahead of every launch.  A buffer that served as
+ *     scratch for one kind of call (attention, selection, sampling, commit) is
+ *     zero-filled again before it serves another kind.  An attention,
+ *     selection or commit call that starts from a header in any other state
  *     (its counters not at zero) detects it at its end and raises
  *     MGD_DEVERR_STALE_WS: its outputs are then unspecified, and the workspace
  *     is zero-filled again before the next call.
@@ -76,8 +74,8 @@ typedef enum {
 #define MGD_DEVERR_TOKEN    0x4u   /* a draft token id outside [0, V) */
 #define MGD_DEVERR_TIMEOUT  0x8u   /* a bounded wait inside a kernel gave up (never expected) */
 #define MGD_DEVERR_COMMIT   0x10u  /* mgd_commit_round: num_accepted, kv_len or draft_len out of range */
-#define MGD_DEVERR_STALE_WS 0x20u  /* an attention call found its workspace header not ready (not zero-filled,
-                                      or last used by another call); its outputs are unspecified */
+#define MGD_DEVERR_STALE_WS 0x20u  /* a call found its workspace header not ready (not zero-filled, or last
+                                      used by another kind of call); its outputs are unspecified */
 
 const char *mgd_status_string(mgd_status s);
 /* Detail text of the last non-OK status returned on the calling thread ("" if none). */

@@ -254,7 +254,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Ws
                                               volatile int *abort_flag) {
   if (*abort_flag) return false;
   if (mbar_wait(bar, parity)) return true;
-  raise_error(hdr, 0x8u);
+  raise_error_sr(hdr, 0x8u);
   *abort_flag = 1;
   return false;
 }
@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
       int stage = 0, qn = 0, msg = 0, groups = 0;
       uint32_t phase = 0;
       int issued = 0;  // K tiles issued; tile i went to stage i % kT5Stages in phase i / kT5Stages
+      unsigned tickets = 0;  // successful claims from the header's work counter
       bool ok = true;
       auto emit = [&](int pair, int slice, int kind, int flags) {
         const int slot = msg % kRing;
@@ -382,10 +383,11 @@ __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
         while (true) {
           const unsigned u = atomicAdd(&hdr->next_unit, 1u);
           if (u >= static_cast<unsigned>(p.units)) break;
+          ++tickets;
           const int pr = static_cast<int>(u) / p.nslice, ticket = static_cast<int>(u) - pr * p.nslice;
           jb = slice_of(pr, 0, kv_len, p);
           if (!jb.valid) {
-            if (ticket == 0 && jb.hkv == 0) raise_error(hdr, 0x2u);
+            if (ticket == 0 && jb.hkv == 0) raise_error_sr(hdr, 0x2u);
             continue;
           }
           if (ticket >= jb.ns) continue;  // a pair has as many tickets as slices
@@ -425,6 +427,8 @@ __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
         ++groups;
       }
       if (ok) emit(-1, 0, kSegEnd, 0);
+      // the selection kernel that follows checks the sum against the number of tickets
+      if (tickets) atomicAdd(&hdr->claimed, tickets);
       // every copy this thread issued has landed before the CTA moves on
       for (int s = 0; s < kT5Stages && s < issued; ++s) {
         const int last = s + kT5Stages * ((issued - 1 - s) / kT5Stages);  // the stage's last tile
@@ -551,7 +555,7 @@ __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
         // ---- wait for every slice of the pair (sg.y of them), then merge their partials into -lse
         const int ns = sg.y;
         if (exch && !*abort_flag && !spin_until_geq(&cnt[pair], static_cast<unsigned>(ns))) {
-          raise_error(hdr, 0x8u);
+          raise_error_sr(hdr, 0x8u);
           *abort_flag = 1;
         }
         named_bar(1, kT5SoftWarps * 32);

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   const int b = pair / p.Hkv;
   const int L = kv_len[b];
   if (L < p.W || L > p.kv_cap) {
-    if (threadIdx.x == 0 && chunk == 0 && rg == 0 && hkv == 0) raise_error(hdr, 0x2u);
+    if (threadIdx.x == 0 && chunk == 0 && rg == 0 && hkv == 0) raise_error_sr(hdr, 0x2u);
     return;
   }
   const int kend = (PASS == 1) ? L : L - p.W;
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     uint32_t phase = 0;
     for (int t = 0; t < ntiles; ++t) {
       if (!mbar_wait(&empty[stage], phase ^ 1u)) {
-        raise_error(hdr, 0x8u);
+        raise_error_sr(hdr, 0x8u);
         for (int s = 0; s < kScoreStages; ++s) mbar_wait(&full[s], phase);
         return;
       }
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   uint32_t phase = 0;
   for (int t = 0; t < ntiles; ++t) {
     if (!mbar_wait(&full[stage], phase)) {
-      raise_error(hdr, 0x8u);
+      raise_error_sr(hdr, 0x8u);
       return;
     }
     const int kt0 = start + 64 * t;
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   const int b = pair / p.Hkv;
   const int L = kv_len[b];
   if (L < p.W || L > p.kv_cap) {
-    if (threadIdx.x == 0 && chunk == 0 && hkv == 0) raise_error(hdr, 0x2u);
+    if (threadIdx.x == 0 && chunk == 0 && hkv == 0) raise_error_sr(hdr, 0x2u);
     return;
   }
   const int kend = (PASS == 1) ? L : L - p.W;
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     uint32_t phase = 0;
     for (int t = 0; t < ntiles; ++t) {
       if (!mbar_wait(&empty[stage], phase ^ 1u)) {
-        raise_error(hdr, 0x8u);
+        raise_error_sr(hdr, 0x8u);
         return;
       }
       mbar_arrive_expect_tx(&full[stage], Lay::kStageBytes);
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   uint32_t phase = 0;
   for (int t = 0; t < ntiles; ++t) {
     if (!mbar_wait(&full[stage], phase)) {
-      raise_error(hdr, 0x8u);
+      raise_error_sr(hdr, 0x8u);
       break;  // still meets the end-of-unit barrier below
     }
     const uint32_t kbase = smem_addr(smem + stage * Lay::kStageBytes);
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(256)
   const int b = blockIdx.x / p.Hkv, hkv = blockIdx.x % p.Hkv;
   const int L = kv_len[b];
   if (L < p.W || L > p.kv_cap) {
-    if (threadIdx.x == 0 && hkv == 0) raise_error(hdr, 0x2u);
+    if (threadIdx.x == 0 && hkv == 0) raise_error_sr(hdr, 0x2u);
     return;
   }
   const Tin *kb = k + b * bstride + hkv * hstride;
@@ -672,6 +672,8 @@ struct SelParams {
   int Hkv, W, pool, K, kv_cap, draft_cap, row_bytes;
   int64_t bstride_bytes, hstride_bytes;
   const int32_t *Kb;  // per-sequence budgets (device), or null for K everywhere
+  size_t off_cnt;     // the one-read scorer's per-pair counters ([2][pairs]), put back to zero here
+  unsigned expect_claims;  // successful work claims the scorer made from a ready header
 };
 
 // Exclusive block scan of one unsigned per thread (kSelThreads threads); returns
@@ -702,14 +704,12 @@ __device__ unsigned block_excl_scan(unsigned v, unsigned *sm_warp, unsigned *tot
   return r;
 }
 
-__global__ void __launch_bounds__(kSelThreads, 2)
-    snap_select(const unsigned char *__restrict__ k, const unsigned char *__restrict__ v,
-                const int32_t *__restrict__ kv_len, SelParams sp, int32_t *__restrict__ sel_idx,
-                unsigned char *__restrict__ k_draft, unsigned char *__restrict__ v_draft,
-                int32_t *__restrict__ draft_len, float *__restrict__ scores_out, unsigned char *__restrict__ ws,
-                size_t off_scores, size_t off_pooled) {
-  pdl_launch_dependents();
-  pdl_wait();
+__device__ __forceinline__ void select_pair(const unsigned char *__restrict__ k, const unsigned char *__restrict__ v,
+                                            const int32_t *__restrict__ kv_len, const SelParams &sp,
+                                            int32_t *__restrict__ sel_idx, unsigned char *__restrict__ k_draft,
+                                            unsigned char *__restrict__ v_draft, int32_t *__restrict__ draft_len,
+                                            float *__restrict__ scores_out, unsigned char *__restrict__ ws,
+                                            size_t off_scores, size_t off_pooled) {
   __shared__ unsigned hist[2048];
   __shared__ unsigned sm_warp[33];
   __shared__ unsigned s_bin, s_above;
@@ -724,7 +724,7 @@ __global__ void __launch_bounds__(kSelThreads, 2)
     for (int i = threadIdx.x; i < sp.draft_cap; i += kSelThreads) sel[i] = -1;
     if (threadIdx.x == 0 && hkv == 0) {
       draft_len[b] = 0;
-      raise_error(hdr, 0x2u);
+      raise_error_sr(hdr, 0x2u);
     }
     return;
   }
@@ -941,6 +941,27 @@ __global__ void __launch_bounds__(kSelThreads, 2)
   }
 }
 
+// Steps 2-4 of the selection for one (sequence, KV head) per CTA, and the end
+// of the call: each CTA puts its pair's scorer counters back to zero and checks
+// in, and the last check-in leaves the workspace header ready for the next
+// call (so no clearing launch is needed ahead of a selection).
+__global__ void __launch_bounds__(kSelThreads, 2)
+    snap_select(const unsigned char *__restrict__ k, const unsigned char *__restrict__ v,
+                const int32_t *__restrict__ kv_len, SelParams sp, int32_t *__restrict__ sel_idx,
+                unsigned char *__restrict__ k_draft, unsigned char *__restrict__ v_draft,
+                int32_t *__restrict__ draft_len, float *__restrict__ scores_out, unsigned char *__restrict__ ws,
+                size_t off_scores, size_t off_pooled) {
+  pdl_launch_dependents();
+  pdl_wait();
+  select_pair(k, v, kv_len, sp, sel_idx, k_draft, v_draft, draft_len, scores_out, ws, off_scores, off_pooled);
+  if (threadIdx.x == 0) {
+    unsigned *cnt = reinterpret_cast<unsigned *>(ws + sp.off_cnt);
+    cnt[blockIdx.x] = 0u;              // slices published
+    cnt[gridDim.x + blockIdx.x] = 0u;  // slices claimed
+    call_check_in(reinterpret_cast<WsHeader *>(ws), gridDim.x, blockIdx.x, 0u, sp.expect_claims);
+  }
+}
+
 }  // namespace
 
 SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W) {
@@ -986,9 +1007,11 @@ SnapPlan plan_snapkv(int B, int Hq, int Hkv, int D, int kv_cap, int W) {
 
 cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, const CUtensorMap *kmap,
                           const CUtensorMap *qmap) {
-  cudaError_t e = cudaMemsetAsync(a.ws, 0, p.off_part, a.stream);  // header and per-pair counters
-  if (e != cudaSuccess) return e;
+  // no clearing launch: the select kernel at the end of the call leaves the header and the
+  // scorer's counters at zero for the next call (the workspace is zero-filled before first use)
+  cudaError_t e = cudaSuccess;
   unsigned char *ws = static_cast<unsigned char *>(a.ws);
+  const bool tc05 = !in_f32 && kmap != nullptr && qmap != nullptr && snap_tc05_eligible(p);
   SnapK kp;
   kp.W = p.W;
   kp.G = p.G;
@@ -1105,6 +1128,8 @@ cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, cons
   sp.row_bytes = p.D * (in_f32 ? 4 : 2);
   sp.bstride_bytes = a.kv_batch_stride * (in_f32 ? 4 : 2);
   sp.hstride_bytes = a.kv_head_stride * (in_f32 ? 4 : 2);
+  sp.off_cnt = p.off_cnt;
+  sp.expect_claims = tc05 ? static_cast<unsigned>(p.pairs * p.nchunk) : 0u;
   return launch_pdl(snap_select, dim3(p.pairs), dim3(kSelThreads), 0, a.stream, static_cast<const unsigned char *>(a.k),
                     static_cast<const unsigned char *>(a.v), a.kv_len, sp, a.sel_idx,
                     static_cast<unsigned char *>(a.k_draft), static_cast<unsigned char *>(a.v_draft), a.draft_len,

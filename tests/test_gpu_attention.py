@@ -341,6 +341,12 @@ def test_stale_workspace_is_detected():
     out = ops.verify_attn(q, k, v, kv_len, ws=ws)
     assert mgd.mgd_workspace_errors(ws) == 0
     assert torch.equal(out[0], fresh[0]) and torch.equal(out[1], fresh[1])
+    # the selection call leaves its header ready too, and checks it the same way
+    ws.zero_()
+    hdr[2] = 3
+    ops.snapkv_select(qw, k, v, kv_len, 32, 7, 128, ws=ws)
+    assert mgd.mgd_workspace_errors(ws) & mgd.MGD_DEVERR_STALE_WS
+    ws.zero_()
     # a buffer last used by a SnapKV call: detected if its counters were left nonzero,
     # otherwise the call is clean
     ops.snapkv_select(qw, k, v, kv_len, 32, 7, 128, ws=ws)
