@@ -488,19 +488,35 @@ __global__ void __launch_bounds__(kStatThreads) spec_decide_kernel(const float *
   const Weights wp{wr.a, nullptr, sM[j], siZ[j], 0.f, 0.f, 0};
   float2 *sub_b = sub + static_cast<size_t>(b) * sp.nsub;
   {
+    // this warp's sub-range in two rounds of 32 entries per lane, every load of a round in
+    // flight at once (8 float4 of each row); each target value serves both sums
     const int sg = s * kWarps + warp;
     const int lo = sg * kSub, hi = min(V, lo + kSub);
     float r = 0.f, pp = 0.f;
-    for (int i = lo + 8 * lane; i < hi; i += 8 * 32) {
-      float vr[8];
-      weights8<VEC4>(wr, i, hi, vr);
+#pragma unroll 1
+    for (int h = 0; h < 2 && lo < hi; ++h) {
+      float a[32], c[32];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) r += vr[e];
-      if (j < g) {
-        float vp[8];
-        weights8<VEC4>(wp, i, hi, vp);
+      for (int k = 0; k < 8; ++k) {
+        const int i = lo + 4 * lane + 128 * (8 * h + k);
+        if (VEC4 && i + 3 < hi) {
+          const float4 fa = __ldg(reinterpret_cast<const float4 *>(wr.a + i));
+          a[4 * k] = fa.x, a[4 * k + 1] = fa.y, a[4 * k + 2] = fa.z, a[4 * k + 3] = fa.w;
+          const float4 fc = (j < g) ? __ldg(reinterpret_cast<const float4 *>(wr.c + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          c[4 * k] = fc.x, c[4 * k + 1] = fc.y, c[4 * k + 2] = fc.z, c[4 * k + 3] = fc.w;
+        } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) pp += vp[e];
+          for (int e = 0; e < 4; ++e) {
+            a[4 * k + e] = (i + e < hi) ? __ldg(wr.a + i + e) : -INFINITY;
+            c[4 * k + e] = (j < g && i + e < hi) ? __ldg(wr.c + i + e) : 0.f;
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float pa = exp2f((a[e] - wr.Ma) * kLog2e) * wr.ia;  // p, as the weights functions compute it
+        pp += pa;
+        r += (j < g) ? fmaxf(0.f, pa - exp2f((c[e] - wr.Mc) * kLog2e) * wr.ic) : pa;
       }
     }
     r = warp_sum_xor(r, 1, 16);
