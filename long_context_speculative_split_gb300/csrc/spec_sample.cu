@@ -40,6 +40,7 @@ constexpr int kStatThreads = 256;
 constexpr int kWarps = kStatThreads / 32;
 constexpr int kSub = 2048;                 // entries per sub-range (one warp)
 constexpr int kChunk = kWarps * kSub;      // entries per CTA of the draw kernels (= the statistics split)
+constexpr int kRecSmem = 512;              // sub-range records a completing CTA stages in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct StatParams {
@@ -320,13 +321,22 @@ __device__ int draw_in_sub(const Weights &w, int V, DrawShared &sh) {
 // CTA (b, s) streams entries [s * kChunk, ...) of the row; warp w keeps the
 // (max, sum of exp) of its sub-range s * kWarps + w.  The CTA completing the
 // sequence merges the sub-range records into weights relative to the row max
-// and draws.
-template <bool VEC4>
-__global__ void __launch_bounds__(kStatThreads) spec_draw_row_kernel(const float *__restrict__ draft,
-                                                                      int32_t *__restrict__ draft_tokens,
-                                                                      const float *__restrict__ u, StatParams sp,
-                                                                      float2 *__restrict__ sub,
-                                                                      unsigned *__restrict__ tickets, WsHeader *hdr) {
+// and draws.  Each lane streams its 64 entries in NR rounds (all loads of a
+// round in flight) with its own running (max, sum), merged over the warp at
+// the end: NR = 1 (all 64 in flight, 2 CTAs per SM) when the grid fits in two
+// CTAs per SM, else NR = 2 (4 CTAs per SM).  Measured at vocab 128256: batch
+// 32, 256 CTAs, 11 us per draw in a chain of draft steps with NR = 1 against
+// 13 us with NR = 2; batch 128, 1024 CTAs, 18.7 us with NR = 2 against 20.2 us
+// with NR = 1 and 23.8 us with NR = 4 at 32 registers (one wave of 8 CTAs per
+// SM, but four dependent rounds).  The stream uses the default L2 policy, so
+// that the completing CTA's second read of the chosen sub-range finds it in L2.
+template <bool VEC4, int NR>
+__global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4) spec_draw_row_kernel(const float *__restrict__ draft,
+                                                                         int32_t *__restrict__ draft_tokens,
+                                                                         const float *__restrict__ u, StatParams sp,
+                                                                         float2 *__restrict__ sub,
+                                                                         unsigned *__restrict__ tickets,
+                                                                         WsHeader *hdr) {
   pdl_launch_dependents();
   {  // warm L2 with this CTA's 64 KB of the row while the previous kernel finishes (prefetch only)
     const float *x0 = draft + (static_cast<size_t>(blockIdx.x) * sp.gamma + (sp.r_begin - sp.gamma - 1)) * sp.V;
@@ -338,6 +348,7 @@ __global__ void __launch_bounds__(kStatThreads) spec_draw_row_kernel(const float
   __shared__ int s_last;
   __shared__ float s_M;
   __shared__ DrawShared sh;
+  __shared__ float2 s_rec[kRecSmem];
   const int b = blockIdx.x, s = blockIdx.y;
   const int row = sp.r_begin - sp.gamma - 1;  // draft position
   const int V = sp.V;
@@ -345,42 +356,50 @@ __global__ void __launch_bounds__(kStatThreads) spec_draw_row_kernel(const float
   const float *x = draft + (static_cast<size_t>(b) * sp.gamma + row) * V;
   float2 *sub_b = sub + static_cast<size_t>(b) * sp.nsub;
   {
-    // this warp's sub-range: 64 entries per lane in two rounds of 32 (8 float4 loads in flight)
     const int g = s * kWarps + warp;
     const int lo = g * kSub, hi = min(V, lo + kSub);
     float m = -INFINITY, l = 0.f;
     if (lo < hi) {
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        float v[32];
+      for (int h = 0; h < NR; ++h) {
+        constexpr int PER = 64 / NR, F4 = PER / 4;
+        float v[PER];
         if (VEC4) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int i = lo + 4 * lane + 128 * (8 * h + k);
-            const float4 f = (i < hi) ? __ldcs(reinterpret_cast<const float4 *>(x + i))
+          for (int k = 0; k < F4; ++k) {
+            const int i = lo + 4 * lane + 128 * (F4 * h + k);
+            const float4 f = (i < hi) ? __ldg(reinterpret_cast<const float4 *>(x + i))
                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             v[4 * k] = f.x, v[4 * k + 1] = f.y, v[4 * k + 2] = f.z, v[4 * k + 3] = f.w;
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int i = lo + lane + 32 * (32 * h + k);
-            v[k] = (i < hi) ? __ldcs(x + i) : -INFINITY;
+          for (int k = 0; k < PER; ++k) {
+            const int i = lo + lane + 32 * (PER * h + k);
+            v[k] = (i < hi) ? __ldg(x + i) : -INFINITY;
           }
         }
         float mx = v[0];
 #pragma unroll
-        for (int k = 1; k < 32; ++k) mx = fmaxf(mx, v[k]);
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float mn = fmaxf(m, mx);
-        const float ml = (mn == -INFINITY) ? 0.f : mn * kLog2e;  // -inf logits (masked entries) weigh 0
-        float t = 0.f;
+        for (int k = 1; k < PER; ++k) mx = fmaxf(mx, v[k]);
+        if (mx > m) {
+          l *= ex2((m - mx) * kLog2e);  // 0 while m is -inf (l is 0 then as well)
+          m = mx;
+        }
+        if (m != -INFINITY) {  // -inf logits (masked entries) weigh 0
+          const float ml = m * kLog2e;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) t += ex2(fmaf(v[k], kLog2e, -ml));
-        l = (m == -INFINITY) ? t : l * ex2((m - mn) * kLog2e) + t;
-        m = mn;
+          for (int k = 0; k < PER; ++k) l += ex2(fmaf(v[k], kLog2e, -ml));
+        }
       }
-      l = warp_sum_xor(l, 1, 16);
+    }
+    for (int o = 16; o > 0; o >>= 1) {  // merge the lanes' (max, sum)
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      const float mn = fmaxf(m, m2);
+      const float mu = (mn == -INFINITY) ? 0.f : mn;
+      l = l * ex2((m - mu) * kLog2e) + l2 * ex2((m2 - mu) * kLog2e);
+      m = mn;
     }
     if (lane == 0 && g < sp.nsub) sub_b[g] = make_float2(m, l);
     __syncthreads();
@@ -392,14 +411,21 @@ __global__ void __launch_bounds__(kStatThreads) spec_draw_row_kernel(const float
     if (!s_last) return;
     __threadfence();
   }
-  // this CTA completed the sequence: sub-range weights relative to the row max, then the draw
+  // this CTA completed the sequence: the sub-range records (one read, into shared memory when
+  // they fit), weights relative to the row max, then the draw
+  const bool rec_smem = sp.nsub <= kRecSmem;
+  if (rec_smem) {
+    for (int q = threadIdx.x; q < sp.nsub; q += kStatThreads) s_rec[q] = __ldcg(&sub_b[q]);
+    __syncthreads();
+  }
   if (warp == 0) {
+    auto rec = [&](int q) { return rec_smem ? s_rec[q] : __ldcg(&sub_b[q]); };
     float M = -INFINITY;
-    for (int q = lane; q < sp.nsub; q += 32) M = fmaxf(M, __ldcg(&sub_b[q].x));
+    for (int q = lane; q < sp.nsub; q += 32) M = fmaxf(M, rec(q).x);
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (lane == 0) s_M = M;
     auto wsum = [&](int q) {
-      const float2 r = __ldcg(sub_b + q);
+      const float2 r = rec(q);
       return r.y * exp2f((r.x - M) * kLog2e);
     };
     pick_sub(wsum, sp.nsub, u[(static_cast<size_t>(b) * (sp.gamma + 1) + row) * 3 + 0], sh);
@@ -429,25 +455,30 @@ __device__ __forceinline__ void merge_row(const float2 *st, int nsplit, float &M
 // Rejection sampling, CTA (b, s): the acceptance decisions of sequence b (the
 // same in every CTA of b), then the weight sums of the final draw over the
 // sub-ranges of chunk s; the CTA completing the sequence draws and writes the
-// round's tokens.
-template <bool VEC4>
-__global__ void __launch_bounds__(kStatThreads) spec_decide_kernel(const float *__restrict__ target,
-                                                                    const float *__restrict__ draft,
-                                                                    const int32_t *__restrict__ draft_tokens,
-                                                                    const float *__restrict__ u, StatParams sp,
-                                                                    const float2 *__restrict__ stats,
-                                                                    float2 *__restrict__ sub,
-                                                                    unsigned *__restrict__ tickets,
-                                                                    int32_t *__restrict__ out_tokens,
-                                                                    int32_t *__restrict__ num_accepted,
-                                                                    WsHeader *hdr) {
+// round's tokens.  Each lane streams its 64 entries of the two rows in NR
+// rounds (all loads of a round in flight): NR = 2 (32 entries of each row in
+// flight, 3 CTAs per SM) when the grid fits in one wave of that, else NR = 8
+// (8 of each row, held to 32 registers so that 8 CTAs share an SM: a batch of
+// 128 sequences at vocab 128256 runs as one wave of 1024 CTAs).
+template <bool VEC4, int NR>
+__global__ void __launch_bounds__(kStatThreads, NR == 2 ? 3 : (NR == 4 ? 4 : 8)) spec_decide_kernel(const float *__restrict__ target,
+                                                                       const float *__restrict__ draft,
+                                                                       const int32_t *__restrict__ draft_tokens,
+                                                                       const float *__restrict__ u, StatParams sp,
+                                                                       const float2 *__restrict__ stats,
+                                                                       float2 *__restrict__ sub,
+                                                                       unsigned *__restrict__ tickets,
+                                                                       int32_t *__restrict__ out_tokens,
+                                                                       int32_t *__restrict__ num_accepted,
+                                                                       WsHeader *hdr) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float sM[33], siZ[33];
   __shared__ int s_tok[16];
   __shared__ unsigned char s_ok[16], s_bad[16];
-  __shared__ int s_j, s_last;
+  __shared__ int s_j, s_last, s_use_p;
   __shared__ DrawShared sh;
+  __shared__ float2 s_rec[kRecSmem];
   const int b = blockIdx.x, s = blockIdx.y;
   const int g = sp.gamma, V = sp.V;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -481,42 +512,44 @@ __global__ void __launch_bounds__(kStatThreads) spec_decide_kernel(const float *
   }
   __syncthreads();
   const int j = s_j;
-  // the draw's weights: the residual at a rejection (kind 1) and p_j for the rare
-  // case where the residual sums to zero; p of the bonus row otherwise
-  const Weights wr{row_ptr(target, draft, b, j, g, V), row_ptr(target, draft, b, g + 1 + min(j, g - 1), g, V),
-                   sM[j], siZ[j], sM[g + 1 + min(j, g - 1)], siZ[g + 1 + min(j, g - 1)], j < g ? 1 : 0};
-  const Weights wp{wr.a, nullptr, sM[j], siZ[j], 0.f, 0.f, 0};
+  const int jc = g + 1 + min(j, g - 1);  // the draft row of position j (read only when j < g)
   float2 *sub_b = sub + static_cast<size_t>(b) * sp.nsub;
   {
-    // this warp's sub-range in two rounds of 32 entries per lane, every load of a round in
-    // flight at once (8 float4 of each row); each target value serves both sums
+    // the draw's weights over this warp's sub-range: the residual max(0, p - q) at a
+    // rejection (and p_j as well, for the rare case where the residual sums to zero), p of
+    // the bonus row otherwise; each target value serves both sums
+    const float *ra = row_ptr(target, draft, b, j, g, V);
+    const float *rc = row_ptr(target, draft, b, jc, g, V);
+    const float Ma = sM[j], ia = siZ[j], Mc = sM[jc], ic = siZ[jc];
+    const bool resid = j < g;
     const int sg = s * kWarps + warp;
     const int lo = sg * kSub, hi = min(V, lo + kSub);
     float r = 0.f, pp = 0.f;
 #pragma unroll 1
-    for (int h = 0; h < 2 && lo < hi; ++h) {
-      float a[32], c[32];
+    for (int h = 0; h < NR && lo < hi; ++h) {
+      constexpr int PER = 64 / NR, F4 = PER / 4;
+      float a[PER], c[PER];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int i = lo + 4 * lane + 128 * (8 * h + k);
+      for (int k = 0; k < F4; ++k) {
+        const int i = lo + 4 * lane + 128 * (F4 * h + k);
         if (VEC4 && i + 3 < hi) {
-          const float4 fa = __ldg(reinterpret_cast<const float4 *>(wr.a + i));
+          const float4 fa = __ldg(reinterpret_cast<const float4 *>(ra + i));
           a[4 * k] = fa.x, a[4 * k + 1] = fa.y, a[4 * k + 2] = fa.z, a[4 * k + 3] = fa.w;
-          const float4 fc = (j < g) ? __ldg(reinterpret_cast<const float4 *>(wr.c + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 fc = resid ? __ldg(reinterpret_cast<const float4 *>(rc + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
           c[4 * k] = fc.x, c[4 * k + 1] = fc.y, c[4 * k + 2] = fc.z, c[4 * k + 3] = fc.w;
         } else {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            a[4 * k + e] = (i + e < hi) ? __ldg(wr.a + i + e) : -INFINITY;
-            c[4 * k + e] = (j < g && i + e < hi) ? __ldg(wr.c + i + e) : 0.f;
+            a[4 * k + e] = (i + e < hi) ? __ldg(ra + i + e) : -INFINITY;
+            c[4 * k + e] = (resid && i + e < hi) ? __ldg(rc + i + e) : 0.f;
           }
         }
       }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float pa = exp2f((a[e] - wr.Ma) * kLog2e) * wr.ia;  // p, as the weights functions compute it
+      for (int e = 0; e < PER; ++e) {
+        const float pa = exp2f((a[e] - Ma) * kLog2e) * ia;  // p, as the weights functions compute it
         pp += pa;
-        r += (j < g) ? fmaxf(0.f, pa - exp2f((c[e] - wr.Mc) * kLog2e) * wr.ic) : pa;
+        r += resid ? fmaxf(0.f, pa - exp2f((c[e] - Mc) * kLog2e) * ic) : pa;
       }
     }
     r = warp_sum_xor(r, 1, 16);
@@ -531,20 +564,30 @@ __global__ void __launch_bounds__(kStatThreads) spec_decide_kernel(const float *
     if (!s_last) return;
     __threadfence();
   }
-  // this CTA completed the sequence: draw the correction (or bonus) token
-  __shared__ int s_use_p;
+  // this CTA completed the sequence: the sub-range sums (one read, into shared memory when
+  // they fit), then the draw of the correction (or bonus) token
+  const bool rec_smem = sp.nsub <= kRecSmem;
+  if (rec_smem) {
+    for (int q = threadIdx.x; q < sp.nsub; q += kStatThreads) s_rec[q] = __ldcg(&sub_b[q]);
+    __syncthreads();
+  }
   if (warp == 0) {
+    auto rec = [&](int q) { return rec_smem ? s_rec[q] : __ldcg(&sub_b[q]); };
     float zr = 0.f;
-    for (int q = lane; q < sp.nsub; q += 32) zr += __ldcg(&sub_b[q].x);
+    for (int q = lane; q < sp.nsub; q += 32) zr += rec(q).x;
     zr = warp_sum_xor(zr, 1, 16);
     const int use_p = (j < g && !(zr > 0.f)) ? 1 : 0;  // the residual vanished through rounding: draw from p_j
     if (lane == 0) s_use_p = use_p;
-    auto wsum = [&](int q) { return use_p ? __ldcg(&sub_b[q].y) : __ldcg(&sub_b[q].x); };
+    auto wsum = [&](int q) { return use_p ? rec(q).y : rec(q).x; };
     pick_sub(wsum, sp.nsub, u[(static_cast<size_t>(b) * (g + 1) + j) * 3 + 2], sh);
   }
   __syncthreads();
   int tok = -1;
-  if (sh.sub >= 0) tok = draw_in_sub<VEC4>(s_use_p ? wp : wr, V, sh);
+  if (sh.sub >= 0) {
+    const Weights wr{row_ptr(target, draft, b, j, g, V), row_ptr(target, draft, b, jc, g, V), sM[j], siZ[j],
+                     sM[jc], siZ[jc], (j < g && !s_use_p) ? 1 : 0};
+    tok = draw_in_sub<VEC4>(wr, V, sh);
+  }
   if (threadIdx.x == 0) {
     int32_t *o = out_tokens + static_cast<size_t>(b) * (g + 1);
     for (int i = 0; i < j; ++i) o[i] = s_tok[i];
@@ -575,6 +618,13 @@ SpecPlan plan_spec(int B, int gamma, int V) {
   return p;
 }
 
+// Resident CTAs of kStatThreads threads per SM for a kernel (0 if the query fails).
+static int ctas_per_sm(const void *fn) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kStatThreads, 0) != cudaSuccess) n = 0;
+  return n;
+}
+
 cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   StatParams sp;
   sp.B = p.B;
@@ -592,14 +642,20 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   const bool vec4 = (p.V % 4) == 0 && (reinterpret_cast<uintptr_t>(a.draft) % 16) == 0 &&
                     (a.target == nullptr || (reinterpret_cast<uintptr_t>(a.target) % 16) == 0);
   const dim3 grid(p.B, p.nsplit);
+  // the round counts that keep every CTA of the grid resident at once when the grid is small
+  const long long ctas = static_cast<long long>(p.B) * p.nsplit, sms = current_sm_count();
+  static const int occ_draw1 = ctas_per_sm(reinterpret_cast<const void *>(spec_draw_row_kernel<true, 1>));
+  static const int occ_decide2 = ctas_per_sm(reinterpret_cast<const void *>(spec_decide_kernel<true, 2>));
   if (a.mode == 1) {  // draft draws: one launch per drawn row
+    const bool one = ctas <= occ_draw1 * sms;
+    auto kd = vec4 ? (one ? spec_draw_row_kernel<true, 1> : spec_draw_row_kernel<true, 2>)
+                   : (one ? spec_draw_row_kernel<false, 1> : spec_draw_row_kernel<false, 2>);
     const int r0 = a.row < 0 ? 0 : a.row, r1 = a.row < 0 ? p.gamma : a.row + 1;
     for (int r = r0; r < r1; ++r) {
       sp.r_begin = p.gamma + 1 + r;
       sp.nr = 1;
-      const cudaError_t e =
-          launch_pdl(vec4 ? spec_draw_row_kernel<true> : spec_draw_row_kernel<false>, grid, dim3(kStatThreads), 0,
-                     a.stream, a.draft, a.draft_tokens, a.u, sp, sub, tickets, hdr);
+      const cudaError_t e = launch_pdl(kd, grid, dim3(kStatThreads), 0, a.stream, a.draft, a.draft_tokens, a.u, sp,
+                                       sub, tickets, hdr);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -610,7 +666,10 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   cudaError_t e = launch_pdl(vec4 ? spec_stats_kernel<true> : spec_stats_kernel<false>, g1, dim3(kStatThreads), 0,
                              a.stream, a.target, a.draft, sp, stats);
   if (e != cudaSuccess) return e;
-  return launch_pdl(vec4 ? spec_decide_kernel<true> : spec_decide_kernel<false>, grid, dim3(kStatThreads), 0, a.stream,
+  const bool wide = ctas <= occ_decide2 * sms;
+  auto kc = vec4 ? (wide ? spec_decide_kernel<true, 2> : spec_decide_kernel<true, 8>)
+                 : (wide ? spec_decide_kernel<false, 2> : spec_decide_kernel<false, 8>);
+  return launch_pdl(kc, grid, dim3(kStatThreads), 0, a.stream,
                     a.target, a.draft, a.draft_tokens, a.u, sp, stats, sub, tickets, a.out_tokens, a.num_accepted,
                     hdr);
 }
