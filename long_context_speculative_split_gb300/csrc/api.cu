@@ -3,6 +3,7 @@
 // to the kernel launchers.  No device memory is allocated here.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <cstdarg>
@@ -228,6 +229,7 @@ mgd_status mgd_verify_attn(const void *q, const void *k, const void *v, const in
                            int Hkv, int D, int kv_cap, int64_t kv_batch_stride, int64_t kv_head_stride,
                            float sm_scale, mgd_dtype in_dtype, void *out, mgd_dtype out_dtype, float *lse, void *ws,
                            size_t ws_bytes, void *stream) {
+  const NvtxRange nvtx_range("mgd_verify_attn");
   return run_attention(q, k, v, kv_len, B, T, Hq, Hkv, D, kv_cap, kv_batch_stride, kv_head_stride, sm_scale, in_dtype,
                        out, out_dtype, lse, ws, ws_bytes, stream);
 }
@@ -240,6 +242,7 @@ mgd_status mgd_draft_attn(const void *q, const void *k_draft, const void *v_draf
                           int Hq, int Hkv, int D, int k_cap, int64_t kv_batch_stride, int64_t kv_head_stride,
                           float sm_scale, mgd_dtype in_dtype, void *out, mgd_dtype out_dtype, float *lse, void *ws,
                           size_t ws_bytes, void *stream) {
+  const NvtxRange nvtx_range("mgd_draft_attn");
   return run_attention(q, k_draft, v_draft, draft_len, B, 1, Hq, Hkv, D, k_cap, kv_batch_stride, kv_head_stride,
                        sm_scale, in_dtype, out, out_dtype, lse, ws, ws_bytes, stream);
 }
@@ -320,6 +323,7 @@ mgd_status mgd_snapkv_select(const void *q_win, const void *k, const void *v, co
                              int pool, int K, float sm_scale, mgd_dtype in_dtype, int32_t *sel_idx, void *k_draft,
                              void *v_draft, int draft_cap, int32_t *draft_len, float *scores, void *ws,
                              size_t ws_bytes, void *stream) {
+  const NvtxRange nvtx_range("mgd_snapkv_select");
   return run_snapkv(q_win, k, v, kv_len, B, Hq, Hkv, D, kv_cap, kv_batch_stride, kv_head_stride, W, pool, K, nullptr,
                     sm_scale, in_dtype, sel_idx, k_draft, v_draft, draft_cap, draft_len, scores, ws, ws_bytes, stream);
 }
@@ -330,6 +334,7 @@ mgd_status mgd_snapkv_select_budgets(const void *q_win, const void *k, const voi
                                      mgd_dtype in_dtype, int32_t *sel_idx, void *k_draft, void *v_draft,
                                      int draft_cap, int32_t *draft_len, float *scores, void *ws, size_t ws_bytes,
                                      void *stream) {
+  const NvtxRange nvtx_range("mgd_snapkv_select_budgets");
   if (B > 0 && !budgets) return fail(MGD_ERR_INVALID_ARG, "null budgets");
   return run_snapkv(q_win, k, v, kv_len, B, Hq, Hkv, D, kv_cap, kv_batch_stride, kv_head_stride, W, pool, W,
                     B > 0 ? budgets : nullptr, sm_scale, in_dtype, sel_idx, k_draft, v_draft, draft_cap, draft_len,
@@ -350,6 +355,7 @@ mgd_status mgd_topk_draft_attn(const void *q, const void *k, const void *v, cons
                                float sm_scale, mgd_dtype in_dtype, int32_t *sel_idx, void *k_draft,
                                void *v_draft, int draft_cap, int32_t *draft_len, void *out, mgd_dtype out_dtype,
                                float *lse, void *ws, size_t ws_bytes, void *stream) {
+  const NvtxRange nvtx_range("mgd_topk_draft_attn");
   if (K < 1) return fail(MGD_ERR_INVALID_ARG, "budget K must be >= 1 (got %d)", K);
   if (B > 0 && !out) return fail(MGD_ERR_INVALID_ARG, "null pointer argument");
   const size_t need = mgd_topk_draft_workspace_size(B, Hq, Hkv, D, kv_cap, draft_cap);
@@ -377,6 +383,7 @@ size_t mgd_spec_workspace_size(int B, int gamma, int V) {
 mgd_status mgd_spec_sample(const float *target_logits, const float *draft_logits, int32_t *draft_tokens,
                            const float *u, int B, int gamma, int V, int mode, int row, int32_t *out_tokens,
                            int32_t *num_accepted, void *ws, size_t ws_bytes, void *stream) {
+  const NvtxRange nvtx_range("mgd_spec_sample");
   if (B < 0) return fail(MGD_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
   if (gamma < 1 || gamma > 16) return fail(MGD_ERR_UNSUPPORTED, "gamma must be in [1, 16] (got %d)", gamma);
   if (V < 1) return fail(MGD_ERR_INVALID_ARG, "V must be >= 1 (got %d)", V);
@@ -408,6 +415,7 @@ mgd_status mgd_streaming_select(const void *k, const void *v, const int32_t *kv_
                                 int kv_cap, int64_t kv_batch_stride, int64_t kv_head_stride, int sink, int K,
                                 mgd_dtype dtype, int32_t *sel_idx, void *k_draft, void *v_draft, int draft_cap,
                                 int32_t *draft_len, void *stream) {
+  const NvtxRange nvtx_range("mgd_streaming_select");
   if (B < 0) return fail(MGD_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
   if (Hkv < 1 || D < 1 || kv_cap < 1) return fail(MGD_ERR_INVALID_ARG, "need Hkv, D, kv_cap >= 1");
   if (sink < 0 || K < 1 || draft_cap < K)
@@ -440,6 +448,7 @@ mgd_status mgd_commit_round(const int32_t *num_accepted, int B, int gamma, int H
                             int64_t kv_head_stride, void *k_draft, void *v_draft, int draft_cap,
                             int64_t draft_batch_stride, int64_t draft_head_stride, int32_t *draft_len, void *ws,
                             size_t ws_bytes, void *stream) {
+  const NvtxRange nvtx_range("mgd_commit_round");
   if (B < 0) return fail(MGD_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
   if (gamma < 1 || gamma > 16) return fail(MGD_ERR_UNSUPPORTED, "gamma must be in [1, 16] (got %d)", gamma);
   if (Hkv < 1 || D < 1) return fail(MGD_ERR_INVALID_ARG, "need Hkv >= 1 and D >= 1");

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -38,6 +39,15 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 constexpr size_t kAlign = 256;
+
+// An NVTX range named after the entry point, open for the duration of one call
+// (the host-side enqueue).  Without a profiler attached the calls return at once.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Whether kernels are launched with programmatic stream serialization
 // (mgd_set_programmatic_launch; on by default).

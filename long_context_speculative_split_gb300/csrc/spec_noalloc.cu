@@ -47,6 +47,7 @@ extern "C" mgd_status mgd_spec_sample_noalloc(const float *target_logits, const 
                                               int32_t *draft_tokens, const float *u, int B, int gamma, int V,
                                               int mode, int row, int32_t *out_tokens, int32_t *num_accepted,
                                               void *stream) {
+  const mgd::NvtxRange nvtx_range("mgd_spec_sample_noalloc");
   if (B <= 0)  // argument checks only (B == 0 is a no-op); nothing touches the GPU
     return mgd_spec_sample(target_logits, draft_logits, draft_tokens, u, B, gamma, V, mode, row, out_tokens,
                            num_accepted, nullptr, 0, stream);
