@@ -811,6 +811,10 @@ __device__ __forceinline__ void select_pair(const unsigned char *__restrict__ k,
       const int b_lo = b_hi - 1;
       const unsigned c_hi = (b_hi >= 0) ? hist[b_hi] : 0u;
       const unsigned c_lo = (b_lo >= 0) ? hist[b_lo] : 0u;
+      if (threadIdx.x == 0) {  // set below by the one thread whose bins hold the krem-th value
+        s_bin = 0u;
+        s_above = 0u;
+      }
       unsigned tot;
       const unsigned above = block_excl_scan(c_hi + c_lo, sm_warp, &tot);
       if (b_hi >= 0 && above < krem && krem <= above + c_hi) {
@@ -900,7 +904,8 @@ __device__ __forceinline__ void select_pair(const unsigned char *__restrict__ k,
       classify(j, key[u], gt, eq);
       const unsigned gb = __ballot_sync(0xffffffffu, gt), eb = __ballot_sync(0xffffffffu, eq);
       const unsigned gpos = g_before + __popc(gb & lt_mask), epos = e_before + __popc(eb & lt_mask);
-      if (gt || (eq && epos < krem)) sel[gpos + min(epos, krem)] = j;
+      const unsigned dst = gpos + min(epos, krem);  // < ktop whenever the counts are those of the data
+      if ((gt || (eq && epos < krem)) && dst < static_cast<unsigned>(ktop)) sel[dst] = j;
       g_before += __popc(gb);
       e_before += __popc(eb);
     }
@@ -925,7 +930,10 @@ __device__ __forceinline__ void select_pair(const unsigned char *__restrict__ k,
       const int i = i0 + u * kSelThreads;
       if (i < total) {
         const int row = i / vecs, c = i % vecs;
-        const size_t src = static_cast<size_t>(sel[row]) * sp.row_bytes + c * 16;
+        // kept positions lie in [0, L); the clamp only guards the reads against a selection
+        // whose counts were not those of its data
+        const int pos = min(max(sel[row], 0), L - 1);
+        const size_t src = static_cast<size_t>(pos) * sp.row_bytes + c * 16;
         dst[u] = static_cast<size_t>(row) * sp.row_bytes + c * 16;
         kx[u] = __ldg(reinterpret_cast<const uint4 *>(ks + src));
         vx[u] = __ldg(reinterpret_cast<const uint4 *>(vs + src));
