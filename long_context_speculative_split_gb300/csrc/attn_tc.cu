@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
     unsigned char *st = smem + stage * Lay::kStageBytes;
     const int key0 = start + md.tile * kTileKeys + warp * 16;
+    bool released = false;  // this warp has handed the stage back to the producer
     if (key0 < L) {
       // ---- S^T[16 keys][8*NT rows] = K Q^T
       float s[NT][4];
@@ -321,6 +322,37 @@ __global__ void __launch_bounds__(kThreads, MINB)
           if (2 * jp + 1 < NT) mma_bf16_16816(s[2 * jp + 1], a0, a1, a2, a3, b2, b3);
         }
       }
+      // ---- rows past the sequence end hold stale bytes: zero this warp's V rows there
+      if (key0 + 16 > L) {
+        const int r0 = L - key0;  // first invalid local row (1..15)
+        const int nchunks = (16 - r0) * 8 * Lay::kBoxes;
+        for (int i = lane; i < nchunks; i += 32) {
+          const int h = i / ((16 - r0) * 8);
+          const int rem = i % ((16 - r0) * 8);
+          const int r = warp * 16 + r0 + rem / 8;
+          const int c = rem % 8;
+          *reinterpret_cast<uint4 *>(st + (Lay::kBoxes + h) * kBoxBytes + swz128(r, c)) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // ---- this warp's V^T fragments into registers, then the stage goes back to the
+      //      producer: the softmax and O^T += V^T P^T below no longer hold it, so the
+      //      ring keeps more tiles in flight
+      uint32_t va[MT][4];
+      {
+        const uint32_t vbase = smem_addr(st + Lay::kBoxes * kBoxBytes);
+        const int vr = warp * 16 + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int d = 16 * mt + 8 * ((lane >> 3) & 1);
+          ldsm_x4_t(vbase + (d >> 6) * kBoxBytes + swz128(vr, (d & 63) >> 3), va[mt][0], va[mt][1], va[mt][2],
+                    va[mt][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      released = true;
       // ---- scale, mask, online softmax (exp2 domain)
       const bool need_mask = key0 + 15 > L - p.T;
       const int k_lo = key0 + gid, k_hi = key0 + gid + 8;
@@ -365,37 +397,20 @@ __global__ void __launch_bounds__(kThreads, MINB)
         plo[j][0] = movmatrix_t(l0);
         plo[j][1] = movmatrix_t(l1);
       }
-      // ---- rows past the sequence end hold stale bytes: zero this warp's V rows there
-      if (key0 + 16 > L) {
-        const int r0 = L - key0;  // first invalid local row (1..15)
-        const int nchunks = (16 - r0) * 8 * Lay::kBoxes;
-        for (int i = lane; i < nchunks; i += 32) {
-          const int h = i / ((16 - r0) * 8);
-          const int rem = i % ((16 - r0) * 8);
-          const int r = warp * 16 + r0 + rem / 8;
-          const int c = rem % 8;
-          *reinterpret_cast<uint4 *>(st + (Lay::kBoxes + h) * kBoxBytes + swz128(r, c)) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
       // ---- O^T[D][rows] += V^T P^T
-      const uint32_t vbase = smem_addr(st + Lay::kBoxes * kBoxBytes);
-      const int vr = warp * 16 + (lane & 7) + 8 * (lane >> 4);
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const int d = 16 * mt + 8 * ((lane >> 3) & 1);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(vbase + (d >> 6) * kBoxBytes + swz128(vr, (d & 63) >> 3), a0, a1, a2, a3);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          mma_bf16_16816(acc[mt][j], a0, a1, a2, a3, phi[j][0], phi[j][1]);
-          mma_bf16_16816(acc[mt][j], a0, a1, a2, a3, plo[j][0], plo[j][1]);
+          mma_bf16_16816(acc[mt][j], va[mt][0], va[mt][1], va[mt][2], va[mt][3], phi[j][0], phi[j][1]);
+          mma_bf16_16816(acc[mt][j], va[mt][0], va[mt][1], va[mt][2], va[mt][3], plo[j][0], plo[j][1]);
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (!released) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
     if (++stage == kStages) {
       stage = 0;
       phase ^= 1u;
