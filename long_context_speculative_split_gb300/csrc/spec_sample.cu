@@ -482,23 +482,36 @@ __global__ void __launch_bounds__(kStatThreads, NR == 2 ? 3 : (NR == 4 ? 4 : 8))
   const int b = blockIdx.x, s = blockIdx.y;
   const int g = sp.gamma, V = sp.V;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the candidates' tokens and the two logits at each are loaded by warp 2 while warp 0
+  // merges the row statistics (the loads do not depend on the statistics)
+  constexpr int kCand = 64;  // first thread of the candidate tests (gamma <= 16, nrows <= 33)
+  const int ci = static_cast<int>(threadIdx.x) - kCand;
+  int xi = -1;
+  bool bad = true;
+  float xa = 0.f, xc = 0.f, uu = 0.f;
+  if (ci >= 0 && ci < g) {
+    xi = draft_tokens[static_cast<size_t>(b) * g + ci];
+    bad = (xi < 0 || xi >= V);
+    if (!bad) {
+      xa = row_ptr(target, draft, b, ci, g, V)[xi];
+      xc = row_ptr(target, draft, b, g + 1 + ci, g, V)[xi];
+      uu = u[(static_cast<size_t>(b) * (g + 1) + ci) * 3 + 1];
+    }
+  }
   for (int r = threadIdx.x; r < sp.nrows; r += kStatThreads)
     merge_row(stats + (static_cast<size_t>(b) * sp.nrows + r) * sp.nsplit, sp.nsplit, sM[r], siZ[r]);
   __syncthreads();
   // every candidate's test at once; the chain keeps the prefix before the first rejection
-  if (threadIdx.x < g) {
-    const int i = threadIdx.x;
-    const int xi = draft_tokens[static_cast<size_t>(b) * g + i];
-    const bool bad = (xi < 0 || xi >= V);
+  if (ci >= 0 && ci < g) {
     bool acc = false;
     if (!bad) {
-      const float px = exp2f((row_ptr(target, draft, b, i, g, V)[xi] - sM[i]) * kLog2e) * siZ[i];
-      const float qx = exp2f((row_ptr(target, draft, b, g + 1 + i, g, V)[xi] - sM[g + 1 + i]) * kLog2e) * siZ[g + 1 + i];
-      acc = u[(static_cast<size_t>(b) * (g + 1) + i) * 3 + 1] * qx < px;
+      const float px = exp2f((xa - sM[ci]) * kLog2e) * siZ[ci];
+      const float qx = exp2f((xc - sM[g + 1 + ci]) * kLog2e) * siZ[g + 1 + ci];
+      acc = uu * qx < px;
     }
-    s_tok[i] = xi;
-    s_ok[i] = acc ? 1 : 0;
-    s_bad[i] = bad ? 1 : 0;
+    s_tok[ci] = xi;
+    s_ok[ci] = acc ? 1 : 0;
+    s_bad[ci] = bad ? 1 : 0;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
