@@ -120,13 +120,16 @@ def test_round_tokens_match_oracle(rnd, i):
     rt, rm = ref_draw(d, u)
     ok = rm >= SAMPLE_BAND
     assert np.array_equal(tok[ok], rt[ok])
-    ref = ref_reject(t, d, tok, u)
+    # the oracle verifies its own draft tokens; compared on the sequences where the GPU drew the same
+    ref = ref_reject(t, d, rt, u)
+    drew_same = np.all(tok == rt, axis=1)
+    assert drew_same.mean() > 0.9
     nacc, out = o["nacc"].cpu().numpy(), o["out_tok"].cpu().numpy()
     with np.errstate(invalid="ignore"):
         amb = ref["accept_margin"] < SAMPLE_BAND
     first = np.where(amb.any(axis=1), amb.argmax(axis=1), r.gamma + 1)
-    assert np.array_equal(np.minimum(nacc, first), np.minimum(ref["num_accepted"], first))
-    full = (first > r.gamma) & ~(ref["draw_margin"] < SAMPLE_BAND)
+    assert np.array_equal(np.minimum(nacc, first)[drew_same], np.minimum(ref["num_accepted"], first)[drew_same])
+    full = (first > r.gamma) & ~(ref["draw_margin"] < SAMPLE_BAND) & drew_same
     assert np.array_equal(out[full], ref["out_tokens"][full])
     # mean acceptance 0.9 by construction: tokens per round near Omega(3, 0.9) = 3.439
     x = nacc + 1.0

@@ -46,12 +46,14 @@ def _compare_round(t, d, u, dev, case=None, min_frac=0.75):
     tok_c = tok.cpu().numpy()
     ok_draw = rmarg >= SAMPLE_BAND
     assert np.array_equal(tok_c[ok_draw], rtok[ok_draw])
-    # the verify step reads the GPU's draft tokens; the oracle is given the same tokens
-    out, nacc = ops.rejection_sample(t.to(dev), d.to(dev), tok, u.to(dev), out_tokens=g["out_tokens"].t,
+    # the verify step reads the oracle's draft tokens, on both sides (no GPU output is an oracle input)
+    rtok_d = torch.from_numpy(np.ascontiguousarray(rtok, dtype=np.int32)).to(dev)
+    out, nacc = ops.rejection_sample(t.to(dev), d.to(dev), rtok_d, u.to(dev), out_tokens=g["out_tokens"].t,
                                      num_accepted=g["num_accepted"].t)
     torch.cuda.synchronize()
     check_guards(**g)
-    ref = ref_reject(t, d, tok_c, u)
+    tok_c = rtok
+    ref = ref_reject(t, d, rtok, u)
     out_c, nacc_c = out.cpu().numpy(), nacc.cpu().numpy()
     with np.errstate(invalid="ignore"):
         ambiguous = ref["accept_margin"] < SAMPLE_BAND          # [B, gamma], False where untested
