@@ -75,6 +75,26 @@ def _oracle_round(r, i):
     return rtok, ref, clear
 
 
+def _oracle_selection(r, layer, b, h):
+    """The oracle's SnapKV selection for one (layer, sequence, KV head) of the round's inputs:
+    (kept positions, pooled scores, score of the lowest-ranked kept prefix position)."""
+    G = r.Hq // r.Hkv
+    L = int(r.kv_len[b])
+    qw = wl.window_queries(r.cfg, r.dev, r.seed, layer=layer)
+    s = window_scores(qw[b:b + 1, :, h * G:(h + 1) * G], r.k[layer][b:b + 1, h:h + 1, :L], r.kv_len[b:b + 1], r.W,
+                      1.0 / math.sqrt(r.D))[0, 0]
+    pooled = np.zeros(L)
+    pooled[:L - r.W] = max_pool(s, L - r.W, r.P)
+    ref_idx = select_indices(pooled, L, r.W, r.K)
+    kth = np.min(pooled[ref_idx[:r.K - r.W]])
+    return ref_idx, pooled, kth
+
+
+def _oracle_draft_cache(r, layer, b, h, ref_idx):
+    sel = torch.from_numpy(np.asarray(ref_idx, dtype=np.int64))
+    return r.k[layer][b, h].cpu()[sel][None, None], r.v[layer][b, h].cpu()[sel][None, None]
+
+
 def test_round_attention_matches_oracle(rnd):
     r = rnd
     G, D = r.Hq // r.Hkv, r.D
@@ -85,28 +105,24 @@ def test_round_attention_matches_oracle(rnd):
         ref, _ = ref_attention(r.q[layer][b:b + 1, :, h * G:(h + 1) * G], r.k[layer][b:b + 1, h:h + 1, :L],
                                r.v[layer][b:b + 1, h:h + 1, :L], r.kv_len[b:b + 1], scale)
         assert_attention_close(o["vout"][layer, b:b + 1, :, h * G:(h + 1) * G], ref, "verify l%d" % layer)
-        sel = r.sel[layer]
-        K = int(r.pre[0]["lengths"][layer, 1, b])
+        # draft attention over the oracle's own selection (where the GPU kept the same rows)
+        ref_idx, pooled, kth = _oracle_selection(r, layer, b, h)
+        got = r.sel[layer]["sel_idx"][b, h].cpu().numpy()[:r.K]
+        assert_index_sets_match(got, ref_idx, pooled, kth)
+        if set(got.tolist()) != set(np.asarray(ref_idx).tolist()):
+            continue
+        kd, vd = _oracle_draft_cache(r, layer, b, h, ref_idx)
         for s in range(r.gamma):
-            rd, _ = ref_draft(r.qd[layer][s][b:b + 1, None, h * G:(h + 1) * G], sel["k_draft"][b:b + 1, h:h + 1, :K],
-                              sel["v_draft"][b:b + 1, h:h + 1, :K], torch.tensor([K]), scale)
+            rd, _ = ref_draft(r.qd[layer][s][b:b + 1, None, h * G:(h + 1) * G], kd, vd,
+                              torch.tensor([len(ref_idx)]), scale)
             assert_attention_close(o["dout"][layer, s, b:b + 1, h * G:(h + 1) * G], rd[:, 0],
                                    "draft l%d s%d" % (layer, s))
 
 
 def test_round_draft_cache_selection(rnd):
     r = rnd
-    G = r.Hq // r.Hkv
     layer, b, h = 9, 12, 2
-    L = int(r.kv_len[b])
-    qw = wl.window_queries(r.cfg, r.dev, r.seed, layer=layer)
-    s = window_scores(qw[b:b + 1, :, h * G:(h + 1) * G], r.k[layer][b:b + 1, h:h + 1, :L], r.kv_len[b:b + 1], r.W,
-                      1.0 / math.sqrt(r.D))[0, 0]
-    pooled = np.zeros(L)
-    pooled[:L - r.W] = max_pool(s, L - r.W, r.P)
-    ref_idx = select_indices(pooled, L, r.W, r.K)
-    n_top = r.K - r.W
-    kth = np.min(pooled[ref_idx[:n_top]])
+    ref_idx, pooled, kth = _oracle_selection(r, layer, b, h)
     got = r.sel[layer]["sel_idx"][b, h].cpu().numpy()
     assert_index_sets_match(got[:r.K], ref_idx, pooled, kth)
 
@@ -137,16 +153,21 @@ def test_round_tokens_match_oracle(rnd, i):
 
 
 def test_commit_over_two_rounds_matches_oracle(rnd):
-    """kv_len, draft_len and the draft-cache rows of layer LC after each of two consecutive rounds
-    equal the oracle's commit applied to the oracle's own decisions (bit-exact; every layer's
-    lengths move together)."""
+    """kv_len, draft_len and the draft-cache rows appended to layer LC after each of two
+    consecutive rounds equal the oracle's commit applied to the oracle's own decisions, from the
+    oracle's own starting lengths (bit-exact; every layer's lengths move together).  The selected
+    rows before the appended ones stay as the selection wrote them."""
     r = rnd
     i16 = lambda x: x.cpu().view(torch.int16).numpy()  # noqa: E731  (bf16 bytes, compared exactly)
     k, v = i16(r.k[LC]), i16(r.v[LC])
     pre = r.pre[0]
-    lens = pre["lengths"][LC, 0].cpu().numpy()
-    dlen = pre["lengths"][LC, 1].cpu().numpy()
-    kd, vd = i16(pre["kd"]), i16(pre["vd"])
+    lens = r.kv_len.numpy().astype(np.int64)                  # the inputs
+    dlen = np.minimum(r.K, lens)                              # K_eff: the selection's length
+    assert np.array_equal(pre["lengths"][LC, 0].cpu().numpy(), lens)
+    assert np.array_equal(pre["lengths"][LC, 1].cpu().numpy(), dlen)
+    kd = np.zeros(tuple(pre["kd"].shape), dtype=np.int16)   # the oracle appends into its own cache
+    vd = np.zeros_like(kd)
+    sel_k, sel_v = i16(pre["kd"]), i16(pre["vd"])
     clear = np.ones(r.B, dtype=bool)
     for i in range(2):
         _, ref, c = _oracle_round(r, i)
@@ -162,7 +183,11 @@ def test_commit_over_two_rounds_matches_oracle(rnd):
         assert np.array_equal(g[LC, 0][clear], lens[clear])
         assert np.array_equal(g[LC, 1][clear], dlen[clear])
         gk, gv = i16(after["kd"]), i16(after["vd"])
-        assert np.array_equal(gk[clear], kd[clear]) and np.array_equal(gv[clear], vd[clear])
+        for b in np.nonzero(clear)[0]:
+            lo = int(min(r.K, int(r.kv_len[b])))
+            hi = int(dlen[b])
+            assert np.array_equal(gk[b, :, lo:hi], kd[b, :, lo:hi]) and np.array_equal(gv[b, :, lo:hi], vd[b, :, lo:hi])
+            assert np.array_equal(gk[b, :, :lo], sel_k[b, :, :lo]) and np.array_equal(gv[b, :, :lo], sel_v[b, :, :lo])
 
 
 def test_second_round_attention_over_committed_state(rnd):
@@ -174,9 +199,7 @@ def test_second_round_attention_over_committed_state(rnd):
     scale = 1.0 / math.sqrt(D)
     _, ref1, _ = _oracle_round(r, 0)
     clear = r.post[0]["nacc"].cpu().numpy() == ref1["num_accepted"]
-    pre = r.pre[0]
-    lens0 = pre["lengths"][LC, 0].cpu().numpy()
-    dl0 = pre["lengths"][LC, 1].cpu().numpy()
+    lens0 = r.kv_len.numpy()
     bs = [b for b in (0, 7, 31) if clear[b]]
     assert bs
     o = r.post[1]
@@ -189,10 +212,16 @@ def test_second_round_attention_over_committed_state(rnd):
             ref, ref_lse = ref_attention(r.q[LC][b:b + 1, :, hs], r.k[LC][b:b + 1, h:h + 1, :L1],
                                          r.v[LC][b:b + 1, h:h + 1, :L1], torch.tensor([L1]), scale)
             assert_attention_close(o["vout"][LC, b:b + 1, :, hs], ref, "round-2 verify b%d h%d" % (b, h))
-            # the draft cache of round 2: the selected rows, then the n + 1 rows round 1 kept
-            dl = int(dl0[b])
-            kd = torch.cat([pre["kd"][b, h, :dl].cpu(), r.k[LC][b, h, first:first + n + 1].cpu()])[None, None]
-            vd = torch.cat([pre["vd"][b, h, :dl].cpu(), r.v[LC][b, h, first:first + n + 1].cpu()])[None, None]
+            # the draft cache of round 2: the oracle's selected rows, then the n + 1 rows round 1
+            # kept (compared where the GPU kept the same rows)
+            ref_idx, pooled, kth = _oracle_selection(r, LC, b, h)
+            got = r.sel[LC]["sel_idx"][b, h].cpu().numpy()[:r.K]
+            if set(got.tolist()) != set(np.asarray(ref_idx).tolist()):
+                continue
+            k_sel, v_sel = _oracle_draft_cache(r, LC, b, h, ref_idx)
+            dl = len(ref_idx)
+            kd = torch.cat([k_sel[0, 0], r.k[LC][b, h, first:first + n + 1].cpu()])[None, None]
+            vd = torch.cat([v_sel[0, 0], r.v[LC][b, h, first:first + n + 1].cpu()])[None, None]
             for s in range(r.gamma):
                 rd, rl = ref_draft(r.qd[LC][s][b:b + 1, None, hs], kd, vd, torch.tensor([dl + n + 1]), scale)
                 assert_attention_close(o["dout"][LC, s, b:b + 1, hs], rd[:, 0], "round-2 draft b%d s%d" % (b, s))
