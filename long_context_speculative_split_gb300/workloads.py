@@ -37,7 +37,7 @@ WORKLOADS = {
             pool=7, K=512, V=128256, sigma=3.0, sigma_n=ROUND_SIGMA_N, hh=0.01, layers=32),
 }
 
-_IDS = dict(k=1, v=2, q=3, qw=4, qd=5, hh=6, tl=7, dl=8, u=9, len=10)
+_IDS = dict(k=1, v=2, q=3, qw=4, qd=5, hh=6, tl=7, dl=8, u=9, len=10, mask=11)
 
 
 def sub_seed(seed, name, layer=0):
@@ -118,15 +118,28 @@ def draft_queries(cfg, device, seed=0, layer=0, step=0):
 
 
 def logits(cfg, device, seed=0, sigma_n="cfg"):
-    """(target [B, gamma+1, V], draft [B, gamma, V]) float32."""
+    """(target [B, gamma+1, V], draft [B, gamma, V]) float32.  With cfg["mask_frac"] = m, a seeded
+    fraction m of each sequence's vocabulary is -inf in all its rows (a constrained vocabulary),
+    and a further 2 % in its target rows only (entries the draft may propose but the target
+    forbids)."""
     B, g, V = cfg["B"], cfg["gamma"], cfg["V"]
     sn = cfg["sigma_n"] if sigma_n == "cfg" else sigma_n
     t = torch.randn((B, g + 1, V), generator=_gen(device, seed, "tl"), device=device) * cfg["sigma"]
     noise = torch.randn((B, g, V), generator=_gen(device, seed, "dl"), device=device)
+    m = cfg.get("mask_frac")
+    if m:
+        gm = _gen(device, seed, "mask")
+        shared = torch.rand((B, 1, V), generator=gm, device=device) < m
+        target_only = torch.rand((B, 1, V), generator=gm, device=device) < 0.02
+        t = t.masked_fill(shared, float("-inf"))
     if sn is None:
         d = noise * cfg["sigma"]
+        if m:
+            d = d.masked_fill(shared, float("-inf"))
     else:
         d = t[:, :g] + noise * sn
+    if m:
+        t = t.masked_fill(target_only, float("-inf"))
     return t, d.contiguous()
 
 

@@ -37,6 +37,7 @@ CASES = [
     ("b128_ctx32k", "b128_ctx32k", {}, 0),
     ("ragged_b256_ctx4k_64k", "ragged_b256_ctx4k_64k", {}, 0),
     ("odd_vocab_b300", "b32_ctx8k", dict(B=300, V=4099, gamma=5, sigma=2.0, sigma_n=1.0), 4),
+    ("masked_vocab_b64", "b32_ctx8k", dict(B=64, V=32000, mask_frac=0.6), 6),
 ]
 
 

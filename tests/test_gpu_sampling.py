@@ -101,6 +101,17 @@ def test_odd_vocab_and_many_sequences():
     _compare_round(t, d, u, dev, case="odd_vocab_b300")
 
 
+def test_masked_vocabulary():
+    """60 % of each sequence's vocabulary at -inf in every row, and 2 % more in the target rows
+    only: masked entries weigh nothing, a drafted token the target forbids is always rejected."""
+    dev = gpu_or_skip()
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=64, V=32000, mask_frac=0.6)
+    t, d = wl.logits(c, "cpu", seed=6)
+    u = wl.uniforms(c, "cpu", seed=6)
+    assert bool(torch.isinf(t).any()) and bool(torch.isinf(d).any())
+    _compare_round(t, d, u, dev, case="masked_vocab_b64")
+
+
 def test_single_row_draft_draw():
     dev = gpu_or_skip()
     c = wl.WORKLOADS["b32_ctx8k"]
