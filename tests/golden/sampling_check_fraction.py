@@ -38,6 +38,8 @@ CASES = [
     ("ragged_b256_ctx4k_64k", "ragged_b256_ctx4k_64k", {}, 0),
     ("odd_vocab_b300", "b32_ctx8k", dict(B=300, V=4099, gamma=5, sigma=2.0, sigma_n=1.0), 4),
     ("masked_vocab_b64", "b32_ctx8k", dict(B=64, V=32000, mask_frac=0.6), 6),
+    ("gamma1_b40", "b32_ctx8k", dict(B=40, V=5000, gamma=1), 7),
+    ("gamma16_b24", "b32_ctx8k", dict(B=24, V=5000, gamma=16), 8),
 ]
 
 

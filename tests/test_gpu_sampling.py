@@ -112,6 +112,16 @@ def test_masked_vocabulary():
     _compare_round(t, d, u, dev, case="masked_vocab_b64")
 
 
+@pytest.mark.parametrize("case,gamma,B,seed", [("gamma1_b40", 1, 40, 7), ("gamma16_b24", 16, 24, 8)])
+def test_gamma_extremes(case, gamma, B, seed):
+    """One draft position, and the largest number the library takes (16: 33 rows per sequence)."""
+    dev = gpu_or_skip()
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=B, V=5000, gamma=gamma)
+    t, d = wl.logits(c, "cpu", seed=seed)
+    u = wl.uniforms(c, "cpu", seed=seed)
+    _compare_round(t, d, u, dev, case=case)
+
+
 def test_single_row_draft_draw():
     dev = gpu_or_skip()
     c = wl.WORKLOADS["b32_ctx8k"]
