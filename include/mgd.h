@@ -149,7 +149,8 @@ mgd_status mgd_selftest_occupy(int ctas, int smem_bytes, int usec, void *stream)
  * Query head h reads KV head h / (Hq/Hkv).  Row t sits at position
  * kv_len[b]-T+t and attends to keys 0 .. kv_len[b]-T+t (causal among the
  * appended rows); scores are sm_scale * <q, k>; softmax and accumulation in
- * float32.  Supported: D in {64, 128}; 1 <= T <= 8; Hq % Hkv == 0.
+ * float32.  Supported: D in {64, 128}; 1 <= T <= 17 (gamma <= 16, as the sampling and
+ * commit calls take); Hq % Hkv == 0.
  * in_dtype MGD_BF16 runs the tensor-core split-KV kernel; MGD_F32 runs a
  * float32 CUDA-core kernel (for float32 inputs; not the timed path).
  * ------------------------------------------------------------------------ */

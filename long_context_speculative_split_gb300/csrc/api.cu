@@ -60,7 +60,7 @@ mgd_status check_attention(const void *q, const void *k, const void *v, const in
                            int Hkv, int D, int cap, int64_t bstride, int64_t hstride, mgd_dtype in_dtype,
                            const void *out, mgd_dtype out_dtype, const void *ws) {
   if (B < 0) return fail(MGD_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
-  if (T < 1 || T > 8) return fail(MGD_ERR_INVALID_ARG, "T must be in [1, 8] (got %d)", T);
+  if (T < 1 || T > 17) return fail(MGD_ERR_INVALID_ARG, "T must be in [1, 17] (got %d)", T);
   if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
     return fail(MGD_ERR_INVALID_ARG, "need Hq >= 1, Hkv >= 1 and Hq %% Hkv == 0 (got %d, %d)", Hq, Hkv);
   if (D != 64 && D != 128) return fail(MGD_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", D);

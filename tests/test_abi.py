@@ -73,7 +73,7 @@ def _verify(mgd, **kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(D=96), 2), (dict(Hq=6, Hkv=4), 1), (dict(T=0), 1), (dict(T=9), 1), (dict(q=None), 1),
+    (dict(D=96), 2), (dict(Hq=6, Hkv=4), 1), (dict(T=0), 1), (dict(T=18), 1), (dict(q=None), 1),
     (dict(kv_len=None), 1), (dict(k=FAKE + 8), 1), (dict(kv_head_stride=100), 1), (dict(kv_batch_stride=1), 1),
     (dict(kv_head_stride=1024 * 128 + 4, kv_batch_stride=2 * (1024 * 128 + 4)), 1), (dict(in_dtype=7), 1),
     (dict(ws_bytes=16), 3), (dict(ws=None), 1), (dict(B=-1), 1)])

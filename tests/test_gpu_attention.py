@@ -54,6 +54,7 @@ CASES = [
     (2, 2, 4, 4, 128, [5000, 4999], 5000),         # MHA (G=1)
     (1, 4, 32, 8, 128, [64], 64),                  # exactly one tile
     (1, 4, 32, 8, 128, [65], 128),                 # one key into the second tile
+    (2, 17, 32, 8, 128, [900, 17], 900),           # gamma 16: 68 rows -> three row groups (32, 32, 4)
 ]
 
 

@@ -65,6 +65,7 @@ CASES = [
     # a window that straddles a slice edge, a prefix of one key
     (4, 32, 8, 128, [1537, 1568, 3112, 33], 3200, 32, 7, 256),
     (2, 64, 8, 128, [3000, 1600], 3000, 16, 5, 300),  # G = 8 x W = 16 window rows on the tensor-core scorer
+    (2, 32, 8, 64, [1500, 900], 1500, 32, 7, 256),    # 128 window rows at head_dim 64 (the mma.sync scorer)
     # windows of <= 8 rows: key sums taken from the logits pass 1 keeps
     (2, 32, 8, 128, [2000, 700], 2000, 2, 3, 128),
     (2, 8, 2, 64, [900, 400], 900, 2, 1, 64),
