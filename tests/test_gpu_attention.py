@@ -212,6 +212,30 @@ def test_draft_full_size_sampled(name):
         assert_lse_close(lse[b:b + 1, h * G:(h + 1) * G], ref_lse[:, 0])
 
 
+def test_verify_five_rows_split_units():
+    """The batch-128 x 32k verify shape (gamma 4: 20 rows per KV head, three n8 row tiles, every
+    sequence split into units with an in-kernel merge) at batch 64 x 16k (2.1 GB of KV), sampled
+    pairs against the oracle.  Also the small case the verify kernel's counters are captured on."""
+    dev = gpu_or_skip()
+    c = dict(wl.WORKLOADS["b128_ctx32k"], B=64, lens=16384)
+    kv_len = wl.lengths(c)
+    k, v = wl.kv_cache(c, dev, kv_len=kv_len)
+    q = wl.queries(c, dev)
+    plan_units = mgd.mgd_verify_workspace_size(c["B"], c["gamma"] + 1, c["Hq"], c["Hkv"], c["D"], 16384)
+    assert plan_units > 256  # split plan: partials in the workspace
+    out, lse = ops.verify_attn(q, k, v, kv_len.to(dev))
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all())
+    G, D = c["Hq"] // c["Hkv"], c["D"]
+    for b, h in _sampled_pairs(kv_len, c["Hkv"], n=4, seed=5):
+        ref, ref_lse = ref_attention(q[b:b + 1, :, h * G:(h + 1) * G], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
+                                     kv_len[b:b + 1], 1.0 / math.sqrt(D))
+        assert_attention_close(out[b:b + 1, :, h * G:(h + 1) * G], ref, "out[b=%d,h=%d]" % (b, h))
+        assert_lse_close(lse[b:b + 1, :, h * G:(h + 1) * G], ref_lse)
+    del k, v
+    torch.cuda.empty_cache()
+
+
 def _torch_attention(q, k, v, L, scale):
     """Float32 torch math on the GPU for one sequence: q [T, Hq, D], k/v [Hkv, L, D] -> [T, Hq, D]."""
     T, Hq, D = q.shape
