@@ -330,7 +330,11 @@ __device__ int draw_in_sub(const Weights &w, int V, DrawShared &sh) {
 // with NR = 1 and 23.8 us with NR = 4 at 32 registers (one wave of 8 CTAs per
 // SM, but four dependent rounds).  The stream uses the default L2 policy, so
 // that the completing CTA's second read of the chosen sub-range finds it in L2.
-template <bool VEC4, int NR>
+// With CLUSTER the CTAs of a row form one thread-block cluster (a row has at
+// most 8 chunks): each warp stores its record into the shared memory of the
+// cluster's first CTA, and after one cluster barrier that CTA draws -- no
+// ticket, no round trip of the records through global memory.
+template <bool VEC4, int NR, bool CLUSTER>
 __global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4) spec_draw_row_kernel(const float *__restrict__ draft,
                                                                          int32_t *__restrict__ draft_tokens,
                                                                          const float *__restrict__ u, StatParams sp,
@@ -401,20 +405,26 @@ __global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4) spec_draw_row_k
       l = l * ex2((m - mu) * kLog2e) + l2 * ex2((m2 - mu) * kLog2e);
       m = mn;
     }
-    if (lane == 0 && g < sp.nsub) sub_b[g] = make_float2(m, l);
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    if (CLUSTER) {
+      if (lane == 0 && g < sp.nsub) st_cluster_f2(&s_rec[g], 0u, make_float2(m, l));
+      cluster_sync_all();  // every record is in the first CTA's shared memory
+      if (s != 0) return;  // (nothing reads the other CTAs' shared memory after the barrier)
+    } else {
+      if (lane == 0 && g < sp.nsub) sub_b[g] = make_float2(m, l);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = (atomicAdd(&tickets[b], 1u) == static_cast<unsigned>(sp.nsplit - 1)) ? 1 : 0;
+      }
+      __syncthreads();
+      if (!s_last) return;
       __threadfence();
-      s_last = (atomicAdd(&tickets[b], 1u) == static_cast<unsigned>(sp.nsplit - 1)) ? 1 : 0;
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
   }
   // this CTA completed the sequence: the sub-range records (one read, into shared memory when
   // they fit), weights relative to the row max, then the draw
-  const bool rec_smem = sp.nsub <= kRecSmem;
-  if (rec_smem) {
+  const bool rec_smem = CLUSTER || sp.nsub <= kRecSmem;
+  if (!CLUSTER && rec_smem) {
     for (int q = threadIdx.x; q < sp.nsub; q += kStatThreads) s_rec[q] = __ldcg(&sub_b[q]);
     __syncthreads();
   }
@@ -438,7 +448,7 @@ __global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4) spec_draw_row_k
   }
   if (threadIdx.x == 0) {
     draft_tokens[static_cast<size_t>(b) * sp.gamma + row] = tok;
-    tickets[b] = 0u;  // left clean for the next call on this workspace
+    if (!CLUSTER) tickets[b] = 0u;  // left clean for the next call on this workspace
     call_check_in(hdr, sp.B, b, 0u, 0u);
   }
 }
@@ -657,18 +667,25 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   const dim3 grid(p.B, p.nsplit);
   // the round counts that keep every CTA of the grid resident at once when the grid is small
   const long long ctas = static_cast<long long>(p.B) * p.nsplit, sms = current_sm_count();
-  static const int occ_draw1 = ctas_per_sm(reinterpret_cast<const void *>(spec_draw_row_kernel<true, 1>));
+  static const int occ_draw1 = ctas_per_sm(reinterpret_cast<const void *>(spec_draw_row_kernel<true, 1, false>));
   static const int occ_decide2 = ctas_per_sm(reinterpret_cast<const void *>(spec_decide_kernel<true, 2>));
   if (a.mode == 1) {  // draft draws: one launch per drawn row
     const bool one = ctas <= occ_draw1 * sms;
-    auto kd = vec4 ? (one ? spec_draw_row_kernel<true, 1> : spec_draw_row_kernel<true, 2>)
-                   : (one ? spec_draw_row_kernel<false, 1> : spec_draw_row_kernel<false, 2>);
+    // a row of at most 8 chunks (vocab up to 131072) draws inside one cluster
+    const bool cl = p.nsplit <= 8;
+    auto kd = cl ? (vec4 ? (one ? spec_draw_row_kernel<true, 1, true> : spec_draw_row_kernel<true, 2, true>)
+                         : (one ? spec_draw_row_kernel<false, 1, true> : spec_draw_row_kernel<false, 2, true>))
+                 : (vec4 ? (one ? spec_draw_row_kernel<true, 1, false> : spec_draw_row_kernel<true, 2, false>)
+                         : (one ? spec_draw_row_kernel<false, 1, false> : spec_draw_row_kernel<false, 2, false>));
     const int r0 = a.row < 0 ? 0 : a.row, r1 = a.row < 0 ? p.gamma : a.row + 1;
     for (int r = r0; r < r1; ++r) {
       sp.r_begin = p.gamma + 1 + r;
       sp.nr = 1;
-      const cudaError_t e = launch_pdl(kd, grid, dim3(kStatThreads), 0, a.stream, a.draft, a.draft_tokens, a.u, sp,
-                                       sub, tickets, hdr);
+      const cudaError_t e =
+          cl ? launch_pdl_cluster(kd, grid, dim3(kStatThreads), dim3(1, p.nsplit, 1), 0, a.stream, a.draft,
+                                  a.draft_tokens, a.u, sp, sub, tickets, hdr)
+             : launch_pdl(kd, grid, dim3(kStatThreads), 0, a.stream, a.draft, a.draft_tokens, a.u, sp, sub, tickets,
+                          hdr);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
