@@ -469,8 +469,10 @@ __device__ __forceinline__ void merge_row(const float2 *st, int nsplit, float &M
 // rounds (all loads of a round in flight): NR = 2 (32 entries of each row in
 // flight, 3 CTAs per SM) when the grid fits in one wave of that, else NR = 8
 // (8 of each row, held to 32 registers so that 8 CTAs share an SM: a batch of
-// 128 sequences at vocab 128256 runs as one wave of 1024 CTAs).
-template <bool VEC4, int NR>
+// 128 sequences at vocab 128256 runs as one wave of 1024 CTAs).  With CLUSTER
+// the CTAs of a sequence form one thread-block cluster and hand their sums to
+// the first CTA's shared memory, which draws after one cluster barrier.
+template <bool VEC4, int NR, bool CLUSTER>
 __global__ void __launch_bounds__(kStatThreads, NR == 2 ? 3 : (NR == 4 ? 4 : 8)) spec_decide_kernel(const float *__restrict__ target,
                                                                        const float *__restrict__ draft,
                                                                        const int32_t *__restrict__ draft_tokens,
@@ -577,20 +579,26 @@ __global__ void __launch_bounds__(kStatThreads, NR == 2 ? 3 : (NR == 4 ? 4 : 8))
     }
     r = warp_sum_xor(r, 1, 16);
     pp = warp_sum_xor(pp, 1, 16);
-    if (lane == 0 && sg < sp.nsub) sub_b[sg] = make_float2(r, pp);
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    if (CLUSTER) {
+      if (lane == 0 && sg < sp.nsub) st_cluster_f2(&s_rec[sg], 0u, make_float2(r, pp));
+      cluster_sync_all();  // every sum is in the first CTA's shared memory
+      if (s != 0) return;  // (nothing reads the other CTAs' shared memory after the barrier)
+    } else {
+      if (lane == 0 && sg < sp.nsub) sub_b[sg] = make_float2(r, pp);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = (atomicAdd(&tickets[b], 1u) == static_cast<unsigned>(sp.nsplit - 1)) ? 1 : 0;
+      }
+      __syncthreads();
+      if (!s_last) return;
       __threadfence();
-      s_last = (atomicAdd(&tickets[b], 1u) == static_cast<unsigned>(sp.nsplit - 1)) ? 1 : 0;
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
   }
   // this CTA completed the sequence: the sub-range sums (one read, into shared memory when
   // they fit), then the draw of the correction (or bonus) token
-  const bool rec_smem = sp.nsub <= kRecSmem;
-  if (rec_smem) {
+  const bool rec_smem = CLUSTER || sp.nsub <= kRecSmem;
+  if (!CLUSTER && rec_smem) {
     for (int q = threadIdx.x; q < sp.nsub; q += kStatThreads) s_rec[q] = __ldcg(&sub_b[q]);
     __syncthreads();
   }
@@ -618,7 +626,7 @@ __global__ void __launch_bounds__(kStatThreads, NR == 2 ? 3 : (NR == 4 ? 4 : 8))
     for (int i = j + 1; i <= g; ++i) o[i] = -1;
     num_accepted[b] = j;
     if (j < g && s_bad[j]) raise_error_sr(hdr, 0x4u);
-    tickets[b] = 0u;
+    if (!CLUSTER) tickets[b] = 0u;
     call_check_in(hdr, sp.B, b, 0u, 0u);
   }
 }
@@ -668,7 +676,7 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   // the round counts that keep every CTA of the grid resident at once when the grid is small
   const long long ctas = static_cast<long long>(p.B) * p.nsplit, sms = current_sm_count();
   static const int occ_draw1 = ctas_per_sm(reinterpret_cast<const void *>(spec_draw_row_kernel<true, 1, false>));
-  static const int occ_decide2 = ctas_per_sm(reinterpret_cast<const void *>(spec_decide_kernel<true, 2>));
+  static const int occ_decide2 = ctas_per_sm(reinterpret_cast<const void *>(spec_decide_kernel<true, 2, false>));
   if (a.mode == 1) {  // draft draws: one launch per drawn row
     const bool one = ctas <= occ_draw1 * sms;
     // a row of at most 8 chunks (vocab up to 131072) draws inside one cluster
@@ -697,8 +705,14 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
                              a.stream, a.target, a.draft, sp, stats);
   if (e != cudaSuccess) return e;
   const bool wide = ctas <= occ_decide2 * sms;
-  auto kc = vec4 ? (wide ? spec_decide_kernel<true, 2> : spec_decide_kernel<true, 8>)
-                 : (wide ? spec_decide_kernel<false, 2> : spec_decide_kernel<false, 8>);
+  const bool cl = p.nsplit <= 8;  // a sequence of at most 8 chunks decides inside one cluster
+  auto kc = cl ? (vec4 ? (wide ? spec_decide_kernel<true, 2, true> : spec_decide_kernel<true, 8, true>)
+                       : (wide ? spec_decide_kernel<false, 2, true> : spec_decide_kernel<false, 8, true>))
+               : (vec4 ? (wide ? spec_decide_kernel<true, 2, false> : spec_decide_kernel<true, 8, false>)
+                       : (wide ? spec_decide_kernel<false, 2, false> : spec_decide_kernel<false, 8, false>));
+  if (cl)
+    return launch_pdl_cluster(kc, grid, dim3(kStatThreads), dim3(1, p.nsplit, 1), 0, a.stream, a.target, a.draft,
+                              a.draft_tokens, a.u, sp, stats, sub, tickets, a.out_tokens, a.num_accepted, hdr);
   return launch_pdl(kc, grid, dim3(kStatThreads), 0, a.stream,
                     a.target, a.draft, a.draft_tokens, a.u, sp, stats, sub, tickets, a.out_tokens, a.num_accepted,
                     hdr);
