@@ -40,6 +40,7 @@ CASES = [
     ("masked_vocab_b64", "b32_ctx8k", dict(B=64, V=32000, mask_frac=0.6), 6),
     ("gamma1_b40", "b32_ctx8k", dict(B=40, V=5000, gamma=1), 7),
     ("gamma16_b24", "b32_ctx8k", dict(B=24, V=5000, gamma=16), 8),
+    ("qwen_vocab_b48", "b32_ctx8k", dict(B=48, V=152064), 9),
 ]
 
 

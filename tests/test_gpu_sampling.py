@@ -122,6 +122,17 @@ def test_gamma_extremes(case, gamma, B, seed):
     _compare_round(t, d, u, dev, case=case)
 
 
+def test_vocab_over_eight_chunks():
+    """Vocabulary 152064 (the Qwen2.5 models' of the MagicDec notes' model ablation): ten
+    16384-entry chunks per row, more than one thread-block cluster takes, so the draw and the
+    decision kernel hand their sub-range records over through the workspace tickets."""
+    dev = gpu_or_skip()
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=48, V=152064)
+    t, d = wl.logits(c, "cpu", seed=9)
+    u = wl.uniforms(c, "cpu", seed=9)
+    _compare_round(t, d, u, dev, case="qwen_vocab_b48")
+
+
 def test_single_row_draft_draw():
     dev = gpu_or_skip()
     c = wl.WORKLOADS["b32_ctx8k"]
