@@ -138,14 +138,14 @@ int current_sm_count() {
 }
 
 int encode_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Hkv, int kv_cap, int D,
-                         int64_t batch_stride, int64_t head_stride) {
+                         int64_t batch_stride, int64_t head_stride, unsigned box_rows) {
   EncodeFn fn = encode_fn();
   if (!fn) return -1;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(kv_cap),
                               static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(head_stride) * 2,
                                  static_cast<cuuint64_t>(batch_stride) * 2};
-  const cuuint32_t box[4] = {64, 64, 1, 1};
+  const cuuint32_t box[4] = {64, box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -309,9 +309,13 @@ static mgd_status run_snapkv(const void *q_win, const void *k, const void *v, co
     CUtensorMap km, qm;
     if (encode_kv_tensor_map(&km, k, B, Hkv, kv_cap, D, kv_batch_stride, kv_head_stride) != 0)
       return fail(MGD_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    // the tcgen05 scorer loads a 128-key tile as two 128-row boxes (its own map); the others
+    // take 64-row boxes
+    CUtensorMap km128;
     const bool tc05 = snap_tc05_eligible(plan) && sm_scale > 0.f &&
-                      encode_qwin_tensor_map(&qm, q_win, B, W, Hq, D, Hq / Hkv) == 0;
-    e = launch_snapkv(plan, a, 0, &km, tc05 ? &qm : nullptr);
+                      encode_qwin_tensor_map(&qm, q_win, B, W, Hq, D, Hq / Hkv) == 0 &&
+                      encode_kv_tensor_map(&km128, k, B, Hkv, kv_cap, D, kv_batch_stride, kv_head_stride, 128) == 0;
+    e = launch_snapkv(plan, a, 0, tc05 ? &km128 : &km, tc05 ? &qm : nullptr);
   } else {
     e = launch_snapkv(plan, a, 1, nullptr, nullptr);
   }

@@ -97,9 +97,10 @@ size_t simt_attention_ws_bytes();
 cudaError_t launch_attention_simt(const AttnPlan &p, const AttnArgs &a, int in_f32);
 
 // Encode a 4-D bf16 tensor map over a KV tensor [B, Hkv, kv_cap, D] with
-// 64x64 boxes and 128-byte swizzling.  Returns a CUDA driver status.
+// boxes of 64 columns x box_rows rows and 128-byte swizzling.  Returns a CUDA
+// driver status.
 int encode_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Hkv, int kv_cap, int D,
-                         int64_t batch_stride, int64_t head_stride);
+                         int64_t batch_stride, int64_t head_stride, unsigned box_rows = 64);
 
 // ------------------------------------------------------------------ SnapKV
 // Keys per job of the one-read tcgen05 scorer (12 tiles of 128 keys): small

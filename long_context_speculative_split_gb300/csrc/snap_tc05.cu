@@ -362,10 +362,8 @@ __global__ void __launch_bounds__(kT5Threads, kT5CtasPerSm)
           mbar_arrive_expect_tx(&full[stage], kT5TileBytes);
           unsigned char *st = smem + T5Layout::off_k + stage * kT5TileBytes;
           const int key0 = jb.start + i * kT5Keys;
-          for (int h = 0; h < 2; ++h)
-            for (int kh = 0; kh < 2; ++kh)
-              tma_load_4d_hint(st + h * kT5Half + kh * 8192, &kmap, &full[stage], 64 * h, key0 + 64 * kh, jb.hkv,
-                               jb.b, pass1 ? keep : drop);
+          for (int h = 0; h < 2; ++h)  // two boxes of 64 columns x 128 keys (16 KB each)
+            tma_load_4d_hint(st + h * kT5Half, &kmap, &full[stage], 64 * h, key0, jb.hkv, jb.b, pass1 ? keep : drop);
           ++issued;
           if (++stage == kT5Stages) {
             stage = 0;
