@@ -266,7 +266,8 @@ class Workload:
         self.bytes_snap = float((Hkv * L * D * esz).sum() + 4 * Hkv * Keff.sum() * D * esz)
         # window scores: two contractions of W*G rows x D per key (pass 1 over all L keys, pass 2 over L - W)
         self.flops_snap = float((2 * self.W * (Hq // Hkv) * D * Hkv * (2 * L - self.W)).sum())
-        self.bytes_spec = float(B * (2 * self.gamma + 1) * self.V * 4)
+        # rejection sample: the gamma + 1 target rows (the draft rows' normalisers come from the draws)
+        self.bytes_spec = float(B * (self.gamma + 1) * self.V * 4)
         # SnapKV (one-read scorer + select), gamma x (draft attention + one-row draw), verify,
         # rejection sample (statistics and finish)
         self.launches_per_step = 2 + self.gamma * 1 + self.gamma * 1 + 1 + 2
@@ -289,7 +290,7 @@ class Workload:
         if ev:
             ev[3].record()
         ops.rejection_sample(self.t, self.d, self.tok, self.u, ws=self.ws_spec, out_tokens=self.out_tok,
-                             num_accepted=self.nacc)
+                             num_accepted=self.nacc, reuse_draft_stats=True)
         if ev:
             ev[4].record()
 

@@ -64,8 +64,9 @@ typedef enum {
 typedef enum { MGD_BF16 = 0, MGD_F32 = 1 } mgd_dtype;
 
 typedef enum {
-  MGD_VERIFY = 0,      /* accept / reject a whole speculation round */
-  MGD_DRAW_DRAFT = 1   /* draw draft tokens from the draft distributions */
+  MGD_VERIFY = 0,        /* accept / reject a whole speculation round */
+  MGD_DRAW_DRAFT = 1,    /* draw draft tokens from the draft distributions */
+  MGD_VERIFY_DRAWN = 2   /* MGD_VERIFY reusing the draft rows' normalisers left by this round's draws */
 } mgd_sample_mode;
 
 /* Bits of the device error word (see mgd_workspace_errors). */
@@ -76,6 +77,9 @@ typedef enum {
 #define MGD_DEVERR_COMMIT   0x10u  /* mgd_commit_round: num_accepted, kv_len or draft_len out of range */
 #define MGD_DEVERR_STALE_WS 0x20u  /* a call found its workspace header not ready (not zero-filled, or last
                                       used by another kind of call); its outputs are unspecified */
+#define MGD_DEVERR_NOT_DRAWN 0x40u /* MGD_VERIFY_DRAWN: a sequence's gamma draft rows were not all drawn on
+                                      this workspace since its last rejection sample; its outputs are
+                                      unspecified */
 
 const char *mgd_status_string(mgd_status s);
 /* Detail text of the last non-OK status returned on the calling thread ("" if none). */
@@ -241,17 +245,17 @@ mgd_status mgd_snapkv_select_budgets(const void *q_win, const void *k, const voi
  * dropped; when all are accepted one more token is drawn from the target.
  * The paragraph after it states that this preserves the target distribution.
  *
- *   target_logits [B, gamma+1, V] float32 (MGD_VERIFY only; may be NULL otherwise)
+ *   target_logits [B, gamma+1, V] float32 (verify modes only; may be NULL otherwise)
  *   draft_logits  [B, gamma, V]   float32
- *   draft_tokens  [B, gamma] int32: written by MGD_DRAW_DRAFT, read by MGD_VERIFY
+ *   draft_tokens  [B, gamma] int32: written by MGD_DRAW_DRAFT, read by the verify modes
  *   u             [B, gamma+1, 3] float32 in [0,1): slot 0 draws the draft
  *                 token of position i, slot 1 is the acceptance test, slot 2
  *                 the correction draw; position gamma uses slot 2 only (bonus)
  *   row           MGD_DRAW_DRAFT: draw only position `row` (0 <= row < gamma),
- *                 or every position when row < 0.  Ignored by MGD_VERIFY.
- *   out_tokens    [B, gamma+1] int32 (MGD_VERIFY): accepted drafts, then the
+ *                 or every position when row < 0.  Ignored by the verify modes.
+ *   out_tokens    [B, gamma+1] int32 (verify modes): accepted drafts, then the
  *                 correction or bonus token, then -1
- *   num_accepted  [B] int32 (MGD_VERIFY)
+ *   num_accepted  [B] int32 (verify modes)
  *
  * p = softmax(target logits), q = softmax(draft logits), temperature 1.
  * Accept position i iff u[b,i,1] * q_i(x_i) < p_i(x_i).  A draw from weights r
@@ -260,6 +264,19 @@ mgd_status mgd_snapkv_select_budgets(const void *q_win, const void *k, const voi
  * zero (rounding only) falls back to p.  Arithmetic in float32.
  * Supported: 1 <= gamma <= 16; 1 <= V < 2^31.
  * ------------------------------------------------------------------------ */
+/*
+ * Modes.  MGD_DRAW_DRAFT draws position `row` (or every position) of
+ * draft_tokens and leaves the drawn rows' softmax statistics (max and sum of
+ * exp per 16384-entry chunk) in the workspace.  MGD_VERIFY computes the
+ * statistics of all 2*gamma+1 rows itself.  MGD_VERIFY_DRAWN computes only the
+ * gamma+1 target rows' and takes the gamma draft rows' from the workspace: it
+ * is for a round whose draft rows were all drawn with MGD_DRAW_DRAFT on this
+ * workspace, from these draft_logits, since the workspace's last rejection
+ * sample (each rejection sample, in either mode, forgets the draws).  A
+ * sequence for which that does not hold raises MGD_DEVERR_NOT_DRAWN and gets
+ * unspecified outputs.  Both verify modes take the same decisions up to
+ * float32 rounding of the normalisers.
+ */
 size_t mgd_spec_workspace_size(int B, int gamma, int V);
 mgd_status mgd_spec_sample(const float *target_logits, const float *draft_logits,
                            int32_t *draft_tokens, const float *u, int B, int gamma, int V,
@@ -364,7 +381,7 @@ mgd_status mgd_commit_round(const int32_t *num_accepted, int B, int gamma, int H
  * memory.  The call allocates nothing.
  *   - Limit: the scratch it needs, mgd_spec_workspace_size(B, gamma, V), must
  *     fit in MGD_NOALLOC_SCRATCH_BYTES (about B * ((2*gamma+1) * ceil(V/16384) * 8
- *     + ceil(V/2048) * 8 + 4) + 512 bytes; e.g. B <= 966 at gamma = 4,
+ *     + ceil(V/2048) * 8 + 8) + 768 bytes; e.g. B <= 963 at gamma = 4,
  *     V = 128256); larger requests return MGD_ERR_UNSUPPORTED with an
  *     explanation in mgd_last_error().
  *   - Every call looks up the array's device address on the current device

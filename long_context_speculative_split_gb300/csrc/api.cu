@@ -391,17 +391,19 @@ mgd_status mgd_spec_sample(const float *target_logits, const float *draft_logits
   if (B < 0) return fail(MGD_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
   if (gamma < 1 || gamma > 16) return fail(MGD_ERR_UNSUPPORTED, "gamma must be in [1, 16] (got %d)", gamma);
   if (V < 1) return fail(MGD_ERR_INVALID_ARG, "V must be >= 1 (got %d)", V);
-  if (mode != MGD_VERIFY && mode != MGD_DRAW_DRAFT) return fail(MGD_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (mode != MGD_VERIFY && mode != MGD_DRAW_DRAFT && mode != MGD_VERIFY_DRAWN)
+    return fail(MGD_ERR_INVALID_ARG, "bad mode %d", mode);
   if (mode == MGD_DRAW_DRAFT && row >= gamma) return fail(MGD_ERR_INVALID_ARG, "row %d >= gamma %d", row, gamma);
   if (B == 0) return ok();
   if (!draft_logits || !draft_tokens || !u || !ws) return fail(MGD_ERR_INVALID_ARG, "null pointer argument");
-  if (mode == MGD_VERIFY && (!target_logits || !out_tokens || !num_accepted))
-    return fail(MGD_ERR_INVALID_ARG, "MGD_VERIFY needs target_logits, out_tokens and num_accepted");
+  const bool verify = mode != MGD_DRAW_DRAFT;
+  if (verify && (!target_logits || !out_tokens || !num_accepted))
+    return fail(MGD_ERR_INVALID_ARG, "MGD_VERIFY and MGD_VERIFY_DRAWN need target_logits, out_tokens and num_accepted");
   if (!aligned16(ws)) return fail(MGD_ERR_INVALID_ARG, "ws must be 16-byte aligned");
   const SpecPlan plan = plan_spec(B, gamma, V);
   if (ws_bytes < plan.ws_bytes) return fail(MGD_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, plan.ws_bytes);
   SpecArgs a;
-  a.target = (mode == MGD_VERIFY) ? target_logits : nullptr;
+  a.target = verify ? target_logits : nullptr;
   a.draft = draft_logits;
   a.draft_tokens = draft_tokens;
   a.u = u;

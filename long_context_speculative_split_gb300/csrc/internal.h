@@ -167,7 +167,7 @@ struct SpecPlan {
   int nsplit;    // ceil(V / split)
   int nsub;      // ceil(V / 2048): sub-ranges of a row (one warp each)
   int nrows;     // 2*gamma + 1 rows per sequence (gamma+1 target, gamma draft)
-  size_t off_tickets, off_stats, off_sub, ws_bytes;
+  size_t off_tickets, off_drawn, off_stats, off_sub, ws_bytes;
 };
 SpecPlan plan_spec(int B, int gamma, int V);
 

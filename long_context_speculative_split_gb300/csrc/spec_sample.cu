@@ -18,9 +18,14 @@
 //   spec_draw_row: a draft step's draw of one draft row per sequence.  Every
 //     warp streams one sub-range and records its (max, sum of exp); the CTA
 //     completing a sequence (atomic ticket) merges the sub-range records and
-//     draws.  One launch.
+//     draws.  Each CTA also leaves its chunk's (max, sum of exp) of the row
+//     in the workspace, and the drawing CTA marks the row as drawn, so that
+//     the round's rejection sample need not stream the draft rows again.
+//     One launch.
 //   spec_stats + spec_decide: rejection sampling.  spec_stats computes
-//     (max, sum of exp) of each 16384-entry slice of every logit row;
+//     (max, sum of exp) of each 16384-entry slice of every target row, and of
+//     every draft row unless the draws of the round left theirs
+//     (MGD_VERIFY_DRAWN: the decision kernel checks the marks and clears them);
 //     spec_decide runs over (sequence, 16384-entry chunk): every CTA of a
 //     sequence merges the row statistics and takes the same acceptance
 //     decisions (u * q(x) < p(x) for each candidate, the chain keeps the prefix
@@ -46,6 +51,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct StatParams {
   int B, gamma, V, split, nsplit, nrows, nsub;
   int r_begin, nr;  // rows [r_begin, r_begin + nr) of every sequence (unified row index)
+  int reuse;        // rejection sample: the draft rows' statistics come from this round's draws
 };
 
 // unified row r of sequence b: r <= gamma -> target row r, else draft row r - gamma - 1
@@ -335,12 +341,11 @@ __device__ int draw_in_sub(const Weights &w, int V, DrawShared &sh) {
 // cluster's first CTA, and after one cluster barrier that CTA draws -- no
 // ticket, no round trip of the records through global memory.
 template <bool VEC4, int NR, bool CLUSTER>
-__global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4) spec_draw_row_kernel(const float *__restrict__ draft,
-                                                                         int32_t *__restrict__ draft_tokens,
-                                                                         const float *__restrict__ u, StatParams sp,
-                                                                         float2 *__restrict__ sub,
-                                                                         unsigned *__restrict__ tickets,
-                                                                         WsHeader *hdr) {
+__global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4)
+    spec_draw_row_kernel(const float *__restrict__ draft, int32_t *__restrict__ draft_tokens,
+                         const float *__restrict__ u, StatParams sp, float2 *__restrict__ stats,
+                         float2 *__restrict__ sub, unsigned *__restrict__ tickets, unsigned *__restrict__ drawn,
+                         WsHeader *hdr) {
   pdl_launch_dependents();
   {  // warm L2 with this CTA's 64 KB of the row while the previous kernel finishes (prefetch only)
     const float *x0 = draft + (static_cast<size_t>(blockIdx.x) * sp.gamma + (sp.r_begin - sp.gamma - 1)) * sp.V;
@@ -353,6 +358,7 @@ __global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4) spec_draw_row_k
   __shared__ float s_M;
   __shared__ DrawShared sh;
   __shared__ float2 s_rec[kRecSmem];
+  __shared__ float2 s_wst[kWarps];  // the warps' (max, sum), merged into the chunk's statistics
   const int b = blockIdx.x, s = blockIdx.y;
   const int row = sp.r_begin - sp.gamma - 1;  // draft position
   const int V = sp.V;
@@ -405,13 +411,25 @@ __global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4) spec_draw_row_k
       l = l * ex2((m - mu) * kLog2e) + l2 * ex2((m2 - mu) * kLog2e);
       m = mn;
     }
+    if (lane == 0) s_wst[warp] = make_float2(m, l);
+    // the chunk's (max, sum of exp) of this draft row, kept for the round's rejection sample
+    auto put_chunk_stats = [&] {
+      float M = -INFINITY;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_wst[w].x);
+      const float Mu = (M == -INFINITY) ? 0.f : M;
+      float Lt = 0.f;
+      for (int w = 0; w < kWarps; ++w) Lt += s_wst[w].y * exp2f((s_wst[w].x - Mu) * kLog2e);
+      stats[(static_cast<size_t>(b) * sp.nrows + sp.r_begin) * sp.nsplit + s] = make_float2(M, Lt);
+    };
     if (CLUSTER) {
       if (lane == 0 && g < sp.nsub) st_cluster_f2(&s_rec[g], 0u, make_float2(m, l));
       cluster_sync_all();  // every record is in the first CTA's shared memory
+      if (threadIdx.x == 32) put_chunk_stats();  // (warp 0 goes on to the pick meanwhile)
       if (s != 0) return;  // (nothing reads the other CTAs' shared memory after the barrier)
     } else {
       if (lane == 0 && g < sp.nsub) sub_b[g] = make_float2(m, l);
       __syncthreads();
+      if (threadIdx.x == 32) put_chunk_stats();
       if (threadIdx.x == 0) {
         __threadfence();
         s_last = (atomicAdd(&tickets[b], 1u) == static_cast<unsigned>(sp.nsplit - 1)) ? 1 : 0;
@@ -449,6 +467,7 @@ __global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4) spec_draw_row_k
   if (threadIdx.x == 0) {
     draft_tokens[static_cast<size_t>(b) * sp.gamma + row] = tok;
     if (!CLUSTER) tickets[b] = 0u;  // left clean for the next call on this workspace
+    atomicOr(&drawn[b], 1u << row);  // this row's statistics are in place
     call_check_in(hdr, sp.B, b, 0u, 0u);
   }
 }
@@ -480,6 +499,7 @@ __global__ void __launch_bounds__(kStatThreads, NR == 2 ? 3 : (NR == 4 ? 4 : 8))
                                                                        const float2 *__restrict__ stats,
                                                                        float2 *__restrict__ sub,
                                                                        unsigned *__restrict__ tickets,
+                                                                       unsigned *__restrict__ drawn,
                                                                        int32_t *__restrict__ out_tokens,
                                                                        int32_t *__restrict__ num_accepted,
                                                                        WsHeader *hdr) {
@@ -627,6 +647,11 @@ __global__ void __launch_bounds__(kStatThreads, NR == 2 ? 3 : (NR == 4 ? 4 : 8))
     num_accepted[b] = j;
     if (j < g && s_bad[j]) raise_error_sr(hdr, 0x4u);
     if (!CLUSTER) tickets[b] = 0u;
+    // the draws' marks go back to zero with every rejection sample; reusing their statistics
+    // needs all gamma of them
+    const unsigned have = drawn[b];
+    drawn[b] = 0u;
+    if (sp.reuse && have != (1u << g) - 1u) raise_error_sr(hdr, 0x40u);
     call_check_in(hdr, sp.B, b, 0u, 0u);
   }
 }
@@ -643,7 +668,8 @@ SpecPlan plan_spec(int B, int gamma, int V) {
   p.nsub = (V + kSub - 1) / kSub;
   p.nrows = 2 * gamma + 1;
   p.off_tickets = kAlign;
-  p.off_stats = align_up(p.off_tickets + sizeof(unsigned) * static_cast<size_t>(B));
+  p.off_drawn = align_up(p.off_tickets + sizeof(unsigned) * static_cast<size_t>(B));
+  p.off_stats = align_up(p.off_drawn + sizeof(unsigned) * static_cast<size_t>(B));
   p.off_sub = align_up(p.off_stats + sizeof(float2) * static_cast<size_t>(B) * p.nrows * p.nsplit);
   p.ws_bytes = align_up(p.off_sub + sizeof(float2) * static_cast<size_t>(B) * p.nsub);
   return p;
@@ -658,6 +684,7 @@ static int ctas_per_sm(const void *fn) {
 
 cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   StatParams sp;
+  sp.reuse = 0;
   sp.B = p.B;
   sp.gamma = p.gamma;
   sp.V = p.V;
@@ -667,6 +694,7 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
   sp.nsub = p.nsub;
   unsigned char *ws = static_cast<unsigned char *>(a.ws);
   unsigned *tickets = reinterpret_cast<unsigned *>(ws + p.off_tickets);
+  unsigned *drawn = reinterpret_cast<unsigned *>(ws + p.off_drawn);
   float2 *stats = reinterpret_cast<float2 *>(ws + p.off_stats);
   float2 *sub = reinterpret_cast<float2 *>(ws + p.off_sub);
   WsHeader *hdr = static_cast<WsHeader *>(a.ws);
@@ -691,15 +719,18 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
       sp.nr = 1;
       const cudaError_t e =
           cl ? launch_pdl_cluster(kd, grid, dim3(kStatThreads), dim3(1, p.nsplit, 1), 0, a.stream, a.draft,
-                                  a.draft_tokens, a.u, sp, sub, tickets, hdr)
-             : launch_pdl(kd, grid, dim3(kStatThreads), 0, a.stream, a.draft, a.draft_tokens, a.u, sp, sub, tickets,
-                          hdr);
+                                  a.draft_tokens, a.u, sp, stats, sub, tickets, drawn, hdr)
+             : launch_pdl(kd, grid, dim3(kStatThreads), 0, a.stream, a.draft, a.draft_tokens, a.u, sp, stats, sub,
+                          tickets, drawn, hdr);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
   }
+  // MGD_VERIFY_DRAWN: the gamma draft rows' statistics were left by this round's draws, so
+  // only the gamma + 1 target rows are streamed here
+  sp.reuse = a.mode == 2 ? 1 : 0;
   sp.r_begin = 0;
-  sp.nr = p.nrows;
+  sp.nr = sp.reuse ? p.gamma + 1 : p.nrows;
   const dim3 g1(p.B * sp.nr, p.nsplit);
   cudaError_t e = launch_pdl(vec4 ? spec_stats_kernel<true> : spec_stats_kernel<false>, g1, dim3(kStatThreads), 0,
                              a.stream, a.target, a.draft, sp, stats);
@@ -712,10 +743,11 @@ cudaError_t launch_spec(const SpecPlan &p, const SpecArgs &a) {
                        : (wide ? spec_decide_kernel<false, 2, false> : spec_decide_kernel<false, 8, false>));
   if (cl)
     return launch_pdl_cluster(kc, grid, dim3(kStatThreads), dim3(1, p.nsplit, 1), 0, a.stream, a.target, a.draft,
-                              a.draft_tokens, a.u, sp, stats, sub, tickets, a.out_tokens, a.num_accepted, hdr);
+                              a.draft_tokens, a.u, sp, stats, sub, tickets, drawn, a.out_tokens, a.num_accepted,
+                              hdr);
   return launch_pdl(kc, grid, dim3(kStatThreads), 0, a.stream,
-                    a.target, a.draft, a.draft_tokens, a.u, sp, stats, sub, tickets, a.out_tokens, a.num_accepted,
-                    hdr);
+                    a.target, a.draft, a.draft_tokens, a.u, sp, stats, sub, tickets, drawn, a.out_tokens,
+                    a.num_accepted, hdr);
 }
 
 }  // namespace mgd

@@ -16,10 +16,11 @@ LIB_PATH = os.path.join(HERE, "libmgd.so")
 
 MGD_OK, MGD_ERR_INVALID_ARG, MGD_ERR_UNSUPPORTED, MGD_ERR_WORKSPACE, MGD_ERR_CUDA = range(5)
 MGD_BF16, MGD_F32 = 0, 1
-MGD_VERIFY, MGD_DRAW_DRAFT = 0, 1
+MGD_VERIFY, MGD_DRAW_DRAFT, MGD_VERIFY_DRAWN = 0, 1, 2
 MGD_DEVERR_KV_LEN, MGD_DEVERR_SNAP_LEN, MGD_DEVERR_TOKEN, MGD_DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 MGD_DEVERR_COMMIT = 0x10
 MGD_DEVERR_STALE_WS = 0x20
+MGD_DEVERR_NOT_DRAWN = 0x40
 
 _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 

@@ -146,8 +146,10 @@ def draft_draw(draft_logits, u, draft_tokens=None, row=-1, ws=None, stream=None)
 
 
 def rejection_sample(target_logits, draft_logits, draft_tokens, u, ws=None, out_tokens=None, num_accepted=None,
-                     stream=None):
-    """-> (out_tokens [B, gamma+1] int32 (-1 padded), num_accepted [B] int32)."""
+                     stream=None, reuse_draft_stats=False):
+    """-> (out_tokens [B, gamma+1] int32 (-1 padded), num_accepted [B] int32).
+    reuse_draft_stats: take the draft rows' normalisers from the draws this round made with
+    draft_draw on the same `ws` (MGD_VERIFY_DRAWN) instead of streaming those rows again."""
     B, gp1, V = target_logits.shape
     gamma = gp1 - 1
     dev = target_logits.device
@@ -155,10 +157,13 @@ def rejection_sample(target_logits, draft_logits, draft_tokens, u, ws=None, out_
         out_tokens = torch.empty((B, gp1), dtype=torch.int32, device=dev)
     if num_accepted is None:
         num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if reuse_draft_stats and ws is None:
+        raise ValueError("reuse_draft_stats needs the workspace the draws used")
     need = mgd.mgd_spec_workspace_size(B, gamma, V)
     if ws is None:
         ws = workspace(need, dev)
-    mgd.mgd_spec_sample(target_logits, draft_logits, draft_tokens, u, B, gamma, V, mgd.MGD_VERIFY, -1, out_tokens,
+    mode = mgd.MGD_VERIFY_DRAWN if reuse_draft_stats else mgd.MGD_VERIFY
+    mgd.mgd_spec_sample(target_logits, draft_logits, draft_tokens, u, B, gamma, V, mode, -1, out_tokens,
                         num_accepted, ws, ws.numel(), stream)
     return out_tokens, num_accepted
 

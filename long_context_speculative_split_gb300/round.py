@@ -116,7 +116,7 @@ class SpeculationRound:
             ops.verify_attn(self.q[layer], self.k[layer], self.v[layer], self.lengths[layer, 0], ws=self.ws_verify,
                             out=self.vout[layer], lse=self.vlse)
         ops.rejection_sample(self.t, self.d, self.tok, self.u, ws=self.ws_spec, out_tokens=self.out_tok,
-                             num_accepted=self.nacc)
+                             num_accepted=self.nacc, reuse_draft_stats=True)
 
     def commit(self):
         """Commit / rollback of every layer's caches after the round's acceptance decisions."""

@@ -151,10 +151,12 @@ def test_spec_sample_rejects_bad_arguments_on_host(lib):
             return e.status
     assert call(gamma=0) == 2 and call(gamma=17) == 2
     assert call(V=0) == 1
-    assert call(mode=5) == 1
+    assert call(mode=5) == 1 and call(mode=3) == 1
     assert call(mode=1, row=3) == 1
     assert call(target_logits=None) == 1          # verify needs the target
     assert call(out_tokens=None) == 1
+    assert call(mode=2, target_logits=None) == 1  # so does the verify that reuses the draws' statistics
+    assert call(mode=2, num_accepted=None) == 1
     assert call(ws_bytes=8) == 3
     assert call(B=0, draft_logits=None) == 0
 

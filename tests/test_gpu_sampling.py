@@ -32,26 +32,36 @@ with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "sa
 FRACTION_SLACK = 0.02
 
 
-def _compare_round(t, d, u, dev, case=None, min_frac=0.75):
+def _compare_round(t, d, u, dev, case=None, min_frac=0.75, reuse=False):
     """Compare one round with the oracle; returns (num_accepted, fully compared fraction).
     With `case`, the fraction must equal the oracle-only value stored for that case
-    (within FRACTION_SLACK); otherwise it must reach `min_frac`."""
+    (within FRACTION_SLACK); otherwise it must reach `min_frac`.  With `reuse`, the draws
+    and the rejection sample share one workspace and the rejection sample takes the draft
+    rows' normalisers from the draws (MGD_VERIFY_DRAWN)."""
     B, gp1, V = t.shape
     gamma = gp1 - 1
     # outputs between poisoned guard regions (checked after each call)
     g = dict(draft_tokens=Guarded((B, gamma), torch.int32, dev), out_tokens=Guarded((B, gp1), torch.int32, dev),
              num_accepted=Guarded((B,), torch.int32, dev))
-    tok = ops.draft_draw(d.to(dev), u.to(dev), draft_tokens=g["draft_tokens"].t)
+    ws = ops.workspace(mgd.mgd_spec_workspace_size(B, gamma, V), dev) if reuse else None
+    if reuse:  # one draft position per call, as a round's draft steps make them
+        for s in range(gamma):
+            ops.draft_draw(d.to(dev), u.to(dev), draft_tokens=g["draft_tokens"].t, row=s, ws=ws)
+        tok = g["draft_tokens"].t
+    else:
+        tok = ops.draft_draw(d.to(dev), u.to(dev), draft_tokens=g["draft_tokens"].t)
     rtok, rmarg = ref_draw(d, u)
     tok_c = tok.cpu().numpy()
     ok_draw = rmarg >= SAMPLE_BAND
     assert np.array_equal(tok_c[ok_draw], rtok[ok_draw])
     # the verify step reads the oracle's draft tokens, on both sides (no GPU output is an oracle input)
     rtok_d = torch.from_numpy(np.ascontiguousarray(rtok, dtype=np.int32)).to(dev)
-    out, nacc = ops.rejection_sample(t.to(dev), d.to(dev), rtok_d, u.to(dev), out_tokens=g["out_tokens"].t,
-                                     num_accepted=g["num_accepted"].t)
+    out, nacc = ops.rejection_sample(t.to(dev), d.to(dev), rtok_d, u.to(dev), ws=ws, out_tokens=g["out_tokens"].t,
+                                     num_accepted=g["num_accepted"].t, reuse_draft_stats=reuse)
     torch.cuda.synchronize()
     check_guards(**g)
+    if reuse:
+        assert mgd.mgd_workspace_errors(ws) == 0
     tok_c = rtok
     ref = ref_reject(t, d, rtok, u)
     out_c, nacc_c = out.cpu().numpy(), nacc.cpu().numpy()
@@ -83,14 +93,47 @@ def _compare_round(t, d, u, dev, case=None, min_frac=0.75):
     return nacc_c, frac
 
 
+@pytest.mark.parametrize("reuse", [False, True], ids=["own_stats", "draws_stats"])
 @pytest.mark.parametrize("name", ["tiny_b2", "b32_ctx8k", "b128_ctx32k", "ragged_b256_ctx4k_64k"])
-def test_round_matches_oracle(name):
-    """Every configuration's round (the ragged one: batch 256, gamma 2, vocab 128256)."""
+def test_round_matches_oracle(name, reuse):
+    """Every configuration's round (the ragged one: batch 256, gamma 2, vocab 128256), with the
+    rejection sample computing every row's statistics, and taking the draft rows' from the draws."""
     dev = gpu_or_skip()
     c = wl.WORKLOADS[name]
     t, d = wl.logits(c, "cpu")
     u = wl.uniforms(c, "cpu")
-    _compare_round(t, d, u, dev, case=name)
+    _compare_round(t, d, u, dev, case=name, reuse=reuse)
+
+
+def test_reuse_without_draws_raises_device_flag():
+    """MGD_VERIFY_DRAWN on a workspace whose draft rows were not all drawn raises
+    MGD_DEVERR_NOT_DRAWN; a rejection sample forgets the draws, so the next round must draw
+    again; a complete round afterwards raises nothing."""
+    dev = gpu_or_skip()
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=8, V=5000)
+    t, d = wl.logits(c, dev, seed=12)
+    u = wl.uniforms(c, dev, seed=12)
+    B, g, V = c["B"], c["gamma"], c["V"]
+    ws = ops.workspace(mgd.mgd_spec_workspace_size(B, g, V), dev)
+    tok = ops.draft_draw(d, u)  # drawn on another workspace
+    ops.rejection_sample(t, d, tok, u, ws=ws, reuse_draft_stats=True)
+    assert mgd.mgd_workspace_errors(ws) & mgd.MGD_DEVERR_NOT_DRAWN
+    for s in range(g - 1):  # one position short
+        ops.draft_draw(d, u, draft_tokens=tok, row=s, ws=ws)
+    ops.rejection_sample(t, d, tok, u, ws=ws, reuse_draft_stats=True)
+    assert mgd.mgd_workspace_errors(ws) & mgd.MGD_DEVERR_NOT_DRAWN
+    ops.draft_draw(d, u, draft_tokens=tok, ws=ws)  # every position
+    ops.rejection_sample(t, d, tok, u, ws=ws)  # the verify that computes its own statistics forgets them too
+    assert mgd.mgd_workspace_errors(ws) == 0
+    ops.rejection_sample(t, d, tok, u, ws=ws, reuse_draft_stats=True)
+    assert mgd.mgd_workspace_errors(ws) & mgd.MGD_DEVERR_NOT_DRAWN
+    ops.draft_draw(d, u, draft_tokens=tok, ws=ws)
+    out, nacc = ops.rejection_sample(t, d, tok, u, ws=ws, reuse_draft_stats=True)
+    assert mgd.mgd_workspace_errors(ws) == 0
+    out_ref, nacc_ref = ops.rejection_sample(t, d, tok, u)
+    torch.cuda.synchronize()
+    # the two verify modes differ only in the rounding of the draft normalisers
+    assert (nacc == nacc_ref).float().mean().item() >= 0.75
 
 
 def test_odd_vocab_and_many_sequences():

@@ -38,6 +38,17 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         assert torch.equal(tok, tok_ref)
         assert torch.equal(nacc, nacc_ref)
         assert torch.equal(out, out_ref)
+        # the verify that reuses the draws' statistics, after draws into the same scratch
+        ws = ops.workspace(mgd.mgd_spec_workspace_size(B, g, V), dev)
+        ops.draft_draw(d, u, draft_tokens=tok_ref, ws=ws)
+        out_ref, nacc_ref = ops.rejection_sample(t, d, tok_ref, u, ws=ws, reuse_draft_stats=True)
+        mgd.mgd_spec_sample_noalloc(None, d, tok, u, B, g, V, mgd.MGD_DRAW_DRAFT, -1, None, None)
+        mgd.mgd_spec_sample_noalloc(t, d, tok, u, B, g, V, mgd.MGD_VERIFY_DRAWN, -1, out, nacc)
+        torch.cuda.synchronize()
+        assert mgd.mgd_workspace_errors(ws) == 0
+        assert torch.equal(tok, tok_ref)
+        assert torch.equal(nacc, nacc_ref)
+        assert torch.equal(out, out_ref)
 
 
 def test_noalloc_refuses_requests_beyond_its_array():
