@@ -108,8 +108,8 @@ int encode_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Hkv, int
 // until their pass 2 re-reads them, large enough that the per-job exchange
 // stays a small share of the job (measured: 1280 / 1536 / 1792 / 2048 keys).
 // Capacities above kSnapMaxSlices * kSnapSliceKeys keys get longer slices, so
-// that a pair never has more slices than CTAs are resident (the scorer's
-// waits for the other slices of a pair rely on that).
+// that a pair never has more than 64 slices (a CTA keeps the slices of a pair
+// it holds in a 64-bit mask).
 constexpr int kSnapSliceKeys = 1536;
 constexpr int kSnapMaxSlices = 64;
 
