@@ -136,15 +136,17 @@ def test_reuse_without_draws_raises_device_flag():
     assert (nacc == nacc_ref).float().mean().item() >= 0.75
 
 
-def test_odd_vocab_and_many_sequences():
+@pytest.mark.parametrize("reuse", [False, True], ids=["own_stats", "draws_stats"])
+def test_odd_vocab_and_many_sequences(reuse):
     dev = gpu_or_skip()
     c = dict(wl.WORKLOADS["b32_ctx8k"], B=300, V=4099, gamma=5, sigma=2.0, sigma_n=1.0)
     t, d = wl.logits(c, "cpu", seed=4)
     u = wl.uniforms(c, "cpu", seed=4)
-    _compare_round(t, d, u, dev, case="odd_vocab_b300")
+    _compare_round(t, d, u, dev, case="odd_vocab_b300", reuse=reuse)
 
 
-def test_masked_vocabulary():
+@pytest.mark.parametrize("reuse", [False, True], ids=["own_stats", "draws_stats"])
+def test_masked_vocabulary(reuse):
     """60 % of each sequence's vocabulary at -inf in every row, and 2 % more in the target rows
     only: masked entries weigh nothing, a drafted token the target forbids is always rejected."""
     dev = gpu_or_skip()
@@ -152,20 +154,22 @@ def test_masked_vocabulary():
     t, d = wl.logits(c, "cpu", seed=6)
     u = wl.uniforms(c, "cpu", seed=6)
     assert bool(torch.isinf(t).any()) and bool(torch.isinf(d).any())
-    _compare_round(t, d, u, dev, case="masked_vocab_b64")
+    _compare_round(t, d, u, dev, case="masked_vocab_b64", reuse=reuse)
 
 
+@pytest.mark.parametrize("reuse", [False, True], ids=["own_stats", "draws_stats"])
 @pytest.mark.parametrize("case,gamma,B,seed", [("gamma1_b40", 1, 40, 7), ("gamma16_b24", 16, 24, 8)])
-def test_gamma_extremes(case, gamma, B, seed):
+def test_gamma_extremes(case, gamma, B, seed, reuse):
     """One draft position, and the largest number the library takes (16: 33 rows per sequence)."""
     dev = gpu_or_skip()
     c = dict(wl.WORKLOADS["b32_ctx8k"], B=B, V=5000, gamma=gamma)
     t, d = wl.logits(c, "cpu", seed=seed)
     u = wl.uniforms(c, "cpu", seed=seed)
-    _compare_round(t, d, u, dev, case=case)
+    _compare_round(t, d, u, dev, case=case, reuse=reuse)
 
 
-def test_vocab_over_eight_chunks():
+@pytest.mark.parametrize("reuse", [False, True], ids=["own_stats", "draws_stats"])
+def test_vocab_over_eight_chunks(reuse):
     """Vocabulary 152064 (the Qwen2.5 models' of the MagicDec notes' model ablation): ten
     16384-entry chunks per row, more than one thread-block cluster takes, so the draw and the
     decision kernel hand their sub-range records over through the workspace tickets."""
@@ -173,7 +177,7 @@ def test_vocab_over_eight_chunks():
     c = dict(wl.WORKLOADS["b32_ctx8k"], B=48, V=152064)
     t, d = wl.logits(c, "cpu", seed=9)
     u = wl.uniforms(c, "cpu", seed=9)
-    _compare_round(t, d, u, dev, case="qwen_vocab_b48")
+    _compare_round(t, d, u, dev, case="qwen_vocab_b48", reuse=reuse)
 
 
 def test_single_row_draft_draw():
