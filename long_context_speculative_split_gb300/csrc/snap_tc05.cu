@@ -72,9 +72,7 @@ constexpr int kExchThread = 64;             // first softmax thread: segment bro
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRing = 8;                    // segment messages in flight between the producer and its consumers
 
-// Instruction descriptor of tcgen05.mma kind::f16: D f32, A and B bf16, both
-// K-major, M = 128, N = 128.
-constexpr uint32_t kIdescM128N128 = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescM128N128 = umma_idesc_bf16(128, 128);
 
 // Segment kinds.  Flags: kFirst -- the first segment of a pair (the MMA thread
 // waits for the pair's window rows); kLast -- the last (it then releases them).
@@ -100,33 +98,6 @@ struct T5Params {
   float sl2;
   size_t off_cnt, off_part, off_scores;
 };
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
-// groups 1024 bytes apart (the layout of a 64-column TMA box).
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1u) << 16;          // leading byte offset (unused for this layout)
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;  // stride byte offset
-  d |= static_cast<uint64_t>(1u) << 46;          // descriptor version
-  d |= static_cast<uint64_t>(2u) << 61;          // 128-byte swizzle
-  return d;
-}
-
-__device__ __forceinline__ void umma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
