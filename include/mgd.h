@@ -153,8 +153,14 @@ mgd_status mgd_selftest_occupy(int ctas, int smem_bytes, int usec, void *stream)
  * Query head h reads KV head h / (Hq/Hkv).  Row t sits at position
  * kv_len[b]-T+t and attends to keys 0 .. kv_len[b]-T+t (causal among the
  * appended rows); scores are sm_scale * <q, k>; softmax and accumulation in
- * float32.  Supported: D in {64, 128}; 1 <= T <= 17 (gamma <= 16, as the sampling and
- * commit calls take); Hq % Hkv == 0.
+ * float32.  The probabilities enter the P V product (bf16 path) as bf16 hi + lo
+ * parts, about 16 significant bits; when a KV head has more than 16 query rows
+ * (Hq/Hkv * T > 16, e.g. G = 4 and T >= 5) as float16 with V converted to
+ * float16 instead (11 significant bits, output rel-L2 about 1e-4 against exact
+ * arithmetic): there V entries must lie within the float16 range, |v| <= 65504,
+ * or the outputs that read them are not finite.  Supported: D in {64, 128};
+ * 1 <= T <= 17 (gamma <= 16, as the sampling and commit calls take);
+ * Hq % Hkv == 0.
  * in_dtype MGD_BF16 runs the tensor-core split-KV kernel; MGD_F32 runs a
  * float32 CUDA-core kernel (for float32 inputs; not the timed path).
  * ------------------------------------------------------------------------ */

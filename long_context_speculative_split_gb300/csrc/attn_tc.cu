@@ -20,7 +20,14 @@
 //     S^T = K Q^T with mma.m16n8k16 (keys on the M side, so G*T rows pad only
 //     to a multiple of 8), an online softmax in the exp2 domain, and
 //     O^T += V^T P^T where P is split into bf16 hi + lo parts (two mmas) so
-//     the probabilities keep ~16 significant bits;
+//     the probabilities keep ~16 significant bits -- or, with three or more
+//     n8 row tiles (more than 16 query rows a KV head, as verify at G = 4 and
+//     gamma >= 4), one mma in float16: there the mma work per tile is what
+//     holds the kernel below the HBM stream (measured at batch 128 x 32k,
+//     T = 5: 2.61 ms, 2.39 ms with the QK^T mmas left out, 2.42 ms with the
+//     P V ones left out), and P in float16 (11 significant bits for values in
+//     [2^-14, 1]) with V converted from bf16 (exact within the float16 range)
+//     halves the P V work: 2.51 ms, output rel-L2 1.5e-4 against float64;
 //   * at the end of a unit the 4 warps merge in shared memory; a unit that
 //     covers the whole sequence writes the final output, otherwise it writes
 //     a partial (O, lse) and the CTA that completes the last chunk of that
@@ -220,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const int gid = lane >> 2;
   const int tig = lane & 3;
   constexpr int MT = D / 16;  // m16 tiles over D (PV) == k16 steps over D (QK)
+  constexpr bool kF16PV = NT >= 3;  // P V in one float16 mma (see the header)
 
   float acc[MT][NT][4];
   float m_run[NT][2], l_run[NT][2];
@@ -348,6 +356,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
           const int d = 16 * mt + 8 * ((lane >> 3) & 1);
           ldsm_x4_t(vbase + (d >> 6) * kBoxBytes + swz128(vr, (d & 63) >> 3), va[mt][0], va[mt][1], va[mt][2],
                     va[mt][3]);
+          if constexpr (kF16PV) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) va[mt][c] = bf16x2_to_f16x2(va[mt][c]);
+          }
         }
       }
       __syncwarp();
@@ -389,21 +401,30 @@ __global__ void __launch_bounds__(kThreads, MINB)
           acc[mt][j][2] = y.x;
           acc[mt][j][3] = y.y;
         }
-        uint32_t h0, l0, h1, l1;
-        split_bf16(s[j][0], s[j][1], h0, l0);  // keys gid,   rows 2tig, 2tig+1
-        split_bf16(s[j][2], s[j][3], h1, l1);  // keys gid+8, rows 2tig, 2tig+1
-        phi[j][0] = movmatrix_t(h0);
-        phi[j][1] = movmatrix_t(h1);
-        plo[j][0] = movmatrix_t(l0);
-        plo[j][1] = movmatrix_t(l1);
+        if constexpr (kF16PV) {
+          phi[j][0] = movmatrix_t(pack_f16(s[j][0], s[j][1]));  // keys gid,   rows 2tig, 2tig+1
+          phi[j][1] = movmatrix_t(pack_f16(s[j][2], s[j][3]));  // keys gid+8, rows 2tig, 2tig+1
+        } else {
+          uint32_t h0, l0, h1, l1;
+          split_bf16(s[j][0], s[j][1], h0, l0);  // keys gid,   rows 2tig, 2tig+1
+          split_bf16(s[j][2], s[j][3], h1, l1);  // keys gid+8, rows 2tig, 2tig+1
+          phi[j][0] = movmatrix_t(h0);
+          phi[j][1] = movmatrix_t(h1);
+          plo[j][0] = movmatrix_t(l0);
+          plo[j][1] = movmatrix_t(l1);
+        }
       }
       // ---- O^T[D][rows] += V^T P^T
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          mma_bf16_16816(acc[mt][j], va[mt][0], va[mt][1], va[mt][2], va[mt][3], phi[j][0], phi[j][1]);
-          mma_bf16_16816(acc[mt][j], va[mt][0], va[mt][1], va[mt][2], va[mt][3], plo[j][0], plo[j][1]);
+          if constexpr (kF16PV) {
+            mma_f16_16816(acc[mt][j], va[mt][0], va[mt][1], va[mt][2], va[mt][3], phi[j][0], phi[j][1]);
+          } else {
+            mma_bf16_16816(acc[mt][j], va[mt][0], va[mt][1], va[mt][2], va[mt][3], phi[j][0], phi[j][1]);
+            mma_bf16_16816(acc[mt][j], va[mt][0], va[mt][1], va[mt][2], va[mt][3], plo[j][0], plo[j][1]);
+          }
         }
       }
     }
