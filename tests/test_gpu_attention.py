@@ -89,6 +89,25 @@ def test_verify_split_units_and_merges_match_oracle(B, T, Hq, Hkv):
     assert_lse_close(lse, ref_lse)
 
 
+@pytest.mark.parametrize("vmax", [1e-3, 6.0e4], ids=["tiny_V", "V_near_f16_max"])
+def test_verify_many_rows_across_the_float16_range_of_v(vmax):
+    """With more than 16 query rows a KV head the P V product runs in float16: V entries of
+    any magnitude the header allows (down to the float16 subnormals, up to 60000 of the
+    65504 limit) still meet the tolerance, relative to the largest |V|."""
+    dev = gpu_or_skip()
+    B, T, Hq, Hkv, D, lens, cap = 2, 5, 32, 8, 128, [3000, 777], 3000
+    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=41)
+    v = (v.float() * (vmax / v.float().abs().max())).to(torch.bfloat16)
+    out, _ = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev))
+    torch.cuda.synchronize()
+    ref, _ = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(D))
+    g = to64(out)
+    assert np.all(np.isfinite(g))
+    scale = float(v.float().abs().max())
+    assert np.abs(g - ref).max() <= 2e-2 * scale / 4.0
+    assert np.linalg.norm(g - ref) / np.linalg.norm(ref) <= 1e-3
+
+
 def test_verify_bf16_output_dtype():
     dev = gpu_or_skip()
     q, k, v, kv_len = _case(2, 4, 32, 8, 128, [900, 333], 900, seed=5)
