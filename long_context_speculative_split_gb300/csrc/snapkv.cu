@@ -23,6 +23,8 @@
 //   snap_score_simt      the same two passes on CUDA cores (float32 inputs);
 //   snap_select          max-pool, 3-pass radix select of the K_eff-W-th
 //                        largest pooled score, ordered compaction, gather.
+// The 128-row bf16 windows at D = 128 (W = 32, G = 4) are scored instead by the
+// one-read tcgen05 kernel of snap_tc05.cu (both passes in one launch).
 #include <algorithm>
 
 #include "common.cuh"

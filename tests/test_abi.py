@@ -42,6 +42,24 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in mgd.SIGNATURES, "binding misses " + name
 
 
+def test_binding_constants_match_the_header():
+    """Every enum value and device error bit the header defines has the same value in the
+    binding (the names the Python side passes and tests against)."""
+    from long_context_speculative_split_gb300 import mgd
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    consts = {name: int(val, 0) for name, val in re.findall(r"#define\s+(MGD_DEVERR_[A-Z_]+)\s+(0x[0-9a-fA-F]+)u", text)}
+    for body in re.findall(r"typedef enum \{(.*?)\}", text, flags=re.S):
+        consts.update({name: int(val) for name, val in re.findall(r"(MGD_[A-Z0-9_]+)\s*=\s*(\d+)", body)})
+    assert "MGD_VERIFY_DRAWN" in consts and "MGD_DEVERR_NOT_DRAWN" in consts
+    for name, val in consts.items():
+        if hasattr(mgd, name):
+            assert getattr(mgd, name) == val, name
+    for name in ("MGD_VERIFY", "MGD_DRAW_DRAFT", "MGD_VERIFY_DRAWN", "MGD_DEVERR_KV_LEN", "MGD_DEVERR_SNAP_LEN",
+                 "MGD_DEVERR_TOKEN", "MGD_DEVERR_TIMEOUT", "MGD_DEVERR_COMMIT", "MGD_DEVERR_STALE_WS",
+                 "MGD_DEVERR_NOT_DRAWN"):
+        assert getattr(mgd, name) == consts[name], name
+
+
 def test_status_strings_and_version(lib):
     from long_context_speculative_split_gb300 import mgd
     for s in range(5):
