@@ -592,7 +592,9 @@ def run_ours(args):
         e_ms, h2d, d2h = run_e2e(w, max(1, min(args.steps, 5)), 1)
         e_ms = max_over_ranks(e_ms, world, dev)
         e2e = {"value": world * tokens / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
+               # host-to-device bytes over the whole step time: the step is bound by this link
+               "h2d_gbs_over_step": h2d / (e_ms / 1e3) / 1e9}
     traffic = load_traffic(args.workload)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
