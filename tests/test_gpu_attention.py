@@ -108,6 +108,52 @@ def test_verify_many_rows_across_the_float16_range_of_v(vmax):
     assert np.linalg.norm(g - ref) / np.linalg.norm(ref) <= 1e-3
 
 
+def _nonfinite_cells(out):
+    return {tuple(i) for i in torch.nonzero(~torch.isfinite(out.cpu())).tolist()}
+
+
+@pytest.mark.parametrize("B,lens,cap", [(2, [3000, 777], 3000), (40, None, 1000)],
+                         ids=["whole_sequence_units", "split_units_merged"])
+def test_v_beyond_float16_range_is_confined_to_the_outputs_that_read_it(B, lens, cap):
+    """The float16 P V path (G = 4, T = 5: 20 rows a KV head) needs |v| <= 65504.  One V entry
+    past it makes exactly the outputs that sum it non-finite (the G heads of that KV head, that
+    dimension, every verify row), both where a unit covers the whole sequence and where the last
+    CTA merges partials; every other output still matches the oracle."""
+    dev = gpu_or_skip()
+    T, Hq, Hkv, D = 5, 32, 8, 128
+    G = Hq // Hkv
+    if lens is None:
+        g = torch.Generator().manual_seed(3)
+        lens = torch.randint(T, cap + 1, (B,), generator=g).tolist()
+        lens[1] = cap  # four 256-key units on a 152-SM part
+    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=B + 100)
+    b, h, j, d = 1, 3, 2, 7
+    v_bad = v.clone()
+    v_bad[b, h, j, d] = 1.0e5  # a bfloat16 value; float16 tops out at 65504
+    out, _ = ops.verify_attn(q.to(dev), k.to(dev), v_bad.to(dev), kv_len.to(dev))
+    expect = {(b, t, hq, d) for t in range(T) for hq in range(h * G, (h + 1) * G)}
+    assert _nonfinite_cells(out) == expect
+    ref, _ = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(D))
+    keep = torch.ones(out.shape, dtype=torch.bool)
+    keep[b, :, h * G:(h + 1) * G] = False
+    assert_attention_close(out.cpu()[keep], ref[keep.numpy()])
+
+
+def test_v_beyond_float16_range_is_finite_on_the_bfloat16_path():
+    """At 16 or fewer rows a KV head (here T = 4, G = 4) P V stays in bfloat16 hi + lo parts,
+    which hold a V entry of 1e5: the outputs are finite and match the oracle."""
+    dev = gpu_or_skip()
+    B, T, Hq, Hkv, D, lens, cap = 2, 4, 32, 8, 128, [3000, 777], 3000
+    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=104)
+    v[1, 3, 2, 7] = 1.0e5
+    out, _ = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev))
+    ref, _ = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(D))
+    g = to64(out)
+    assert np.all(np.isfinite(g))
+    # error relative to the largest |V| (the P V sum carries it)
+    assert np.abs(g - ref).max() <= 2e-2 * 1.0e5 / 4.0
+
+
 def test_verify_bf16_output_dtype():
     dev = gpu_or_skip()
     q, k, v, kv_len = _case(2, 4, 32, 8, 128, [900, 333], 900, seed=5)
