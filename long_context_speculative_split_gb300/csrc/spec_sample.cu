@@ -330,18 +330,20 @@ __device__ int draw_in_sub(const Weights &w, int V, DrawShared &sh) {
 // and draws.  Each lane streams its 64 entries in NR rounds (all loads of a
 // round in flight) with its own running (max, sum), merged over the warp at
 // the end: NR = 1 (all 64 in flight, 2 CTAs per SM) when the grid fits in two
-// CTAs per SM, else NR = 2 (4 CTAs per SM).  Measured at vocab 128256: batch
-// 32, 256 CTAs, 11 us per draw in a chain of draft steps with NR = 1 against
-// 13 us with NR = 2; batch 128, 1024 CTAs, 18.7 us with NR = 2 against 20.2 us
-// with NR = 1 and 23.8 us with NR = 4 at 32 registers (one wave of 8 CTAs per
-// SM, but four dependent rounds).  The stream uses the default L2 policy, so
+// CTAs per SM, else NR = 2 (5 CTAs per SM at 48 registers).  Measured at vocab
+// 128256: batch 32, 256 CTAs, 11 us per draw in a chain of draft steps with
+// NR = 1 against 13 us with NR = 2; batch 128, 1024 CTAs, 18.7 us with NR = 2
+// at 4 CTAs per SM against 20.2 us with NR = 1 and 23.8 us with NR = 4 at 32
+// registers (one wave of 8 CTAs per SM, but four dependent rounds); 5 CTAs per
+// SM take 0.85 us off each draw of the 4-step draft phase (1.35 waves instead
+// of 1.7), 6 (40 registers, a few spilled) add 4 us.  The stream uses the default L2 policy, so
 // that the completing CTA's second read of the chosen sub-range finds it in L2.
 // With CLUSTER the CTAs of a row form one thread-block cluster (a row has at
 // most 8 chunks): each warp stores its record into the shared memory of the
 // cluster's first CTA, and after one cluster barrier that CTA draws -- no
 // ticket, no round trip of the records through global memory.
 template <bool VEC4, int NR, bool CLUSTER>
-__global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 4)
+__global__ void __launch_bounds__(kStatThreads, NR == 1 ? 2 : 5)
     spec_draw_row_kernel(const float *__restrict__ draft, int32_t *__restrict__ draft_tokens,
                          const float *__restrict__ u, StatParams sp, float2 *__restrict__ stats,
                          float2 *__restrict__ sub, unsigned *__restrict__ tickets, unsigned *__restrict__ drawn,
