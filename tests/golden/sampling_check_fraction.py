@@ -41,6 +41,8 @@ CASES = [
     ("gamma1_b40", "b32_ctx8k", dict(B=40, V=5000, gamma=1), 7),
     ("gamma16_b24", "b32_ctx8k", dict(B=24, V=5000, gamma=16), 8),
     ("qwen_vocab_b48", "b32_ctx8k", dict(B=48, V=152064), 9),
+    ("odd_vocab_five_chunks_b100", "b32_ctx8k", dict(B=100, V=65539), 10),
+    ("odd_vocab_ten_chunks_b50", "b32_ctx8k", dict(B=50, V=147459), 11),
 ]
 
 

@@ -180,6 +180,21 @@ def test_vocab_over_eight_chunks(reuse):
     _compare_round(t, d, u, dev, case="qwen_vocab_b48", reuse=reuse)
 
 
+@pytest.mark.parametrize("case,B,V,seed", [("odd_vocab_five_chunks_b100", 100, 65539, 10),
+                                           ("odd_vocab_ten_chunks_b50", 50, 147459, 11)],
+                         ids=["cluster_rows", "ticket_rows"])
+@pytest.mark.parametrize("reuse", [False, True], ids=["stream_rows", "reuse_draws"])
+def test_unaligned_vocab_in_two_round_draws(case, B, V, seed, reuse):
+    """A vocabulary that is not a multiple of 4 (scalar loads) in grids of 500 CTAs, more than
+    the one-round draw keeps resident on a 152-SM part, so every lane streams its sub-range in
+    two rounds: rows of five chunks draw inside a cluster, rows of ten through the tickets."""
+    dev = gpu_or_skip()
+    c = dict(wl.WORKLOADS["b32_ctx8k"], B=B, V=V)
+    t, d = wl.logits(c, "cpu", seed=seed)
+    u = wl.uniforms(c, "cpu", seed=seed)
+    _compare_round(t, d, u, dev, case=case, reuse=reuse)
+
+
 def test_single_row_draft_draw():
     dev = gpu_or_skip()
     c = wl.WORKLOADS["b32_ctx8k"]
