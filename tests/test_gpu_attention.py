@@ -55,6 +55,9 @@ CASES = [
     (1, 4, 32, 8, 128, [64], 64),                  # exactly one tile
     (1, 4, 32, 8, 128, [65], 128),                 # one key into the second tile
     (2, 17, 32, 8, 128, [900, 17], 900),           # gamma 16: 68 rows -> three row groups (32, 32, 4)
+    (2, 1, 8, 2, 64, [513, 1], 513),               # head_dim 64: one row tile
+    (2, 5, 32, 8, 64, [1000, 333], 1000),          # head_dim 64: 20 rows, P V in float16
+    (1, 8, 16, 4, 64, [2000], 2048),               # head_dim 64: 32 rows (four n8 tiles)
 ]
 
 
@@ -191,14 +194,15 @@ def test_draft_float32_tiny_config_full():
     assert_lse_close(lse, ref_lse[:, 0])
 
 
-@pytest.mark.parametrize("lens,cap", [([1024, 700, 1], 1024), ([516, 512, 64, 65], 516)])
-def test_draft_bf16_matches_oracle(lens, cap):
+@pytest.mark.parametrize("lens,cap,D", [([1024, 700, 1], 1024, 128), ([516, 512, 64, 65], 516, 128),
+                                        ([516, 512, 64, 65], 516, 64)])
+def test_draft_bf16_matches_oracle(lens, cap, D):
     dev = gpu_or_skip()
     B = len(lens)
-    q, k, v, dlen = _case(B, 1, 32, 8, 128, lens, cap, seed=cap, poison_pad=True)
+    q, k, v, dlen = _case(B, 1, 32, 8, D, lens, cap, seed=cap + D, poison_pad=True)
     out, lse = _guarded_attention(lambda **kw: ops.draft_attn(q.to(dev), k.to(dev), v.to(dev), dlen.to(dev), **kw),
-                                  q, B, 0, 32, 128, dev)
-    ref, ref_lse = ref_draft(q, k, v, dlen, 1.0 / math.sqrt(128))
+                                  q, B, 0, 32, D, dev)
+    ref, ref_lse = ref_draft(q, k, v, dlen, 1.0 / math.sqrt(D))
     assert_attention_close(out, ref[:, 0])
     assert_lse_close(lse, ref_lse[:, 0])
 
