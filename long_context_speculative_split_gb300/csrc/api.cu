@@ -104,7 +104,7 @@ mgd_status run_attention(const void *q, const void *k, const void *v, const int3
   if (in_dtype == MGD_F32) {
     if (ws_bytes < simt_attention_ws_bytes())
       return fail(MGD_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, simt_attention_ws_bytes());
-    cudaError_t e = launch_attention_simt(plan, a, 1);
+    cudaError_t e = launch_attention_simt(plan, a);
     return e == cudaSuccess ? ok() : cuda_fail(e, "attention (float32) launch");
   }
   if (ws_bytes < plan.ws_bytes) return fail(MGD_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, plan.ws_bytes);

@@ -1,4 +1,4 @@
-// CUDA-core attention for float32 (or bf16) inputs: the float32 instantiation
+// CUDA-core attention for float32 inputs: the float32 instantiation
 // of the verify / draft pass.  Same definition as the tensor-core kernel
 // (MagicDec notes, section 3.2: verify = decode attention over gamma+1 rows;
 // causal among the appended rows), float32 arithmetic throughout.  One CTA
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 size_t simt_attention_ws_bytes() { return kAlign; }
 
-cudaError_t launch_attention_simt(const AttnPlan &p, const AttnArgs &a, int in_f32) {
+cudaError_t launch_attention_simt(const AttnPlan &p, const AttnArgs &a) {
   cudaError_t e = cudaMemsetAsync(a.ws, 0, kAlign, a.stream);
   if (e != cudaSuccess) return e;
   const float sl2 = a.sm_scale * 1.4426950408889634f;
@@ -134,17 +134,10 @@ cudaError_t launch_attention_simt(const AttnPlan &p, const AttnArgs &a, int in_f
   attn_simt_kernel<TY, DD><<<grid, kWarps * 32, 0, a.stream>>>(                                              \
       static_cast<const TY *>(a.q), static_cast<const TY *>(a.k), static_cast<const TY *>(a.v), a.kv_len, p.T, \
       p.Hq, p.Hkv, p.G, p.kv_cap, a.kv_batch_stride, a.kv_head_stride, sl2, of, ob, a.lse, hdr)
-  if (in_f32) {
-    if (p.D == 128)
-      MGD_SIMT(float, 128);
-    else
-      MGD_SIMT(float, 64);
-  } else {
-    if (p.D == 128)
-      MGD_SIMT(__nv_bfloat16, 128);
-    else
-      MGD_SIMT(__nv_bfloat16, 64);
-  }
+  if (p.D == 128)
+    MGD_SIMT(float, 128);
+  else
+    MGD_SIMT(float, 64);
 #undef MGD_SIMT
   return cudaGetLastError();
 }

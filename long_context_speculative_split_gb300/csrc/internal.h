@@ -94,7 +94,7 @@ cudaError_t launch_attention_tc(const AttnPlan &p, const AttnArgs &a, const CUte
                                 const CUtensorMap &vmap);
 // Any-dtype CUDA-core attention, one CTA per (sequence, KV head).
 size_t simt_attention_ws_bytes();
-cudaError_t launch_attention_simt(const AttnPlan &p, const AttnArgs &a, int in_f32);
+cudaError_t launch_attention_simt(const AttnPlan &p, const AttnArgs &a);
 
 // Encode a 4-D bf16 tensor map over a KV tensor [B, Hkv, kv_cap, D] with
 // boxes of 64 columns x box_rows rows and 128-byte swizzling.  Returns a CUDA

@@ -180,6 +180,23 @@ def test_verify_float32_tiny_config_full():
     assert_lse_close(lse, ref_lse)
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32_out", "bf16_out"])
+def test_verify_float32_head_dim_128(out_dtype):
+    """The float32 CUDA-core kernel at head_dim 128, 20 rows a KV head (three passes of 8 rows),
+    ragged lengths down to kv_len = T + 4, both output types."""
+    dev = gpu_or_skip()
+    B, T, Hq, Hkv, D, lens, cap = 2, 5, 32, 8, 128, [700, 9], 700
+    q, k, v, kv_len = _case(B, T, Hq, Hkv, D, lens, cap, seed=77, dtype=torch.float32)
+    out, lse = ops.verify_attn(q.to(dev), k.to(dev), v.to(dev), kv_len.to(dev), out_dtype=out_dtype)
+    ref, ref_lse = ref_attention(q, k, v, kv_len, 1.0 / math.sqrt(D))
+    if out_dtype == torch.float32:
+        assert_attention_close(out, ref)
+    else:  # bf16 output adds its own rounding (2^-9 relative)
+        g = to64(out)
+        assert np.abs(g - ref).max() <= 2e-2 and np.linalg.norm(g - ref) / np.linalg.norm(ref) <= 5e-3
+    assert_lse_close(lse, ref_lse)
+
+
 def test_draft_float32_tiny_config_full():
     dev = gpu_or_skip()
     c = wl.WORKLOADS["tiny_b2"]
