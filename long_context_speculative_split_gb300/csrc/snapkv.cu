@@ -1037,27 +1037,17 @@ cudaError_t launch_snapkv(const SnapPlan &p, const SnapArgs &a, int in_f32, cons
   kp.off_scores = p.off_scores;
   kp.lrows = p.lrows;
   kp.off_logits = p.off_logits;
-  if (in_f32 || kmap == nullptr) {
+  if (in_f32 || kmap == nullptr) {  // float32 inputs (bf16 calls always come with the K map)
+    if (!in_f32) return cudaErrorInvalidValue;
     const size_t smem = sizeof(float) * p.rows;
-    if (in_f32) {
-      if (p.D == 128)
-        snap_score_simt<float, 128><<<p.pairs, 256, smem, a.stream>>>(
-            static_cast<const float *>(a.q_win), static_cast<const float *>(a.k), a.kv_len, a.kv_batch_stride,
-            a.kv_head_stride, ws, kp);
-      else
-        snap_score_simt<float, 64><<<p.pairs, 256, smem, a.stream>>>(
-            static_cast<const float *>(a.q_win), static_cast<const float *>(a.k), a.kv_len, a.kv_batch_stride,
-            a.kv_head_stride, ws, kp);
-    } else {
-      if (p.D == 128)
-        snap_score_simt<__nv_bfloat16, 128><<<p.pairs, 256, smem, a.stream>>>(
-            static_cast<const __nv_bfloat16 *>(a.q_win), static_cast<const __nv_bfloat16 *>(a.k), a.kv_len,
-            a.kv_batch_stride, a.kv_head_stride, ws, kp);
-      else
-        snap_score_simt<__nv_bfloat16, 64><<<p.pairs, 256, smem, a.stream>>>(
-            static_cast<const __nv_bfloat16 *>(a.q_win), static_cast<const __nv_bfloat16 *>(a.k), a.kv_len,
-            a.kv_batch_stride, a.kv_head_stride, ws, kp);
-    }
+    if (p.D == 128)
+      snap_score_simt<float, 128><<<p.pairs, 256, smem, a.stream>>>(
+          static_cast<const float *>(a.q_win), static_cast<const float *>(a.k), a.kv_len, a.kv_batch_stride,
+          a.kv_head_stride, ws, kp);
+    else
+      snap_score_simt<float, 64><<<p.pairs, 256, smem, a.stream>>>(
+          static_cast<const float *>(a.q_win), static_cast<const float *>(a.k), a.kv_len, a.kv_batch_stride,
+          a.kv_head_stride, ws, kp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   } else if (qmap != nullptr && snap_tc05_eligible(p)) {
