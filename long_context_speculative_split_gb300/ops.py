@@ -17,6 +17,31 @@ def _dtype_code(t):
     raise TypeError("unsupported dtype %s (bfloat16 or float32)" % t.dtype)
 
 
+def _check(device, dense=(), int32=(), f32=(), same=()):
+    """Argument checks the C ABI cannot make on raw pointers: every tensor on `device`; the
+    ones in `dense` packed row-major (the calls take them without strides); `int32` / `f32`
+    of that dtype; `same` a list of tensors that must share one dtype.  Raises before any
+    launch."""
+    named = list(dense) + list(int32) + list(f32) + list(same)
+    for name, t in named:
+        if t is not None and t.device != device:
+            raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    for name, t in dense:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("%s must be contiguous (the C ABI reads it as a packed row-major array)" % name)
+    for name, t in int32:
+        if t is not None and t.dtype != torch.int32:
+            raise TypeError("%s must be int32, got %s" % (name, t.dtype))
+    for name, t in f32:
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("%s must be float32, got %s" % (name, t.dtype))
+    if same:
+        d0 = same[0][1].dtype
+        for name, t in same[1:]:
+            if t.dtype != d0:
+                raise TypeError("%s has dtype %s, expected %s like %s" % (name, t.dtype, d0, same[0][0]))
+
+
 def _kv_strides(k, v, D):
     if k.stride(3) != 1 or k.stride(2) != D or k.stride() != v.stride():
         raise ValueError("K and V must share strides with contiguous rows of D elements")
@@ -39,6 +64,8 @@ def verify_attn(q, k, v, kv_len, sm_scale=None, out_dtype=torch.float32, ws=None
         out = torch.empty((B, T, Hq, D), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+    _check(q.device, dense=[("q", q), ("kv_len", kv_len), ("out", out), ("lse", lse)], int32=[("kv_len", kv_len)],
+           f32=[("lse", lse)], same=[("q", q), ("k", k), ("v", v)])
     need = mgd.mgd_verify_workspace_size(B, T, Hq, Hkv, D, cap)
     if ws is None:
         ws = workspace(need, q.device)
@@ -60,6 +87,8 @@ def draft_attn(q, k_draft, v_draft, draft_len, sm_scale=None, out_dtype=torch.fl
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(q.device, dense=[("q", q), ("draft_len", draft_len), ("out", out), ("lse", lse)],
+           int32=[("draft_len", draft_len)], f32=[("lse", lse)], same=[("q", q), ("k_draft", k_draft), ("v_draft", v_draft)])
     need = mgd.mgd_draft_workspace_size(B, Hq, Hkv, D, cap)
     if ws is None:
         ws = workspace(need, q.device)
@@ -89,6 +118,12 @@ def snapkv_select(q_win, k, v, kv_len, W, pool, K, draft_cap=None, sm_scale=None
                    v_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
                    draft_len=torch.empty((B,), dtype=torch.int32, device=dev),
                    scores=torch.zeros((B, Hkv, cap), dtype=torch.float32, device=dev) if want_scores else None)
+    _check(dev, dense=[("q_win", q_win), ("kv_len", kv_len), ("sel_idx", out["sel_idx"]),
+                       ("draft_len", out["draft_len"]), ("scores", out["scores"]), ("K", K if per_seq else None)],
+           int32=[("kv_len", kv_len), ("sel_idx", out["sel_idx"]), ("draft_len", out["draft_len"]),
+                  ("K", K if per_seq else None)],
+           f32=[("scores", out["scores"])],
+           same=[("q_win", q_win), ("k", k), ("v", v), ("k_draft", out["k_draft"]), ("v_draft", out["v_draft"])])
     need = mgd.mgd_snapkv_workspace_size(B, Hq, Hkv, D, cap, W)
     if ws is None:
         ws = workspace(need, dev)
@@ -123,6 +158,11 @@ def topk_draft_attn(q, k, v, kv_len, K, draft_cap=None, sm_scale=None, out_dtype
                    k_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
                    v_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
                    draft_len=torch.empty((B,), dtype=torch.int32, device=dev))
+    _check(dev, dense=[("q", q), ("kv_len", kv_len), ("out", out["out"]), ("lse", out["lse"]), ("sel_idx", out["sel_idx"]),
+                       ("draft_len", out["draft_len"])],
+           int32=[("kv_len", kv_len), ("sel_idx", out["sel_idx"]), ("draft_len", out["draft_len"])],
+           f32=[("lse", out["lse"])],
+           same=[("q", q), ("k", k), ("v", v), ("k_draft", out["k_draft"]), ("v_draft", out["v_draft"])])
     need = mgd.mgd_topk_draft_workspace_size(B, Hq, Hkv, D, cap, cap_d)
     if ws is None:
         ws = workspace(need, dev)
@@ -137,6 +177,8 @@ def draft_draw(draft_logits, u, draft_tokens=None, row=-1, ws=None, stream=None)
     B, gamma, V = draft_logits.shape
     if draft_tokens is None:
         draft_tokens = torch.full((B, gamma), -1, dtype=torch.int32, device=draft_logits.device)
+    _check(draft_logits.device, dense=[("draft_logits", draft_logits), ("u", u), ("draft_tokens", draft_tokens)],
+           int32=[("draft_tokens", draft_tokens)], f32=[("draft_logits", draft_logits), ("u", u)])
     need = mgd.mgd_spec_workspace_size(B, gamma, V)
     if ws is None:
         ws = workspace(need, draft_logits.device)
@@ -159,6 +201,10 @@ def rejection_sample(target_logits, draft_logits, draft_tokens, u, ws=None, out_
         num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
     if reuse_draft_stats and ws is None:
         raise ValueError("reuse_draft_stats needs the workspace the draws used")
+    _check(dev, dense=[("target_logits", target_logits), ("draft_logits", draft_logits), ("draft_tokens", draft_tokens),
+                       ("u", u), ("out_tokens", out_tokens), ("num_accepted", num_accepted)],
+           int32=[("draft_tokens", draft_tokens), ("out_tokens", out_tokens), ("num_accepted", num_accepted)],
+           f32=[("target_logits", target_logits), ("draft_logits", draft_logits), ("u", u)])
     need = mgd.mgd_spec_workspace_size(B, gamma, V)
     if ws is None:
         ws = workspace(need, dev)
@@ -174,6 +220,9 @@ def commit_round(num_accepted, gamma, kv_len, k, v, k_draft, v_draft, draft_len,
     if k_draft.stride(3) != 1 or k_draft.stride(2) != D or k_draft.stride() != v_draft.stride():
         raise ValueError("draft K and V must share strides with contiguous rows of D elements")
     sb, sh = _kv_strides(k, v, D)
+    _check(k.device, dense=[("num_accepted", num_accepted), ("kv_len", kv_len), ("draft_len", draft_len)],
+           int32=[("num_accepted", num_accepted), ("kv_len", kv_len), ("draft_len", draft_len)],
+           same=[("k", k), ("v", v), ("k_draft", k_draft), ("v_draft", v_draft)])
     if ws is None:
         ws = workspace(mgd.mgd_commit_workspace_size(B), k.device)
     mgd.mgd_commit_round(num_accepted, B, gamma, Hkv, D, _dtype_code(k), kv_len, k, v, cap, sb, sh, k_draft,
@@ -193,6 +242,9 @@ def streaming_select(k, v, kv_len, sink, K, draft_cap=None, out=None, stream=Non
                    k_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
                    v_draft=torch.zeros((B, Hkv, cap_d, D), dtype=k.dtype, device=dev),
                    draft_len=torch.empty((B,), dtype=torch.int32, device=dev))
+    _check(dev, dense=[("kv_len", kv_len), ("sel_idx", out["sel_idx"]), ("draft_len", out["draft_len"])],
+           int32=[("kv_len", kv_len), ("sel_idx", out["sel_idx"]), ("draft_len", out["draft_len"])],
+           same=[("k", k), ("v", v), ("k_draft", out["k_draft"]), ("v_draft", out["v_draft"])])
     mgd.mgd_streaming_select(k, v, kv_len, B, Hkv, D, cap, sb, sh, sink, K, _dtype_code(k), out["sel_idx"],
                              out["k_draft"], out["v_draft"], cap_d, out["draft_len"], stream)
     return out
